@@ -1,0 +1,245 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct CPU reference for the layout-folding
+ * hot path.  TEST INFRASTRUCTURE ONLY: nothing on the product path may link,
+ * load or call this file; only the test-suite, the smoke check and the bench's
+ * CPU-baseline leg do.  It shares no code with the CUDA library.
+ *
+ * Arithmetic is fp64 over inputs widened exactly from bf16 (or fp32), with
+ * every reduction summed sequentially in its natural index order.  OpenMP only
+ * distributes independent output rows over cores; it never changes the order of
+ * any sum.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [P1] "Strength reduction: fold transpose into a subsequent GEMM call"
+ *       (lightning-thunder issue 1252) -- the Feature program and its trace.
+ *  [P2] "Feature request: Schedule a small matmul op as a reduction (or
+ *       pointwise) op" (NVIDIA/Fuser issue 3646) -- the T19 matmul and its
+ *       broadcast/mul/squeeze rewrite.
+ *  [P4] "Allow reductions in matmul epilogues" (NVIDIA/Fuser issue 2213) --
+ *       the fused matmul + cross-entropy fusion definition.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 -> fp64, exact: a bf16 value is the top 16 bits of an IEEE binary32. */
+static double bf16_to_f64(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* fp32 -> bf16 with round-to-nearest, ties to even (the IEEE default rounding
+ * applied to an 8-bit significand).  NaN stays a quiet NaN. */
+static uint16_t f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+uint16_t oracle_bf16_round(float f) { return f32_to_bf16_rne(f); }
+
+/*
+ * NT GEMM [P1, Feature: `torch.matmul(x, weight.t())`, and the "so-called NT
+ * GEMM" remark]:  out[m,n] = sum_k X[m,k] * W[n,k], with X [M,K] and W [N,K]
+ * both row-major (K contiguous).  The weight is read in its stored layout.
+ */
+void oracle_gemm_nt(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N,
+                    int64_t K, double *out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *xr = x + m * K;
+        for (int64_t n = 0; n < N; ++n) {
+            const uint16_t *wr = w + n * K;
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += bf16_to_f64(xr[k]) * bf16_to_f64(wr[k]);
+            out[m * N + n] = acc;
+        }
+    }
+}
+
+/* Same definition restricted to a list of rows of X (for shapes whose full
+ * product is too slow here): out[r,n] = sum_k X[rows[r],k] * W[n,k]. */
+void oracle_gemm_nt_rows(const uint16_t *x, const uint16_t *w, const int64_t *rows,
+                         int64_t R, int64_t N, int64_t K, double *out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < R; ++r) {
+        const uint16_t *xr = x + rows[r] * K;
+        for (int64_t n = 0; n < N; ++n) {
+            const uint16_t *wr = w + n * K;
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += bf16_to_f64(xr[k]) * bf16_to_f64(wr[k]);
+            out[r * N + n] = acc;
+        }
+    }
+}
+
+/* The materialised transpose that the traced program runs as its own fusion
+ * [P1, trace: `prims.transpose(weight, (1, 0))`]:  wt[k,n] = W[n,k]. */
+void oracle_transpose_bf16(const uint16_t *w, int64_t N, int64_t K, uint16_t *wt)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            wt[k * N + n] = w[n * K + k];
+}
+
+/* The GEMM the trace then runs on the transposed copy [P1, trace:
+ * `prims.matmul(t7, t)`]:  out[m,n] = sum_k X[m,k] * Wt[k,n], Wt [K,N]. */
+void oracle_gemm_nn(const uint16_t *x, const uint16_t *wt, int64_t M, int64_t N,
+                    int64_t K, double *out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *xr = x + m * K;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += bf16_to_f64(xr[k]) * bf16_to_f64(wt[k * N + n]);
+            out[m * N + n] = acc;
+        }
+    }
+}
+
+/*
+ * Row-wise cross-entropy over logits z [M,N] (fp64) [P4, fusion example]:
+ *   mx   = max_n z[m,n]                      ("allreduce log sum exp in N")
+ *   e    = exp(z - mx),  sumexp = sum_n e
+ *   lse  = log(sumexp) + mx
+ *   loss = lse - z[m, L[m]]                  (the "xent = lse - y_i*onehot(L)_i"
+ *                                             comment; see the reading below)
+ *   grad = e / sumexp - onehot(L)            ("yhatminusy")
+ * Reading: the example's code sums (lse - where(onehot, z, 0)) over N, which
+ * would give N*lse - z_L; its comment and the standard cross-entropy give
+ * lse - z_L, and only that form gives ln N for equal logits, so it is taken.
+ * A label outside [0,N) makes that row's loss NaN (the page defines no
+ * ignore-index); its grad row is then the softmax alone.
+ * lse_or_null / grad_or_null may be NULL.
+ */
+void oracle_xent_logits(const double *z, const int32_t *labels, int64_t M, int64_t N,
+                        double *loss, double *lse_or_null, double *grad_or_null)
+{
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t m = 0; m < M; ++m) {
+        const double *zr = z + m * N;
+        double mx = -INFINITY;
+        for (int64_t n = 0; n < N; ++n)
+            if (zr[n] > mx)
+                mx = zr[n];
+        double sumexp = 0.0;
+        for (int64_t n = 0; n < N; ++n)
+            sumexp += exp(zr[n] - mx);
+        double lse = log(sumexp) + mx;
+        int64_t L = labels[m];
+        int valid = (L >= 0 && L < N);
+        loss[m] = valid ? lse - zr[L] : NAN;
+        if (lse_or_null)
+            lse_or_null[m] = lse;
+        if (grad_or_null) {
+            double *g = grad_or_null + m * N;
+            for (int64_t n = 0; n < N; ++n)
+                g[n] = exp(zr[n] - mx) / sumexp - ((valid && n == L) ? 1.0 : 0.0);
+        }
+    }
+}
+
+/*
+ * Brute-force cross-entropy on small inputs: loss = -log(exp(z_L) / sum_n exp(z_n))
+ * in long double, with no max subtraction (the textbook definition the fused
+ * form must reproduce).  Only meaningful while exp(z) stays in range.
+ */
+void oracle_xent_bruteforce(const double *z, const int32_t *labels, int64_t M, int64_t N,
+                            double *loss)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        const double *zr = z + m * N;
+        long double den = 0.0L;
+        for (int64_t n = 0; n < N; ++n)
+            den += expl((long double)zr[n]);
+        int64_t L = labels[m];
+        if (L < 0 || L >= N) {
+            loss[m] = NAN;
+            continue;
+        }
+        long double p = expl((long double)zr[L]) / den;
+        loss[m] = (double)(-logl(p));
+    }
+}
+
+/* GEMM + cross-entropy from bf16 inputs: z = X W^T (oracle_gemm_nt) followed
+ * by oracle_xent_logits, for a list of rows of X.  z_or_null receives the fp64
+ * logits [R,N] if given; the caller owns every buffer. */
+void oracle_xent_rows(const uint16_t *x, const uint16_t *w, const int32_t *labels,
+                      const int64_t *rows, int64_t R, int64_t N, int64_t K,
+                      double *z, double *loss, double *lse_or_null, double *grad_or_null)
+{
+    oracle_gemm_nt_rows(x, w, rows, R, N, K, z);
+    /* labels are indexed by the original row */
+    int32_t lab_small[1];
+    for (int64_t r = 0; r < R; ++r) {
+        lab_small[0] = labels[rows[r]];
+        oracle_xent_logits(z + r * N, lab_small, 1, N, loss + r,
+                           lse_or_null ? lse_or_null + r : NULL,
+                           grad_or_null ? grad_or_null + r * N : NULL);
+    }
+}
+
+/*
+ * K=1 matmul as broadcast-multiply-squeeze [P2, the T19 matmul of a [64,1]
+ * and a [1,4096] operand and its proposed rewrite broadcast(T15) *
+ * broadcast(T18), squeezed]:  out[i,j] = a[i] * b[j], one fp32 multiply
+ * (the single rounding of the exact product), no accumulation.
+ */
+void oracle_matmul_k1(const float *a, const float *b, int64_t M, int64_t N, float *out)
+{
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double p = (double)a[i] * (double)b[j];  /* exact in fp64 */
+            out[i * N + j] = (float)p;               /* one rounding to fp32 */
+        }
+}
+
+/* The same product for bf16 operands of a K=1 NT GEMM: X [M,1], W [N,1],
+ * out[i,j] = bf16_rn(x[i] * w[j]) -- the bf16 x bf16 product is exact in fp64
+ * (and in fp32), so this is the single rounding of the exact result. */
+void oracle_matmul_k1_bf16(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N,
+                           uint16_t *out)
+{
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double p = bf16_to_f64(x[i]) * bf16_to_f64(w[j]);
+            out[i * N + j] = f32_to_bf16_rne((float)p);
+        }
+}
