@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the layout-folding hot path on GB300.
+
+Headline line (one JSON line on rank 0): TFLOP/s of ``gemm_nt`` on the NT
+projection workload -- X bf16[384,2,13824] viewed [768,13824], W
+bf16[5120,13824] in its stored layout, out bf16[384,2,5120] -- one step = one
+``gemm_nt`` call on inputs resident in HBM, with L2 flushed (a 256 MiB write)
+between steps and each step timed with CUDA events on the launching stream.
+The same line carries the other paths of the metric under "paths": the fused
+GEMM + cross-entropy with gradient (4096x32768x4096), the loss-only
+large-vocabulary case (8192x128256x4096) and the K=1 product (GB/s).
+
+``--impl reference`` times the CPU oracle (fp64, plain loops) on a bounded
+sample of the same workload, on this machine's host cores.
+
+Multi-GPU: the path has no exchange step, so N ranks run N independent
+replicas (weak scaling, no data-path collective); value = all ranks' FLOPs /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TFLOP/s and % of dense-BF16 peak for gemm_nt and gemm_nt_xent; K=1 GB/s"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["layout_folding_gb300/csrc/gemm_nt_tc.cu", "layout_folding_gb300/csrc/lf_ptx.cuh",
+                  "layout_folding_gb300/csrc/lf_internal.h"]
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_over_ranks(value: float, op: str) -> float:
+    """max or sum of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    e = rec.get(kernel, {}).get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="lf_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = max((num(r[2]) for r in rows if num(r[2]) is not None), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [v for v in sm if smax and v >= 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ our arm
+
+class Timer:
+    """Per-step CUDA events on the launching stream, L2 flushed between steps."""
+
+    def __init__(self, torch, stream):
+        self.torch = torch
+        self.stream = stream
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def run(self, fn, steps, warmup, flush=True):
+        torch = self.torch
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        evs = []
+        with torch.cuda.stream(self.stream):
+            for _ in range(steps):
+                if flush:
+                    self.flush_buf.fill_(1.0)
+                s = torch.cuda.Event(enable_timing=True)
+                e = torch.cuda.Event(enable_timing=True)
+                s.record(self.stream)
+                fn()
+                e.record(self.stream)
+                evs.append((s, e))
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in evs]   # ms per step
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import layout_folding_gb300 as lf
+    from layout_folding_gb300 import synthetic
+
+    torch.cuda.set_device(local_rank)
+    lf.lib()
+    peaks = load_peaks()
+    stream = torch.cuda.Stream()
+    timer = Timer(torch, stream)
+
+    # ---------------- headline: gemm_nt, NT projection
+    wl = synthetic.WORKLOADS["nt_projection"]
+    inp = synthetic.make_workload("nt_projection")
+    x_h, w_h = inp["x"].pin_memory(), inp["w"].pin_memory()
+    x, w = x_h.to("cuda"), w_h.to("cuda")
+    out = torch.empty(384, 2, wl.N, dtype=torch.bfloat16, device="cuda")
+    flops = 2.0 * wl.M * wl.N * wl.K
+
+    def step():
+        lf.gemm_nt(x, w, out, stream=stream)
+
+    with ClockSampler(local_rank) as clk:
+        c0 = lf.launch_count()
+        times = timer.run(step, args.steps, args.warmup)
+        launches = lf.launch_count() - c0
+    lf.check_device_error(stream)
+    total_ms = reduce_over_ranks(sum(times), "max")
+    ms_per_step = total_ms / args.steps
+    value = reduce_over_ranks(flops * args.steps, "sum") / (total_ms * 1e-3) / 1e12
+    kernel_ms = statistics.mean(times)
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = recorded_traffic("k_gemm_nt<EPI_STORE>", "nt_projection")
+
+    # ---------------- e2e: host buffers in, result out, through the same C-ABI call
+    out_h = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
+    xs = torch.empty_like(x)
+    ws_ = torch.empty_like(w)
+
+    def e2e_step():
+        xs.copy_(x_h, non_blocking=True)
+        ws_.copy_(w_h, non_blocking=True)
+        lf.gemm_nt(xs, ws_, out, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+
+    def e2e_in_stream():
+        with torch.cuda.stream(stream):
+            e2e_step()
+    e2e_times = timer.run(e2e_in_stream, max(3, args.steps // 2), 2, flush=False)
+    e2e_ms = reduce_over_ranks(sum(e2e_times), "max") / len(e2e_times)
+    e2e_value = reduce_over_ranks(flops, "sum") / (e2e_ms * 1e-3) / 1e12
+    del xs, ws_
+
+    paths = {}
+    if not args.headline_only:
+        paths = secondary_paths(args, torch, lf, synthetic, timer, stream, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_gemm(inp["x"].reshape(wl.M, wl.K), inp["w"], wl, budget_s=args.cpu_budget)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1)*0.02 bf16; no dataset)",
+        "config": {"workload": "nt_projection", "path": "gemm_nt", "M": wl.M, "N": wl.N, "K": wl.K,
+                   "x_shape": list(wl.x_shape), "accumulate": "fp32", "out": "bf16",
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "pct_of_peak": round(100.0 * achieved / peak, 1),
+        "roofline": {"bound": "tensor", "kernel": "k_gemm_nt<EPI_STORE>", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": "bf16 burst (%s)" % peaks["source"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": (wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": (x.numel() + w.numel()) * 2, "d2h_bytes_per_step": out.numel() * 2,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "paths": paths,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
+    res = {}
+    steps = max(3, min(args.steps, 10))
+    for name, want_grad in (("xent_grad", True), ("xent_loss", False)):
+        wl = synthetic.WORKLOADS[name]
+        inp = synthetic.make_workload(name)
+        x, w, lab = inp["x"].to("cuda"), inp["w"].to("cuda"), inp["labels"].to("cuda")
+        loss = torch.empty(wl.M, dtype=torch.float32, device="cuda")
+        grad = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda") if want_grad else None
+
+        def step():
+            lf.gemm_nt_xent(x, w, lab, loss=loss, grad=grad, stream=stream)
+        c0 = lf.launch_count()
+        times = timer.run(step, steps, 2)
+        launches = lf.launch_count() - c0
+        lf.check_device_error(stream)
+        ms = statistics.mean(times)
+        flops = 2.0 * wl.M * wl.N * wl.K
+        executed = flops * (2 if want_grad else 1)
+        peak = peaks["bf16_tflops_sustained"]
+        res[name] = {"M": wl.M, "N": wl.N, "K": wl.K, "grad": want_grad, "ms": round(ms, 4),
+                     "tflops_algorithmic": round(flops / ms / 1e9, 1),
+                     "tflops_executed": round(executed / ms / 1e9, 1),
+                     "pct_of_peak_algorithmic": round(100 * flops / ms / 1e9 / peak, 1),
+                     "pct_of_peak_executed": round(100 * executed / ms / 1e9 / peak, 1),
+                     "peak": peak, "peak_kind": "bf16 sustained (%s)" % peaks["source"],
+                     "launches_per_step": launches / steps}
+        del x, w, lab, loss, grad, inp
+        torch.cuda.empty_cache()
+    # K=1: the page's [64,1]x[1,4096] (latency regime) and a scaled column count for bandwidth
+    a, b = synthetic.k1_operands(64, 4096)
+    for label, N in (("k1_rope", 4096), ("k1_scaled", 1 << 23)):
+        bb = torch.arange(N, dtype=torch.float32).reshape(1, N) if N != 4096 else b
+        ad, bd = a.to("cuda"), bb.to("cuda")
+        out = torch.empty(64, N, dtype=torch.float32, device="cuda")
+
+        def step():
+            lf.matmul_k1(ad, bd, out, stream=stream)
+        times = timer.run(step, max(steps, 10), 3)
+        ms = statistics.median(times)
+        nbytes = (64 + N + 64 * N) * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[label] = {"M": 64, "N": N, "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes}
+        del ad, bd, out
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------- CPU oracle legs
+
+def cpu_baseline_gemm(x, w, wl, budget_s=15.0):
+    """Time the oracle (as it stands) on a bounded sample of rows of the workload."""
+    import numpy as np
+
+    import oracle
+    xb = oracle._bits(x)
+    wb = oracle._bits(w)
+    rows = np.arange(2, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm_nt_rows(xb, wb, rows, )
+    t_probe = max(time.perf_counter() - t0, 1e-3)
+    nrows = int(max(2, min(wl.M, 2 * budget_s / t_probe)))
+    rows = np.arange(nrows, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm_nt_rows(xb, wb, rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * nrows * wl.N * wl.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "%d of %d rows of X (all %d columns of W, K=%d), fp64 plain loops" % (nrows, wl.M, wl.N, wl.K)}
+
+
+def run_reference(args, rank, world):
+    from layout_folding_gb300 import synthetic
+    wl = synthetic.WORKLOADS["nt_projection"]
+    inp = synthetic.make_workload("nt_projection")
+    import numpy as np
+
+    import oracle
+    xb = oracle._bits(inp["x"].reshape(wl.M, wl.K))
+    wb = oracle._bits(inp["w"])
+    # size one step to about (budget / (warmup + steps)) seconds
+    t0 = time.perf_counter()
+    oracle.gemm_nt_rows(xb, wb, np.arange(1, dtype=np.int64))
+    per_row = max(time.perf_counter() - t0, 1e-3)
+    per_step_s = args.cpu_budget * 6 / max(1, args.steps + args.warmup)
+    nrows = int(max(1, min(wl.M, per_step_s / per_row)))
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = (np.arange(nrows, dtype=np.int64) + i * nrows) % wl.M
+        t0 = time.perf_counter()
+        oracle.gemm_nt_rows(xb, wb, rows)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    flops = 2.0 * nrows * wl.N * wl.K
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    sample = "%d of %d rows of X per step (all %d columns of W, K=%d), fp64 plain loops" % (nrows, wl.M, wl.N, wl.K)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1)*0.02 bf16; no dataset)",
+        "config": {"workload": "nt_projection", "path": "gemm_nt", "M": wl.M, "N": wl.N, "K": wl.K,
+                   "sample_rows_per_step": nrows},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true", help="skip the xent and K=1 paths")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

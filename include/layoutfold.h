@@ -1,0 +1,141 @@
+/*
+ * layoutfold.h -- C ABI of liblayoutfold.so, the GB300 (sm_103a) library for
+ * the layout-folded GEMM paths.
+ *
+ * Notation: X is [M,K], W is [N,K]; both are row-major with K contiguous
+ * ("K-major").  All matrices are contiguous, row-major, and live in device
+ * memory owned by the caller; the library never frees them and keeps no
+ * reference to them after the call returns.
+ *
+ * Every entry point validates its arguments on the host and then enqueues its
+ * kernels on `stream` (0 = the legacy default stream) and returns without
+ * synchronising.  Host-checkable errors are returned immediately and nothing
+ * is enqueued.  A launch failure returns LF_ERR_LAUNCH.  A device-side wait
+ * that runs past its time limit is not visible at return time: it is recorded
+ * in a per-device error word that lf_check_device_error() reads.
+ *
+ * Every compute call requires an sm_103 device (LF_ERR_ARCH otherwise).  There
+ * is no CPU fallback.
+ */
+#ifndef LAYOUTFOLD_H
+#define LAYOUTFOLD_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LF_OK = 0,
+    LF_ERR_NULL = 1,            /* a required pointer is NULL */
+    LF_ERR_SHAPE = 2,           /* M, N or K out of range (<= 0, too large), or K=1 given to gemm_nt_xent */
+    LF_ERR_ALIGN = 3,           /* a base address is not 16-byte aligned, or K % 8 != 0 (K > 1), or N % 8 != 0 */
+    LF_ERR_LAUNCH = 4,          /* a CUDA launch or runtime call failed */
+    LF_ERR_WORKSPACE = 5,       /* the internal workspace could not be allocated */
+    LF_ERR_DEVICE_TIMEOUT = 6,  /* a device-side wait exceeded its limit (reported by lf_check_device_error) */
+    LF_ERR_ARCH = 7             /* the current device is not sm_103 */
+} lf_status;
+
+/*
+ * gemm_nt -- out = X · Wᵀ with the weight consumed in its stored [N,K] layout.
+ *
+ * Source: "Strength reduction: fold transpose into a subsequent GEMM call"
+ * (lightning-thunder issue 1252), Feature: `matmul(x, weight.t())` traced as a
+ * separate transpose fusion followed by a GEMM; the page asks for an "NT" GEMM
+ * that skips the transpose.  Here no transpose and no transposed copy exist:
+ * both operands are read K-major by the tensor-core GEMM.
+ *
+ *   x   : bf16 [M,K], device, row-major (any leading batch dims flattened into M)
+ *   w   : bf16 [N,K], device, row-major (the stored weight)
+ *   out : bf16 [M,N], device, row-major; out[m,n] = bf16_rn(sum_k x[m,k]*w[n,k]),
+ *         the sum accumulated in fp32.
+ *   M, N, K : 1 <= M, N, K < 2^31.  K > 1 needs K % 8 == 0 and N % 8 == 0
+ *         (16-byte row pitch for the tensor copies).
+ *   K == 1 is not an error: it is sent to the pointwise outer-product kernel
+ *         (out[m,n] = bf16_rn(float(x[m]) * float(w[n])), exact product, one rounding),
+ *         as "Feature request: Schedule a small matmul op as a reduction (or
+ *         pointwise) op" (NVIDIA/Fuser issue 3646) proposes; N % 8 == 0 is still required.
+ *   x, w, out must be 16-byte aligned.  out must not overlap x or w.
+ * One kernel launch per call.
+ */
+lf_status gemm_nt(const void *x, const void *w, void *out,
+                  int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * gemm_nt_xent -- logits z = X · Wᵀ (fp32, never written to memory) followed by
+ * the row-wise cross-entropy over N, fused into the GEMM epilogue.
+ *
+ * Source: "Allow reductions in matmul epilogues" (NVIDIA/Fuser issue 2213),
+ * the fusion example (row max, exp, sum-exp, log-sum-exp, the label logit via
+ * a one-hot compare, and the softmax-minus-onehot output), and its follow-up
+ * on reducing a row across tiles by a grid reduction.
+ *
+ *   x, w    : as for gemm_nt (K > 1, K % 8 == 0, N % 8 == 0).
+ *   labels  : int32 [M], device.  Precondition 0 <= labels[m] < N; a row whose
+ *             label is outside that range gets loss NaN and a grad row without
+ *             the -1 term (no ignore-index exists).
+ *   loss    : fp32 [M], device; loss[m] = logsumexp_n z[m,n] - z[m,labels[m]]
+ *             (per row, no mean).
+ *   grad_or_null : NULL, or bf16 [M,N], device;
+ *             grad[m,n] = bf16_rn(exp(z[m,n] - lse[m]) - [n == labels[m]]).
+ *             When NULL nothing of size [M,N] is written anywhere.
+ * Work: one GEMM pass writing per-(row, 256-column tile) partials (max,
+ * sum-exp) and the label logit, one combine kernel, and -- only with grad --
+ * a second GEMM pass that recomputes the logits and writes the gradient.
+ * The partials live in a per-device workspace that the library allocates on
+ * first use (and grows, never shrinks) and frees at unload; calls that share a
+ * device must therefore not run concurrently on different streams.
+ */
+lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels,
+                       float *loss, void *grad_or_null,
+                       int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * matmul_k1 -- the degenerate K=1 matmul as a broadcast multiply.
+ *
+ * Source: "Feature request: Schedule a small matmul op as a reduction (or
+ * pointwise) op" (NVIDIA/Fuser issue 3646): the RoPE matmul of a [64,1]
+ * inverse-frequency column and a [1,4096] position row, and its rewrite as
+ * broadcast, multiply, squeeze.
+ *
+ *   a   : fp32 [M,1], device
+ *   b   : fp32 [1,N], device
+ *   out : fp32 [M,N], device, row-major; out[i,j] = a[i] * b[j] (one IEEE
+ *         multiply, round-to-nearest: bit-exact).  The page's permuted
+ *         [N,M] result is out viewed transposed.
+ *   1 <= M, N < 2^31.  No alignment requirement beyond 4 bytes.
+ */
+lf_status matmul_k1(const float *a, const float *b, float *out,
+                    int64_t M, int64_t N, cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *lf_status_string(lf_status status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns LF_ERR_DEVICE_TIMEOUT if any kernel of this library gave up
+ * on a device-side wait since the last check (its outputs are then invalid),
+ * LF_ERR_LAUNCH if the stream reports a CUDA error, LF_OK otherwise.
+ */
+lf_status lf_check_device_error(cudaStream_t stream);
+
+/* Number of kernel launches this library has enqueued in this process (all devices). */
+uint64_t lf_launch_count(void);
+
+/*
+ * Test hooks (not for production use).  inject_stall = 1 makes the next
+ * tensor-core GEMM launches skip the first operand load of CTA 0, so that
+ * CTA's MMA wait never completes: the bounded wait then gives up after
+ * wait_timeout_ns, records LF_ERR_DEVICE_TIMEOUT for lf_check_device_error()
+ * and every CTA exits normally (no trap, the context stays usable).
+ * wait_timeout_ns = 0 restores the default limit of 2 s.
+ */
+void lf_set_test_hooks(int inject_stall, uint64_t wait_timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAYOUTFOLD_H */

@@ -1,1 +1,169 @@
-"""layout_folding_gb300 -- placeholder, replaced by the binding module."""
+"""layout_folding_gb300 -- Python binding of liblayoutfold.so.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of the library (``include/layoutfold.h`` is the contract).  PyTorch is
+used for device memory and the current stream.  There is no fallback: if the
+library is missing or the device is not sm_103, the calls raise.
+
+Entry points (same names as the C ABI):
+  gemm_nt(x, w, out=None)                       -> out = x @ w.T   (bf16)
+  gemm_nt_xent(x, w, labels, want_grad=False)   -> (loss fp32 [M], grad bf16 [M,N] | None)
+  matmul_k1(a, b, out=None)                     -> out = a * b     (fp32, K=1)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_lib", "liblayoutfold.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "layoutfold.h")
+
+LF_OK = 0
+STATUS_NAMES = {0: "LF_OK", 1: "LF_ERR_NULL", 2: "LF_ERR_SHAPE", 3: "LF_ERR_ALIGN", 4: "LF_ERR_LAUNCH",
+                5: "LF_ERR_WORKSPACE", 6: "LF_ERR_DEVICE_TIMEOUT", 7: "LF_ERR_ARCH"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LayoutFoldError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        msg = lib().lf_status_string(status).decode() if _lib is not None else name
+        super().__init__("%s: %s (%s)" % (where, name, msg))
+
+
+def lib():
+    """Load liblayoutfold.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("liblayoutfold.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.gemm_nt.argtypes = [P, P, P, I64, I64, I64, P]
+        L.gemm_nt.restype = I32
+        L.gemm_nt_xent.argtypes = [P, P, P, P, P, I64, I64, I64, P]
+        L.gemm_nt_xent.restype = I32
+        L.matmul_k1.argtypes = [P, P, P, I64, I64, P]
+        L.matmul_k1.restype = I32
+        L.lf_status_string.argtypes = [I32]
+        L.lf_status_string.restype = ctypes.c_char_p
+        L.lf_check_device_error.argtypes = [P]
+        L.lf_check_device_error.restype = I32
+        L.lf_launch_count.argtypes = []
+        L.lf_launch_count.restype = ctypes.c_uint64
+        L.lf_set_test_hooks.argtypes = [I32, ctypes.c_uint64]
+        L.lf_set_test_hooks.restype = None
+        _lib = L
+        return L
+
+
+def declared_functions(header: str = HEADER):
+    """Names of the functions include/layoutfold.h declares."""
+    with open(header) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
+
+
+def _check(status: int, where: str):
+    if status != LF_OK:
+        raise LayoutFoldError(status, where)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def gemm_nt(x, w, out=None, stream=None):
+    """out[..., n] = sum_k x[..., k] * w[n, k]; x bf16 [..., K], w bf16 [N, K]."""
+    import torch
+    _require(x, torch.bfloat16, "x")
+    _require(w, torch.bfloat16, "w")
+    K = x.shape[-1]
+    N = w.shape[0]
+    if w.dim() != 2 or w.shape[1] != K:
+        raise ValueError("w must be [N, K] with K = x.shape[-1]")
+    M = x.numel() // K if K else 0
+    if out is None:
+        out = torch.empty(*x.shape[:-1], N, dtype=torch.bfloat16, device=x.device)
+    _require(out, torch.bfloat16, "out")
+    if out.numel() != M * N:
+        raise ValueError("out has the wrong size")
+    _check(lib().gemm_nt(x.data_ptr(), w.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)), "gemm_nt")
+    return out
+
+
+def gemm_nt_xent(x, w, labels, want_grad=False, loss=None, grad=None, stream=None):
+    """Fused x @ w.T + row-wise cross-entropy.  Returns (loss fp32 [M], grad bf16 [M, N] or None)."""
+    import torch
+    _require(x, torch.bfloat16, "x")
+    _require(w, torch.bfloat16, "w")
+    _require(labels, torch.int32, "labels")
+    K = x.shape[-1]
+    N = w.shape[0]
+    if w.dim() != 2 or w.shape[1] != K:
+        raise ValueError("w must be [N, K] with K = x.shape[-1]")
+    M = x.numel() // K
+    if labels.numel() != M:
+        raise ValueError("labels must have M elements")
+    if loss is None:
+        loss = torch.empty(M, dtype=torch.float32, device=x.device)
+    _require(loss, torch.float32, "loss")
+    if want_grad and grad is None:
+        grad = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    if grad is not None:
+        _require(grad, torch.bfloat16, "grad")
+        if grad.numel() != M * N:
+            raise ValueError("grad must be [M, N]")
+    _check(lib().gemm_nt_xent(x.data_ptr(), w.data_ptr(), labels.data_ptr(), loss.data_ptr(),
+                              grad.data_ptr() if grad is not None else None, M, N, K, _stream(stream)),
+           "gemm_nt_xent")
+    return loss, grad
+
+
+def matmul_k1(a, b, out=None, stream=None):
+    """out[i, j] = a[i] * b[j]; a fp32 [M, 1], b fp32 [1, N] -> out fp32 [M, N]."""
+    import torch
+    _require(a, torch.float32, "a")
+    _require(b, torch.float32, "b")
+    M, N = a.numel(), b.numel()
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=a.device)
+    _require(out, torch.float32, "out")
+    if out.numel() != M * N:
+        raise ValueError("out must be [M, N]")
+    _check(lib().matmul_k1(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, _stream(stream)), "matmul_k1")
+    return out
+
+
+def check_device_error(stream=None):
+    """Synchronise the stream; raise LayoutFoldError if a device wait timed out."""
+    _check(lib().lf_check_device_error(_stream(stream)), "lf_check_device_error")
+
+
+def launch_count() -> int:
+    return int(lib().lf_launch_count())
+
+
+def set_test_hooks(inject_stall: bool, wait_timeout_ns: int = 0):
+    lib().lf_set_test_hooks(1 if inject_stall else 0, int(wait_timeout_ns))

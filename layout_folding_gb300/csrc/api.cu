@@ -1,0 +1,311 @@
+// api.cu -- the C ABI of liblayoutfold.so: argument validation, tensor-map
+// encoding, per-device state (error word, cross-entropy workspace) and the
+// launch sequences.  Declarations and the contract of each call are in
+// include/layoutfold.h.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "layoutfold.h"
+#include "lf_internal.h"
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+constexpr int64_t MAX_DIM = (int64_t(1) << 31) - 1;
+
+struct DeviceState {
+    bool probed = false;
+    bool arch_ok = false;
+    int num_sms = 0;
+    int *err_word = nullptr;  // device int[64]; [0] = first error code
+    void *ws = nullptr;       // cross-entropy workspace (grow-only)
+    size_t ws_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[MAX_DEVICES];
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_inject{0};
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Resolve (and on first use, set up) the current device.
+lf_status current_device(DeviceState **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return LF_ERR_ARCH;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &d = g_dev[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return LF_ERR_LAUNCH;
+        }
+        d.arch_ok = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.arch_ok) {
+            if (cudaMalloc(&d.err_word, 64 * sizeof(int)) != cudaSuccess ||
+                cudaMemset(d.err_word, 0, 64 * sizeof(int)) != cudaSuccess ||
+                cudaDeviceSynchronize() != cudaSuccess) {
+                cudaGetLastError();
+                return LF_ERR_LAUNCH;
+            }
+        }
+        d.probed = true;
+    }
+    if (!d.arch_ok)
+        return LF_ERR_ARCH;
+    *out = &d;
+    return LF_OK;
+}
+
+// Grow-only workspace of the current device.  Growing frees the old block
+// (cudaFree waits for the device, so no kernel still uses it).
+lf_status ensure_workspace(DeviceState *d, size_t bytes, void **ws)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (d->ws_bytes < bytes) {
+        if (d->ws) {
+            cudaFree(d->ws);
+            d->ws = nullptr;
+            d->ws_bytes = 0;
+        }
+        if (cudaMalloc(&d->ws, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            d->ws = nullptr;
+            return LF_ERR_WORKSPACE;
+        }
+        d->ws_bytes = bytes;
+    }
+    *ws = d->ws;
+    return LF_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// 2-D bf16 tensor [rows, K] (K contiguous), box = 64 columns x box_rows rows,
+// 128-byte swizzle; out-of-range rows/columns read as zero.
+bool make_tmap(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, uint32_t box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(lf::BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+lf::GemmParams gemm_params(const DeviceState *d, int64_t M, int64_t N, int64_t K)
+{
+    lf::GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_m_blocks = static_cast<int>((M + lf::BM - 1) / lf::BM);
+    p.num_n_blocks = static_cast<int>((N + lf::BN - 1) / lf::BN);
+    p.num_k_blocks = static_cast<int>((K + lf::BK - 1) / lf::BK);
+    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    p.err = d->err_word;
+    p.timeout_ns = g_timeout_ns.load();
+    p.inject = g_inject.load();
+    return p;
+}
+
+int gemm_grid(const DeviceState *d, const lf::GemmParams &p)
+{
+    return p.num_tiles < d->num_sms ? p.num_tiles : d->num_sms;
+}
+
+lf_status launched(cudaError_t e, int n)
+{
+    if (e != cudaSuccess)
+        return LF_ERR_LAUNCH;
+    g_launches.fetch_add(static_cast<uint64_t>(n));
+    return LF_OK;
+}
+
+lf_status check_gemm_shape(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
+        return LF_ERR_SHAPE;
+    // the number of output tiles must fit an int as well
+    if (((M + lf::BM - 1) / lf::BM) * ((N + lf::BN - 1) / lf::BN) > MAX_DIM)
+        return LF_ERR_SHAPE;
+    return LF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lf_status gemm_nt(const void *x, const void *w, void *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    if (!x || !w || !out)
+        return LF_ERR_NULL;
+    lf_status st = check_gemm_shape(M, N, K);
+    if (st != LF_OK)
+        return st;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || N % 8 != 0 || (K != 1 && K % 8 != 0))
+        return LF_ERR_ALIGN;
+    DeviceState *d = nullptr;
+    if ((st = current_device(&d)) != LF_OK)
+        return st;
+    if (K == 1)
+        return launched(lf::launch_matmul_k1_bf16(x, w, out, M, N, d->num_sms, stream), 1);
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, x, M, K, lf::BM) || !make_tmap(&tb, w, N, K, lf::BN))
+        return LF_ERR_LAUNCH;
+    lf::GemmParams p = gemm_params(d, M, N, K);
+    p.out = out;
+    return launched(lf::launch_gemm_nt(lf::EPI_STORE, ta, tb, p, gemm_grid(d, p), stream), 1);
+}
+
+lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
+                       int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    if (!x || !w || !labels || !loss)
+        return LF_ERR_NULL;
+    lf_status st = check_gemm_shape(M, N, K);
+    if (st != LF_OK)
+        return st;
+    if (K == 1)
+        return LF_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(w) || !aligned4(labels) || !aligned4(loss) ||
+        (grad_or_null && !aligned16(grad_or_null)) || N % 8 != 0 || K % 8 != 0)
+        return LF_ERR_ALIGN;
+    DeviceState *d = nullptr;
+    if ((st = current_device(&d)) != LF_OK)
+        return st;
+    lf::GemmParams p = gemm_params(d, M, N, K);
+    // workspace: part_max, part_sum [M, NB]; label_logit, row_max, row_logsum [M]
+    const size_t part = round_up(static_cast<size_t>(M) * p.num_n_blocks * sizeof(float), 256);
+    const size_t vec = round_up(static_cast<size_t>(M) * sizeof(float), 256);
+    void *ws = nullptr;
+    if ((st = ensure_workspace(d, 2 * part + 3 * vec, &ws)) != LF_OK)
+        return st;
+    char *wsb = static_cast<char *>(ws);
+    p.part_max = reinterpret_cast<float *>(wsb);
+    p.part_sum = reinterpret_cast<float *>(wsb + part);
+    p.label_logit = reinterpret_cast<float *>(wsb + 2 * part);
+    float *row_max = reinterpret_cast<float *>(wsb + 2 * part + vec);
+    float *row_logsum = reinterpret_cast<float *>(wsb + 2 * part + 2 * vec);
+    p.labels = labels;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, x, M, K, lf::BM) || !make_tmap(&tb, w, N, K, lf::BN))
+        return LF_ERR_LAUNCH;
+    const int grid = gemm_grid(d, p);
+    if ((st = launched(lf::launch_gemm_nt(lf::EPI_XENT_PARTIAL, ta, tb, p, grid, stream), 1)) != LF_OK)
+        return st;
+    if ((st = launched(lf::launch_xent_combine(p.part_max, p.part_sum, p.label_logit, labels, p.M, p.N,
+                                               p.num_n_blocks, loss, grad_or_null ? row_max : nullptr,
+                                               grad_or_null ? row_logsum : nullptr, stream),
+                       1)) != LF_OK)
+        return st;
+    if (!grad_or_null)
+        return LF_OK;
+    p.out = grad_or_null;
+    p.row_max = row_max;
+    p.row_logsum = row_logsum;
+    p.inject = 0;
+    return launched(lf::launch_gemm_nt(lf::EPI_XENT_GRAD, ta, tb, p, grid, stream), 1);
+}
+
+lf_status matmul_k1(const float *a, const float *b, float *out, int64_t M, int64_t N, cudaStream_t stream)
+{
+    if (!a || !b || !out)
+        return LF_ERR_NULL;
+    if (M <= 0 || N <= 0 || M > MAX_DIM || N > MAX_DIM)
+        return LF_ERR_SHAPE;
+    if (!aligned4(a) || !aligned4(b) || !aligned4(out))
+        return LF_ERR_ALIGN;
+    DeviceState *d = nullptr;
+    lf_status st = current_device(&d);
+    if (st != LF_OK)
+        return st;
+    return launched(lf::launch_matmul_k1_f32(a, b, out, M, N, d->num_sms, stream), 1);
+}
+
+const char *lf_status_string(lf_status s)
+{
+    switch (s) {
+    case LF_OK: return "ok";
+    case LF_ERR_NULL: return "null pointer argument";
+    case LF_ERR_SHAPE: return "invalid shape";
+    case LF_ERR_ALIGN: return "misaligned pointer or unsupported row pitch";
+    case LF_ERR_LAUNCH: return "CUDA launch or runtime error";
+    case LF_ERR_WORKSPACE: return "workspace allocation failed";
+    case LF_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case LF_ERR_ARCH: return "current device is not sm_103";
+    }
+    return "unknown status";
+}
+
+lf_status lf_check_device_error(cudaStream_t stream)
+{
+    DeviceState *d = nullptr;
+    lf_status st = current_device(&d);
+    if (st != LF_OK)
+        return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LF_ERR_LAUNCH;
+    }
+    int code = 0;
+    if (cudaMemcpyAsync(&code, d->err_word, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LF_ERR_LAUNCH;
+    }
+    if (code == 0)
+        return LF_OK;
+    if (cudaMemsetAsync(d->err_word, 0, sizeof(int), stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return LF_ERR_LAUNCH;
+    }
+    return LF_ERR_DEVICE_TIMEOUT;
+}
+
+uint64_t lf_launch_count(void) { return g_launches.load(); }
+
+void lf_set_test_hooks(int inject_stall, uint64_t wait_timeout_ns)
+{
+    g_inject.store(inject_stall ? 1 : 0);
+    g_timeout_ns.store(wait_timeout_ns ? wait_timeout_ns : 2000000000ull);
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// lf_internal.h -- declarations shared by the translation units of
+// liblayoutfold.so (not part of the public C ABI).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace lf {
+
+// GEMM tile: one CTA owns a BM x BN output tile, the K loop advances BK
+// columns (one 128-byte swizzle row of bf16) per pipeline stage.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+
+// Epilogues of the NT GEMM kernel.
+enum Epilogue : int {
+    EPI_STORE = 0,         // out = bf16_rn(acc)
+    EPI_XENT_PARTIAL = 1,  // per (row, N-tile): max, sum exp(z - max); label logit
+    EPI_XENT_GRAD = 2,     // grad = bf16_rn(exp(z - lse) - onehot)
+};
+
+struct GemmParams {
+    int M, N, K;
+    int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
+    void *out;                  // EPI_STORE: bf16 [M,N]; EPI_XENT_GRAD: grad bf16 [M,N]
+    const int32_t *labels;      // [M]
+    float *part_max;            // [M, num_n_blocks]: max_n z over the tile
+    float *part_sum;            // [M, num_n_blocks]: sum_n exp(z - part_max)
+    float *label_logit;         // [M]: z[m, labels[m]]
+    const float *row_max;       // [M]: max over the whole row (grad pass)
+    const float *row_logsum;    // [M]: log sum_n exp(z - row_max) (grad pass)
+    int *err;                   // device error word
+    unsigned long long timeout_ns;
+    int inject;                 // test hook: 1 = CTA 0 never loads its first stage
+};
+
+// Launchers (host).  Return cudaSuccess or the launch error.
+cudaError_t launch_gemm_nt(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
+                           int grid, cudaStream_t s);
+int gemm_smem_bytes();
+
+cudaError_t launch_xent_combine(const float *part_max, const float *part_sum, const float *label_logit,
+                                const int32_t *labels, int M, int N, int num_n_blocks, float *loss,
+                                float *row_max, float *row_logsum, cudaStream_t s);
+
+cudaError_t launch_matmul_k1_f32(const float *a, const float *b, float *out, int64_t M, int64_t N,
+                                 int num_sms, cudaStream_t s);
+cudaError_t launch_matmul_k1_bf16(const void *x, const void *w, void *out, int64_t M, int64_t N,
+                                  int num_sms, cudaStream_t s);
+
+}  // namespace lf

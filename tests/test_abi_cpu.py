@@ -1,0 +1,91 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function the public header declares, and rejects invalid arguments on
+the host before any CUDA call is made."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import layout_folding_gb300 as lf
+from layout_folding_gb300 import build as lfbuild
+
+EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
+            "lf_launch_count", "lf_set_test_hooks"}
+
+
+@pytest.fixture(scope="module")
+def L():
+    lfbuild.build()
+    return lf.lib()
+
+
+def test_header_declares_the_boundary():
+    assert set(lf.declared_functions()) >= EXPECTED
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", lf.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in lf.declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_status_strings(L):
+    for code in range(8):
+        s = L.lf_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert L.lf_status_string(99).decode() == "unknown status"
+
+
+A16 = 1 << 20  # a 16-byte aligned fake address: validation fails before it is used
+P = ctypes.c_void_p
+
+
+@pytest.mark.parametrize("args,want", [
+    ((None, A16, A16, 64, 256, 128), 1),
+    ((A16, None, A16, 64, 256, 128), 1),
+    ((A16, A16, None, 64, 256, 128), 1),
+    ((A16, A16, A16, 0, 256, 128), 2),
+    ((A16, A16, A16, 64, -1, 128), 2),
+    ((A16, A16, A16, 64, 256, 0), 2),
+    ((A16, A16, A16, 1 << 31, 256, 128), 2),
+    ((A16 + 2, A16, A16, 64, 256, 128), 3),
+    ((A16, A16 + 8, A16, 64, 256, 128), 3),
+    ((A16, A16, A16 + 4, 64, 256, 128), 3),
+    ((A16, A16, A16, 64, 250, 128), 3),      # N % 8 != 0
+    ((A16, A16, A16, 64, 256, 100), 3),      # K % 8 != 0
+    ((A16, A16, A16, 64, 12, 1), 3),         # K = 1 still needs N % 8 == 0
+])
+def test_gemm_nt_rejects_on_host(L, args, want):
+    assert L.gemm_nt(*[P(a) if a is not None else None for a in args[:3]], *args[3:], None) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((None, A16, A16, A16, None, 64, 256, 128), 1),
+    ((A16, A16, None, A16, None, 64, 256, 128), 1),
+    ((A16, A16, A16, None, None, 64, 256, 128), 1),
+    ((A16, A16, A16, A16, None, 64, 256, 1), 2),      # K = 1 has no cross-entropy path
+    ((A16, A16, A16, A16, None, 0, 256, 128), 2),
+    ((A16, A16, A16 + 2, A16, None, 64, 256, 128), 3),
+    ((A16, A16, A16, A16, A16 + 8, 64, 256, 128), 3),
+    ((A16, A16, A16, A16, None, 64, 256, 132), 3),
+])
+def test_gemm_nt_xent_rejects_on_host(L, args, want):
+    ptrs = [P(a) if a is not None else None for a in args[:5]]
+    assert L.gemm_nt_xent(*ptrs, *args[5:], None) == want
+
+
+def test_matmul_k1_rejects_on_host(L):
+    assert L.matmul_k1(None, P(A16), P(A16), 4, 4, None) == 1
+    assert L.matmul_k1(P(A16), P(A16), P(A16), 0, 4, None) == 2
+    assert L.matmul_k1(P(A16 + 1), P(A16), P(A16), 4, 4, None) == 3
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        lf.gemm_nt(x, x)

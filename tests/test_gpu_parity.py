@@ -1,0 +1,260 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, on the
+same seeded inputs.
+
+Tolerances (stated for the path): GEMM max|gpu - ref| <= 1e-2 * max|ref|
+(plus a stricter element-wise diagnostic: the bf16 rounding bound 2^-8|ref|
+plus 1e-3 * max|ref| for fp32 summation order); per-row loss relative error
+<= 1e-3; gradient absolute error <= 2e-3; the K=1 path bit-exact.
+Full-size workloads are checked on sampled rows (every column of each sampled
+row), small ones in full.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import layout_folding_gb300 as lf
+import oracle
+from layout_folding_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+_cache = {}
+
+
+def workload(name):
+    if name not in _cache:
+        _cache[name] = synthetic.make_workload(name)
+    return _cache[name]
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def sample_rows(M, k=24, seed=0, extra=()):
+    rng = np.random.default_rng(seed)
+    base = {0, M - 1, min(127, M - 1), min(128, M - 1), M // 2}
+    base.update(int(r) for r in rng.integers(0, M, size=k))
+    base.update(r for r in extra if 0 <= r < M)
+    return np.array(sorted(base), dtype=np.int64)
+
+
+def assert_gemm_close(got, ref, what=""):
+    err = np.abs(got - ref)
+    scale = np.abs(ref).max()
+    assert err.max() <= 1e-2 * scale, "%s: max err %g vs bound %g" % (what, err.max(), 1e-2 * scale)
+    bad = err > (2.0 ** -8) * np.abs(ref) + 1e-3 * scale
+    assert not bad.any(), "%s: %d elements outside the element-wise bound, first at %s" % (
+        what, bad.sum(), np.argwhere(bad)[0])
+
+
+def assert_loss_close(got, ref, what=""):
+    rel = np.abs(got - ref) / np.abs(ref)
+    assert rel.max() <= 1e-3, "%s: loss rel err %g at row %d" % (what, rel.max(), rel.argmax())
+
+
+def assert_grad_close(got, ref, what=""):
+    err = np.abs(got - ref)
+    assert err.max() <= 2e-3, "%s: grad abs err %g at %s" % (what, err.max(), np.unravel_index(err.argmax(), err.shape))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    lf.lib()
+    torch.cuda.set_device(0)
+    yield
+    lf.check_device_error()
+
+
+# -------------------------------------------------------------- gemm_nt
+
+def test_gemm_nt_tiny_full():
+    inp = workload("tiny")
+    x, w = inp["x"], inp["w"]
+    out = lf.gemm_nt(x.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    assert out.shape == (64, 256) and out.dtype == torch.bfloat16
+    assert_gemm_close(f64(out), oracle.gemm_nt(x, w), "tiny")
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 520, 200), (130, 264, 72), (1, 8, 8), (257, 1032, 4104)])
+def test_gemm_nt_ragged_full(M, N, K):
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    out = lf.gemm_nt(x.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    assert_gemm_close(f64(out), oracle.gemm_nt(x, w), "ragged %dx%dx%d" % (M, N, K))
+
+
+def test_gemm_nt_persistent_many_tiles():
+    # more tiles than SMs: every CTA runs several tiles through both TMEM buffers
+    M, N, K = 1280, 8192, 512
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    out = lf.gemm_nt(x.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    rows = sample_rows(M, k=40, seed=3)
+    assert_gemm_close(f64(out)[rows], oracle.gemm_nt_rows(x, w, rows), "persistent")
+
+
+def test_gemm_nt_onehot_rows_select_weight_columns_exactly():
+    M, N, K = 256, 512, 256
+    w = synthetic.bf16_normal((N, K), 1.0, 5)
+    ks = (np.arange(M) * 37 + 11) % K
+    x = torch.zeros(M, K, dtype=torch.bfloat16)
+    x[torch.arange(M), torch.from_numpy(ks)] = 1.0
+    out = lf.gemm_nt(x.to(DEV), w.to(DEV)).cpu()
+    want = w.t()[torch.from_numpy(ks)]            # row m = column ks[m] of W^T = W[:, ks[m]]
+    assert torch.equal(out.view(torch.int16), want.contiguous().view(torch.int16))
+
+
+def test_gemm_nt_projection_full_size():
+    wl = synthetic.WORKLOADS["nt_projection"]
+    inp = workload("nt_projection")
+    x, w = inp["x"], inp["w"]
+    assert tuple(x.shape) == (384, 2, 13824)
+    out = lf.gemm_nt(x.to(DEV), w.to(DEV))       # [384,2,13824] viewed as [768,13824]
+    torch.cuda.synchronize()
+    assert tuple(out.shape) == (384, 2, 5120)
+    rows = sample_rows(wl.M, k=20, seed=1, extra=(255, 256, 511, 512, 640))
+    ref = oracle.gemm_nt_rows(x.reshape(wl.M, wl.K), w, rows)
+    assert_gemm_close(f64(out.reshape(wl.M, wl.N))[rows], ref, "nt_projection")
+
+
+def test_gemm_nt_k1_routes_to_pointwise_bitexact():
+    x = synthetic.bf16_normal((96, 1), 2.0, 0)
+    w = synthetic.bf16_normal((264, 1), 0.5, 1)
+    before = lf.launch_count()
+    out = lf.gemm_nt(x.to(DEV), w.to(DEV)).cpu()
+    assert lf.launch_count() - before == 1
+    want = oracle.matmul_k1_bf16(x, w)
+    assert np.array_equal(out.view(torch.int16).numpy().view(np.uint16), want)
+
+
+def test_gemm_nt_is_one_launch_and_allocates_nothing():
+    M, N, K = 768, 5120, 1024
+    x, w = synthetic.make_gemm_inputs(M, N, K, 0.02, 0.02)
+    xd, wd = x.to(DEV), w.to(DEV)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    lf.gemm_nt(xd, wd, out)          # first call: any one-time setup happens here
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    before = lf.launch_count()
+    lf.gemm_nt(xd, wd, out)
+    torch.cuda.synchronize()
+    assert lf.launch_count() - before == 1
+    # no transposed copy of W (K*N*2 bytes) appears anywhere on the device
+    assert abs(torch.cuda.mem_get_info()[0] - free0) < K * N * 2 // 4
+
+
+# --------------------------------------------------------- gemm_nt_xent
+
+def _xent_check(x, w, lab, rows=None, what=""):
+    M = x.reshape(-1, x.shape[-1]).shape[0]
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+    loss_only, none = lf.gemm_nt_xent(xd, wd, ld, want_grad=False)
+    torch.cuda.synchronize()
+    assert none is None
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    _, rloss, _, rgrad = oracle.xent_rows(x.reshape(M, -1), w, lab.numpy(), rows)
+    assert_loss_close(f64(loss)[rows], rloss, what)
+    assert_loss_close(f64(loss_only)[rows], rloss, what + " (loss only)")
+    assert_grad_close(f64(grad)[rows], rgrad, what)
+    return loss, grad
+
+
+def test_xent_tiny_full():
+    inp = workload("tiny")
+    _xent_check(inp["x"], inp["w"], inp["labels"], what="tiny")
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 1000, 136), (64, 8, 64), (129, 776, 520)])
+def test_xent_ragged_full(M, N, K):
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N)
+    edges = [0, N - 1, min(255, N - 1), min(256, N - 1), min(767, N - 1), min(768, N - 1)]
+    for i, e in enumerate(edges):
+        lab[i] = e
+    _xent_check(x, w, lab, what="ragged %dx%dx%d" % (M, N, K))
+
+
+def test_xent_zero_weight_gives_ln_n():
+    M, N, K = 192, 2048, 128
+    x = synthetic.bf16_normal((M, K), 1.0, 0)
+    w = torch.zeros(N, K, dtype=torch.bfloat16)
+    lab = synthetic.labels_uniform(M, N)
+    loss, grad = lf.gemm_nt_xent(x.to(DEV), w.to(DEV), lab.to(DEV), want_grad=True)
+    assert np.allclose(f64(loss), math.log(N), rtol=1e-6, atol=0)
+    want = np.full((M, N), 1.0 / N)
+    want[np.arange(M), lab.numpy()] -= 1.0
+    assert_grad_close(f64(grad), want, "zero weight")
+
+
+def test_xent_large_logits():
+    M, N, K = 256, 1536, 256
+    x, w = synthetic.make_gemm_inputs(M, N, K, 30.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N)
+    _xent_check(x, w, lab, what="large logits")
+
+
+def test_xent_launch_counts():
+    inp = workload("tiny")
+    xd, wd, ld = inp["x"].to(DEV), inp["w"].to(DEV), inp["labels"].to(DEV)
+    lf.gemm_nt_xent(xd, wd, ld)
+    b0 = lf.launch_count()
+    lf.gemm_nt_xent(xd, wd, ld)
+    b1 = lf.launch_count()
+    lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+    b2 = lf.launch_count()
+    assert (b1 - b0, b2 - b1) == (2, 3)
+
+
+def test_xent_grad_full_size():
+    wl = synthetic.WORKLOADS["xent_grad"]
+    inp = workload("xent_grad")
+    lab = inp["labels"].clone()
+    lab[1], lab[2], lab[3] = 0, wl.N - 1, 256 * 77
+    rows = sample_rows(wl.M, k=28, seed=4, extra=(1, 2, 3))
+    _xent_check(inp["x"], inp["w"], lab, rows=rows, what="xent_grad")
+
+
+def test_xent_loss_only_full_size():
+    wl = synthetic.WORKLOADS["xent_loss"]
+    inp = workload("xent_loss")
+    lab = inp["labels"].clone()
+    lab[1], lab[2], lab[3] = 0, wl.N - 1, 256 * 400
+    xd, wd, ld = inp["x"].to(DEV), inp["w"].to(DEV), lab.to(DEV)
+    loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=False)
+    torch.cuda.synchronize()
+    assert grad is None
+    rows = sample_rows(wl.M, k=20, seed=5, extra=(1, 2, 3))
+    _, rloss, _, _ = oracle.xent_rows(inp["x"], inp["w"], lab.numpy(), rows, want_grad=False)
+    assert_loss_close(f64(loss)[rows], rloss, "xent_loss")
+    assert np.all(np.isfinite(f64(loss))) and np.all(f64(loss) > 0)
+
+
+# ------------------------------------------------------------- matmul_k1
+
+def test_matmul_k1_rope_bitexact_and_permuted_view():
+    inp = workload("k1_rope")
+    a, b = inp["a"], inp["b"]
+    out = lf.matmul_k1(a.to(DEV), b.to(DEV)).cpu()
+    want = oracle.matmul_k1(a.numpy(), b.numpy())
+    assert out.shape == (64, 4096)
+    assert np.array_equal(out.numpy().view(np.uint32), want.view(np.uint32))
+    perm = out.t()                                   # the page's [4096, 64] permute
+    assert perm.shape == (4096, 64)
+    assert np.array_equal(perm.numpy().view(np.uint32), want.T.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,N,offset", [(7, 13, 0), (3, 4096, 1), (64, 1 << 20, 0), (1, 1, 0), (70000, 8, 0)])
+def test_matmul_k1_shapes_bitexact(M, N, offset):
+    rng = np.random.default_rng(M + N)
+    a = torch.from_numpy((rng.standard_normal(M) * 100).astype(np.float32))
+    b = torch.from_numpy((rng.standard_normal(N + offset) * 0.01).astype(np.float32))
+    bd = b.to(DEV)[offset:]                          # offset 1: not 16-byte aligned -> scalar path
+    out = lf.matmul_k1(a.to(DEV).reshape(M, 1), bd.reshape(1, N)).cpu()
+    want = oracle.matmul_k1(a.numpy(), b.numpy()[offset:])
+    assert np.array_equal(out.numpy().view(np.uint32), want.view(np.uint32))
