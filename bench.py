@@ -167,13 +167,16 @@ class Timer:
         self.stream = stream
         self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
-    def run(self, fn, steps, warmup, flush=True):
+    def run(self, fn, steps, warmup, flush=True, counter=None):
+        """Returns per-step ms; if `counter` is given, also the number of
+        library launches inside the timed steps."""
         torch = self.torch
         for _ in range(warmup):
             fn()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
+        c0 = counter() if counter else 0
         evs = []
         with torch.cuda.stream(self.stream):
             for _ in range(steps):
@@ -186,9 +189,11 @@ class Timer:
                 e.record(self.stream)
                 evs.append((s, e))
         torch.cuda.synchronize()
+        launches = (counter() - c0) if counter else None
         barrier()
         torch.cuda.synchronize()
-        return [s.elapsed_time(e) for s, e in evs]   # ms per step
+        times = [s.elapsed_time(e) for s, e in evs]   # ms per step
+        return (times, launches) if counter else times
 
 
 def run_ours(args, rank, world, local_rank):
@@ -215,9 +220,7 @@ def run_ours(args, rank, world, local_rank):
         lf.gemm_nt(x, w, out, stream=stream)
 
     with ClockSampler(local_rank) as clk:
-        c0 = lf.launch_count()
-        times = timer.run(step, args.steps, args.warmup)
-        launches = lf.launch_count() - c0
+        times, launches = timer.run(step, args.steps, args.warmup, counter=lf.launch_count)
     lf.check_device_error(stream)
     total_ms = reduce_over_ranks(sum(times), "max")
     ms_per_step = total_ms / args.steps
@@ -300,9 +303,7 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
 
         def step():
             lf.gemm_nt_xent(x, w, lab, loss=loss, grad=grad, stream=stream)
-        c0 = lf.launch_count()
-        times = timer.run(step, steps, 2)
-        launches = lf.launch_count() - c0
+        times, launches = timer.run(step, steps, 3, counter=lf.launch_count)
         lf.check_device_error(stream)
         ms = statistics.mean(times)
         flops = 2.0 * wl.M * wl.N * wl.K
