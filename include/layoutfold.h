@@ -125,6 +125,14 @@ lf_status lf_check_device_error(cudaStream_t stream);
 uint64_t lf_launch_count(void);
 
 /*
+ * Tuning knob: how many K blocks (64 columns each) ahead of its shared-memory
+ * loads each GEMM CTA prefetches its operand slices into L2.  A negative
+ * value restores the default (0: off); 0 disables the prefetch.  Applies to
+ * launches made after the call, on every device.
+ */
+void lf_set_tuning(int l2_prefetch_kblocks);
+
+/*
  * Test hooks (not for production use).  inject_stall = 1 makes the next
  * tensor-core GEMM launches skip the first operand load of CTA 0, so that
  * CTA's MMA wait never completes: the bounded wait then gives up after

@@ -59,6 +59,8 @@ def lib():
         L.lf_check_device_error.restype = I32
         L.lf_launch_count.argtypes = []
         L.lf_launch_count.restype = ctypes.c_uint64
+        L.lf_set_tuning.argtypes = [I32]
+        L.lf_set_tuning.restype = None
         L.lf_set_test_hooks.argtypes = [I32, ctypes.c_uint64]
         L.lf_set_test_hooks.restype = None
         _lib = L
@@ -163,6 +165,11 @@ def check_device_error(stream=None):
 
 def launch_count() -> int:
     return int(lib().lf_launch_count())
+
+
+def set_tuning(l2_prefetch_kblocks: int = -1):
+    """K blocks of L2 prefetch ahead of the shared-memory loads (-1 = default)."""
+    lib().lf_set_tuning(int(l2_prefetch_kblocks))
 
 
 def set_test_hooks(inject_stall: bool, wait_timeout_ns: int = 0):

@@ -29,6 +29,7 @@ DeviceState g_dev[MAX_DEVICES];
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_inject{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_l2_prefetch{-1};  // -1: per-shape default
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -142,6 +143,8 @@ lf::GemmParams gemm_params(const DeviceState *d, int64_t M, int64_t N, int64_t K
     p.err = d->err_word;
     p.timeout_ns = g_timeout_ns.load();
     p.inject = g_inject.load();
+    const int pf = g_l2_prefetch.load();
+    p.l2_prefetch = pf >= 0 ? pf : 0;
     return p;
 }
 
@@ -301,6 +304,8 @@ lf_status lf_check_device_error(cudaStream_t stream)
 }
 
 uint64_t lf_launch_count(void) { return g_launches.load(); }
+
+void lf_set_tuning(int l2_prefetch_kblocks) { g_l2_prefetch.store(l2_prefetch_kblocks < 0 ? -1 : l2_prefetch_kblocks); }
 
 void lf_set_test_hooks(int inject_stall, uint64_t wait_timeout_ns)
 {

@@ -292,6 +292,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int s = 0; s < STAGES; ++s)
                 armed[s] = 0;
             bool ok = true, first = true;
+            // L2 prefetch cursor: walks the same (tile, k-block) sequence as the
+            // loads, l2_prefetch steps ahead, so operand slices are already in
+            // L2 when their shared-memory load is issued.
+            int pf_tile = blockIdx.x, pf_kb = 0;
+            auto prefetch_next = [&]() {
+                if (pf_tile < p.num_tiles) {
+                    tma_prefetch_l2_2d(&tmA, pf_kb * BK, (pf_tile % p.num_m_blocks) * BM);
+                    tma_prefetch_l2_2d(&tmB, pf_kb * BK, (pf_tile / p.num_m_blocks) * BN);
+                    if (++pf_kb == p.num_k_blocks) {
+                        pf_kb = 0;
+                        pf_tile += gridDim.x;
+                    }
+                }
+            };
+            for (int i = 0; i < p.l2_prefetch; ++i)
+                prefetch_next();
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 const int mb = tile % p.num_m_blocks;
                 const int nb = tile / p.num_m_blocks;
@@ -300,6 +316,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
+                    if (p.l2_prefetch > 0)
+                        prefetch_next();
                     const bool skip = first && p.inject == 1 && blockIdx.x == 0;
                     first = false;
                     if (!skip) {

@@ -33,6 +33,7 @@ struct GemmParams {
     int *err;                   // device error word
     unsigned long long timeout_ns;
     int inject;                 // test hook: 1 = CTA 0 never loads its first stage
+    int l2_prefetch;            // k-blocks the L2 prefetch stream runs ahead of the loads (0 = off)
 };
 
 // Launchers (host).  Return cudaSuccess or the launch error.
