@@ -110,6 +110,41 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels,
 lf_status matmul_k1(const float *a, const float *b, float *out,
                     int64_t M, int64_t N, cudaStream_t stream);
 
+/*
+ * gemm_nt_xent_noalloc -- the same computation and outputs as gemm_nt_xent,
+ * for callers that cannot allocate device memory during the call.  The pages
+ * have no counterpart to this entry point: it is an interface addition.
+ *
+ * Who needs it: code that runs while a CUDA graph is being captured (where
+ * cudaMalloc/cudaFree are not allowed and cudaFree would synchronise the
+ * device), programs whose allocator already owns all device memory (a
+ * framework caching allocator, a serving engine that reserved the GPU up
+ * front), and latency-critical paths that cannot take the device
+ * synchronisation of a first-use allocation.  gemm_nt_xent allocates its
+ * workspace on first use; this variant never calls cudaMalloc, cudaFree or
+ * any allocating library routine.
+ *
+ * Scratch: a fixed 32 MiB device array inside the library (it holds the
+ * per-tile partials, M * ceil(N/256) * 8 bytes, plus 12 * M bytes and an
+ * error word).  Every GPU that loads the library keeps those 32 MiB until
+ * the process exits.  A call whose scratch need exceeds 32 MiB returns
+ * LF_ERR_WORKSPACE before anything is enqueued (for example M = 8192 with
+ * N = 128256, a 128K vocabulary, fits; M = 16384 with N = 262144 does not).
+ * Set-up: the first call made with a given device current looks up the
+ * scratch's device address (cudaGetSymbolAddress) and checks the device;
+ * make that first call before any stream capture begins.
+ * Concurrency: every call shares the one scratch array, which keeps the last
+ * call's contents; calls that overlap on the GPU (different streams, or
+ * graphs replayed concurrently) race on it and must be serialised.
+ * Device-side wait timeouts are not reported through lf_check_device_error:
+ * a call whose device waits ran out writes NaN to every loss[m].
+ * Arguments, layouts, preconditions and the other error codes are those of
+ * gemm_nt_xent.
+ */
+lf_status gemm_nt_xent_noalloc(const void *x, const void *w, const int32_t *labels,
+                               float *loss, void *grad_or_null,
+                               int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *lf_status_string(lf_status status);
 
