@@ -160,12 +160,21 @@ lf_status lf_check_device_error(cudaStream_t stream);
 uint64_t lf_launch_count(void);
 
 /*
- * Tuning knob: how many K blocks (64 columns each) ahead of its shared-memory
- * loads each GEMM CTA prefetches its operand slices into L2.  A negative
- * value restores the default (0: off); 0 disables the prefetch.  Applies to
- * launches made after the call, on every device.
+ * Sets up the current device if needed and reports its SM count and how many
+ * CTA pairs of the pair GEMM kernel can be resident at once (either pointer
+ * may be NULL).  LF_ERR_ARCH on a device that is not sm_103.
  */
-void lf_set_tuning(int l2_prefetch_kblocks);
+lf_status lf_device_query(int *num_sms, int *pair_clusters);
+
+/*
+ * Tuning knobs, applied to launches made after the call, on every device.
+ *   l2_prefetch_kblocks: how many K blocks (64 columns each) ahead of its
+ *     shared-memory loads each GEMM CTA prefetches its operand slices into
+ *     L2; 0 disables it, a negative value restores the default (off).
+ *   gemm_variant: 1 = single-CTA 128x256 tiles, 2 = CTA-pair 256x256 tiles
+ *     (tcgen05 cta_group::2), anything else = automatic (pairs when M > 128).
+ */
+void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant);
 
 /*
  * Test hooks (not for production use).  inject_stall = 1 makes the next

@@ -59,7 +59,9 @@ def lib():
         L.lf_check_device_error.restype = I32
         L.lf_launch_count.argtypes = []
         L.lf_launch_count.restype = ctypes.c_uint64
-        L.lf_set_tuning.argtypes = [I32]
+        L.lf_device_query.argtypes = [P, P]
+        L.lf_device_query.restype = I32
+        L.lf_set_tuning.argtypes = [I32, I32]
         L.lf_set_tuning.restype = None
         L.lf_set_test_hooks.argtypes = [I32, ctypes.c_uint64]
         L.lf_set_test_hooks.restype = None
@@ -167,9 +169,17 @@ def launch_count() -> int:
     return int(lib().lf_launch_count())
 
 
-def set_tuning(l2_prefetch_kblocks: int = -1):
-    """K blocks of L2 prefetch ahead of the shared-memory loads (-1 = default)."""
-    lib().lf_set_tuning(int(l2_prefetch_kblocks))
+def device_query():
+    """(SM count, co-resident CTA pairs of the pair GEMM kernel) of the current device."""
+    sms, pairs = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().lf_device_query(ctypes.byref(sms), ctypes.byref(pairs)), "lf_device_query")
+    return sms.value, pairs.value
+
+
+def set_tuning(l2_prefetch_kblocks: int = -1, gemm_variant: int = -1):
+    """L2-prefetch distance in K blocks (-1 = default, off) and GEMM tile
+    variant (1 = single CTA, 2 = CTA pair, -1 = automatic)."""
+    lib().lf_set_tuning(int(l2_prefetch_kblocks), int(gemm_variant))
 
 
 def set_test_hooks(inject_stall: bool, wait_timeout_ns: int = 0):

@@ -19,6 +19,7 @@ struct DeviceState {
     bool probed = false;
     bool arch_ok = false;
     int num_sms = 0;
+    int pair_clusters = 0;    // co-resident CTA pairs of the pair kernel
     int *err_word = nullptr;  // device int[64]; [0] = first error code
     void *ws = nullptr;       // cross-entropy workspace (grow-only)
     size_t ws_bytes = 0;
@@ -30,6 +31,7 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_inject{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_l2_prefetch{-1};  // -1: per-shape default
+std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA tiles, 2 CTA-pair tiles
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -72,6 +74,7 @@ lf_status current_device(DeviceState **out)
         d.arch_ok = (major == 10 && minor == 3);
         d.num_sms = sms;
         if (d.arch_ok) {
+            d.pair_clusters = lf::gemm_pair_max_active_clusters();
             if (cudaMalloc(&d.err_word, 64 * sizeof(int)) != cudaSuccess ||
                 cudaMemset(d.err_word, 0, 64 * sizeof(int)) != cudaSuccess ||
                 cudaDeviceSynchronize() != cudaSuccess) {
@@ -129,14 +132,28 @@ bool make_tmap(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, uint32_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-lf::GemmParams gemm_params(const DeviceState *d, int64_t M, int64_t N, int64_t K)
-{
+// Everything one GEMM launch needs: variant, tensor maps, parameters, grid.
+struct GemmPlan {
+    bool pair = false;
+    CUtensorMap ta, tb;
     lf::GemmParams p;
+    int grid = 0;
+};
+
+lf_status plan_gemm(const DeviceState *d, const void *x, const void *w, int64_t M, int64_t N, int64_t K,
+                    GemmPlan *g)
+{
+    const int variant = g_variant.load();
+    g->pair = d->pair_clusters > 0 && (variant == 2 || (variant < 0 && M > lf::BM));
+    const int tile_m = g->pair ? 2 * lf::BM : lf::BM;
+    if (!make_tmap(&g->ta, x, M, K, lf::BM) || !make_tmap(&g->tb, w, N, K, g->pair ? lf::BN / 2 : lf::BN))
+        return LF_ERR_LAUNCH;
+    lf::GemmParams &p = g->p;
     std::memset(&p, 0, sizeof p);
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.num_m_blocks = static_cast<int>((M + lf::BM - 1) / lf::BM);
+    p.num_m_blocks = static_cast<int>((M + tile_m - 1) / tile_m);
     p.num_n_blocks = static_cast<int>((N + lf::BN - 1) / lf::BN);
     p.num_k_blocks = static_cast<int>((K + lf::BK - 1) / lf::BK);
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
@@ -145,12 +162,17 @@ lf::GemmParams gemm_params(const DeviceState *d, int64_t M, int64_t N, int64_t K
     p.inject = g_inject.load();
     const int pf = g_l2_prefetch.load();
     p.l2_prefetch = pf >= 0 ? pf : 0;
-    return p;
+    if (g->pair)
+        g->grid = 2 * (p.num_tiles < d->pair_clusters ? p.num_tiles : d->pair_clusters);
+    else
+        g->grid = p.num_tiles < d->num_sms ? p.num_tiles : d->num_sms;
+    return LF_OK;
 }
 
-int gemm_grid(const DeviceState *d, const lf::GemmParams &p)
+cudaError_t run_gemm(int epi, const GemmPlan &g, cudaStream_t stream)
 {
-    return p.num_tiles < d->num_sms ? p.num_tiles : d->num_sms;
+    return g.pair ? lf::launch_gemm_nt_pair(epi, g.ta, g.tb, g.p, g.grid, stream)
+                  : lf::launch_gemm_nt(epi, g.ta, g.tb, g.p, g.grid, stream);
 }
 
 lf_status launched(cudaError_t e, int n)
@@ -189,12 +211,11 @@ lf_status gemm_nt(const void *x, const void *w, void *out, int64_t M, int64_t N,
         return st;
     if (K == 1)
         return launched(lf::launch_matmul_k1_bf16(x, w, out, M, N, d->num_sms, stream), 1);
-    CUtensorMap ta, tb;
-    if (!make_tmap(&ta, x, M, K, lf::BM) || !make_tmap(&tb, w, N, K, lf::BN))
-        return LF_ERR_LAUNCH;
-    lf::GemmParams p = gemm_params(d, M, N, K);
-    p.out = out;
-    return launched(lf::launch_gemm_nt(lf::EPI_STORE, ta, tb, p, gemm_grid(d, p), stream), 1);
+    GemmPlan g;
+    if ((st = plan_gemm(d, x, w, M, N, K, &g)) != LF_OK)
+        return st;
+    g.p.out = out;
+    return launched(run_gemm(lf::EPI_STORE, g, stream), 1);
 }
 
 lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
@@ -213,7 +234,10 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
     DeviceState *d = nullptr;
     if ((st = current_device(&d)) != LF_OK)
         return st;
-    lf::GemmParams p = gemm_params(d, M, N, K);
+    GemmPlan g;
+    if ((st = plan_gemm(d, x, w, M, N, K, &g)) != LF_OK)
+        return st;
+    lf::GemmParams &p = g.p;
     // workspace: part_max, part_sum [M, NB]; label_logit, row_max, row_logsum [M]
     const size_t part = round_up(static_cast<size_t>(M) * p.num_n_blocks * sizeof(float), 256);
     const size_t vec = round_up(static_cast<size_t>(M) * sizeof(float), 256);
@@ -227,11 +251,7 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
     float *row_max = reinterpret_cast<float *>(wsb + 2 * part + vec);
     float *row_logsum = reinterpret_cast<float *>(wsb + 2 * part + 2 * vec);
     p.labels = labels;
-    CUtensorMap ta, tb;
-    if (!make_tmap(&ta, x, M, K, lf::BM) || !make_tmap(&tb, w, N, K, lf::BN))
-        return LF_ERR_LAUNCH;
-    const int grid = gemm_grid(d, p);
-    if ((st = launched(lf::launch_gemm_nt(lf::EPI_XENT_PARTIAL, ta, tb, p, grid, stream), 1)) != LF_OK)
+    if ((st = launched(run_gemm(lf::EPI_XENT_PARTIAL, g, stream), 1)) != LF_OK)
         return st;
     if ((st = launched(lf::launch_xent_combine(p.part_max, p.part_sum, p.label_logit, labels, p.M, p.N,
                                                p.num_n_blocks, loss, grad_or_null ? row_max : nullptr,
@@ -244,7 +264,7 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
     p.row_max = row_max;
     p.row_logsum = row_logsum;
     p.inject = 0;
-    return launched(lf::launch_gemm_nt(lf::EPI_XENT_GRAD, ta, tb, p, grid, stream), 1);
+    return launched(run_gemm(lf::EPI_XENT_GRAD, g, stream), 1);
 }
 
 lf_status matmul_k1(const float *a, const float *b, float *out, int64_t M, int64_t N, cudaStream_t stream)
@@ -305,7 +325,24 @@ lf_status lf_check_device_error(cudaStream_t stream)
 
 uint64_t lf_launch_count(void) { return g_launches.load(); }
 
-void lf_set_tuning(int l2_prefetch_kblocks) { g_l2_prefetch.store(l2_prefetch_kblocks < 0 ? -1 : l2_prefetch_kblocks); }
+lf_status lf_device_query(int *num_sms, int *pair_clusters)
+{
+    DeviceState *d = nullptr;
+    lf_status st = current_device(&d);
+    if (st != LF_OK)
+        return st;
+    if (num_sms)
+        *num_sms = d->num_sms;
+    if (pair_clusters)
+        *pair_clusters = d->pair_clusters;
+    return LF_OK;
+}
+
+void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant)
+{
+    g_l2_prefetch.store(l2_prefetch_kblocks < 0 ? -1 : l2_prefetch_kblocks);
+    g_variant.store(gemm_variant == 1 || gemm_variant == 2 ? gemm_variant : -1);
+}
 
 void lf_set_test_hooks(int inject_stall, uint64_t wait_timeout_ns)
 {

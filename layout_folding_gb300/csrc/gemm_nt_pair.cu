@@ -1,0 +1,306 @@
+// gemm_nt_pair.cu -- the NT GEMM  acc = X[M,K] · W[N,K]^T  on a CTA pair
+// (tcgen05 cta_group::2): one 256x256 output tile per pair of SMs.
+//
+// Source: "Strength reduction: fold transpose into a subsequent GEMM call"
+// (lightning-thunder issue 1252), Feature/Motivation: the weight is read in
+// its stored [N,K] layout as the K-major B operand -- no transpose op, no
+// transposed copy.  "Allow reductions in matmul epilogues" (NVIDIA/Fuser issue
+// 2213): the cross-entropy epilogues run on the finished accumulator.
+//
+// Why a pair: each CTA stages only its half of the tile's operands (128 rows
+// of X and 128 rows of W per 64-wide K slice = 32 KiB), yet the pair's MMA
+// computes a 256x256 product, so the bytes each SM must pull per FLOP drop by
+// a third against a 128x256 single-CTA tile, and the same 192 KiB of shared
+// memory holds a 6-deep ring instead of a 4-deep one (50% more load latency
+// covered).
+//
+// Roles (192 threads per CTA, cluster of 2 CTAs, rank 0 = leader):
+//   warp 0 (both CTAs): TMA producer for this CTA's halves; both CTAs' copies
+//            complete on the LEADER's full barrier (the leader arms it for the
+//            bytes of both halves).
+//   warp 1 (both CTAs): TMEM allocation (pair form); in the leader one lane
+//            issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and commits
+//            with a multicast arrive to both CTAs' barriers.
+//   warps 2..5 (both CTAs): epilogue on this CTA's 128 accumulator rows; one
+//            lane per warp arrives on the leader's accumulator-free barrier.
+// Bounded waits everywhere; an abort raised in either CTA is mirrored into the
+// peer, and both meet at a final cluster barrier before TMEM is freed.
+#include "lf_gemm_common.cuh"
+
+namespace lf {
+namespace {
+
+constexpr int PAIR_M = 2 * BM;          // 256 rows of X per pair tile
+constexpr int PAIR_UMMA_K = 16;
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_A_BYTES = BM * BK * 2;          // 16 KiB: this CTA's 128 rows of X
+constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;    // 16 KiB: this CTA's 128 rows of W
+constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_ACC_BUFS = 2;
+constexpr int PAIR_TMEM_COLS = PAIR_ACC_BUFS * BN;  // 512
+constexpr int PAIR_THREADS = 192;
+constexpr int PAIR_EPI_WARPS = 4;
+constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 1;
+constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + PAIR_NUM_BARS * 8 + 16;
+constexpr uint32_t PAIR_IDESC = idesc_bf16_f32(PAIR_M, BN);
+constexpr uint64_t ABORT_SETTLE_NS = 100000;  // after an abort: let copies in flight land
+
+template <int EPI>
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
+    k_gemm_nt_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + PAIR_STAGES * PAIR_A_BYTES;
+    const uint32_t bar0 = base + PAIR_STAGES * PAIR_STAGE_BYTES;
+    const uint32_t drain_bar = bar0 + 8u * (2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+#define FULL_BAR(s) (bar0 + 8u * (s))
+#define EMPTY_BAR(s) (bar0 + 8u * (PAIR_STAGES + (s)))
+#define TFULL_BAR(b) (bar0 + 8u * (2 * PAIR_STAGES + (b)))
+#define TEMPTY_BAR(b) (bar0 + 8u * (2 * PAIR_STAGES + PAIR_ACC_BUFS + (b)))
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PAIR_STAGES; ++s) {
+            mbar_init(FULL_BAR(s), 1);   // leader: its arrive.expect_tx + both CTAs' bytes
+            mbar_init(EMPTY_BAR(s), 1);  // the leader's multicast commit
+        }
+        for (int b = 0; b < PAIR_ACC_BUFS; ++b) {
+            mbar_init(TFULL_BAR(b), 1);                    // the leader's multicast commit
+            mbar_init(TEMPTY_BAR(b), 2 * PAIR_EPI_WARPS);  // leader: one arrive per epilogue warp of each CTA
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), PAIR_TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed[PAIR_STAGES];
+#pragma unroll
+            for (int s = 0; s < PAIR_STAGES; ++s)
+                armed[s] = 0;
+            bool ok = true, first = true;
+            for (int tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
+                const int mb = tile % p.num_m_blocks;
+                const int nb = tile / p.num_m_blocks;
+                const int arow = mb * PAIR_M + static_cast<int>(rank) * BM;
+                const int brow = nb * BN + static_cast<int>(rank) * (BN / 2);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_bar(EMPTY_BAR(stage), phase ^ 1u, abort_flag, p, ERR_PRODUCER, peer_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_leader = mapa_shared(FULL_BAR(stage), 0u);
+                    // test hook: pair 0's leader never arms its first stage, so
+                    // that stage can never complete and the MMA wait runs out
+                    const bool skip = first && p.inject == 1 && blockIdx.x == 0;
+                    first = false;
+                    if (!skip) {
+                        if (leader) {
+                            mbar_arrive_expect_tx(FULL_BAR(stage), 2 * PAIR_STAGE_BYTES);
+                            ++armed[stage];
+                        }
+                        tma_load_2d_pair(sA + stage * PAIR_A_BYTES, &tmA, kb * BK, arow, full_leader);
+                        tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tmB, kb * BK, brow, full_leader);
+                    }
+                    if (++stage == PAIR_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (leader)
+                for (int s = 0; s < PAIR_STAGES; ++s)
+                    if (armed[s])
+                        wait_bar_drain(FULL_BAR(s), (armed[s] - 1u) & 1u, abort_flag, p, peer_abort);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        if (leader && lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
+                if (!wait_bar(TEMPTY_BAR(acc), acc_phase ^ 1u, abort_flag, p, ERR_MMA_ACC, peer_abort))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_bar(FULL_BAR(stage), phase, abort_flag, p, ERR_MMA_FULL, peer_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * PAIR_A_BYTES;
+                    const uint32_t b0 = sB + stage * PAIR_B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / PAIR_UMMA_K; ++k)
+                        umma_f16_pair(d_tmem, smem_desc_k128(a0 + k * PAIR_UMMA_K * 2),
+                                      smem_desc_k128(b0 + k * PAIR_UMMA_K * 2), PAIR_IDESC, (kb | k) != 0 ? 1u : 0u);
+                    umma_commit_pair_mc(EMPTY_BAR(stage), 0x3);  // both CTAs may refill this slot
+                    if (++stage == PAIR_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit_pair_mc(TFULL_BAR(acc), 0x3);  // accumulator complete in both TMEMs
+                if (++acc == PAIR_ACC_BUFS) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            umma_commit_pair_mc(drain_bar, 0x1);
+            wait_bar_drain(drain_bar, 0u, abort_flag, p, peer_abort);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = pair; tile < p.num_tiles; tile += num_pairs) {
+            const int mb = tile % p.num_m_blocks;
+            const int nb = tile / p.num_m_blocks;
+            const bool ok = wait_bar(TFULL_BAR(acc), acc_phase, abort_flag, p, ERR_EPI, peer_abort);
+            if (!__all_sync(0xffffffffu, ok))
+                break;
+            tc_fence_after();
+            const int row = mb * PAIR_M + static_cast<int>(rank) * BM + q * 32 + lane;
+            const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
+            if (EPI == EPI_STORE)
+                epi_store(p, taddr, row, nb);
+            else if (EPI == EPI_XENT_PARTIAL)
+                epi_xent_partial(p, taddr, row, nb);
+            else
+                epi_xent_grad(p, taddr, row, nb);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(mapa_shared(TEMPTY_BAR(acc), 0u));
+            if (++acc == PAIR_ACC_BUFS) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+#undef FULL_BAR
+#undef EMPTY_BAR
+#undef TFULL_BAR
+#undef TEMPTY_BAR
+
+    if (*abort_flag) {
+        // Copies this CTA issued complete on the leader's barrier, so nothing
+        // here can wait for them: give them a fixed, generous time to land.
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < ABORT_SETTLE_NS) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer no longer touches this CTA's barriers, smem or TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, PAIR_TMEM_COLS);
+    }
+}
+
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t s, cudaLaunchAttribute *attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(PAIR_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int EPI>
+cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid,
+                          cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_nt_pair<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PAIR_SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config(grid, s, attr);
+    return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI>, ta, tb, p);
+}
+
+}  // namespace
+
+int gemm_pair_smem_bytes() { return PAIR_SMEM_BYTES; }
+
+// Number of CTA pairs of the pair kernel that fit on the device at once.
+int gemm_pair_max_active_clusters()
+{
+    if (cudaFuncSetAttribute(k_gemm_nt_pair<EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PAIR_SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config(2, 0, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_nt_pair<EPI_STORE>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+cudaError_t launch_gemm_nt_pair(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
+                                int grid, cudaStream_t s)
+{
+    switch (epi) {
+    case EPI_STORE:
+        return launch_pair_t<EPI_STORE>(ta, tb, p, grid, s);
+    case EPI_XENT_PARTIAL:
+        return launch_pair_t<EPI_XENT_PARTIAL>(ta, tb, p, grid, s);
+    case EPI_XENT_GRAD:
+        return launch_pair_t<EPI_XENT_GRAD>(ta, tb, p, grid, s);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace lf

@@ -1,0 +1,214 @@
+// lf_gemm_common.cuh -- device code shared by the NT GEMM kernels (single-CTA
+// and CTA-pair): bounded mbarrier waits with CTA-wide abort, and the three
+// epilogues that read a finished accumulator out of TMEM.
+//
+// Epilogue sources: "Strength reduction: fold transpose into a subsequent GEMM
+// call" (the bf16 output of the traced matmul) and "Allow reductions in matmul
+// epilogues" (NVIDIA/Fuser issue 2213), the fusion example: row max, exp and
+// its sum, the label logit picked by comparing the column index with the
+// label, and the softmax-minus-onehot output.
+#pragma once
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "lf_internal.h"
+#include "lf_ptx.cuh"
+
+namespace lf {
+namespace {
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+// Error codes written to the device error word (first writer wins).
+constexpr int ERR_PRODUCER = 0x101;   // ring slot never freed
+constexpr int ERR_MMA_FULL = 0x102;   // stage never landed
+constexpr int ERR_MMA_ACC = 0x103;    // accumulator never released by the epilogue
+constexpr int ERR_EPI = 0x104;        // accumulator never completed
+constexpr int ERR_DRAIN = 0x105;      // copies / MMAs did not finish while unwinding
+
+// Record `code` (first writer wins), raise this CTA's abort flag and, in a
+// CTA pair, the peer's (peer_abort: its shared::cluster address, 0 if none).
+__device__ __forceinline__ void raise_error(const GemmParams &p, volatile int *abort_flag, int code,
+                                            uint32_t peer_abort)
+{
+    *abort_flag = 1;
+    if (peer_abort)
+        st_cluster_u32(peer_abort, 1u);
+    atomicCAS(p.err, 0, code);
+}
+
+// Wait for phase `parity` of `bar`; false if the CTA is aborting or the time
+// limit passed (then the error is recorded and the abort flag raised).
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                      const GemmParams &p, int code, uint32_t peer_abort = 0)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+                raise_error(p, abort_flag, code, peer_abort);
+                return false;
+            }
+        }
+    }
+}
+
+// Same, used while unwinding: ignores the abort flag, keeps the time limit.
+__device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                            const GemmParams &p, uint32_t peer_abort = 0)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+            raise_error(p, abort_flag, ERR_DRAIN, peer_abort);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x (lower address) = lo
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Store 32 consecutive fp32 values as bf16 to dst[0..32), 8 at a time, keeping
+// only the 8-column groups that start below `limit` columns.
+__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16 *dst, const float (&f)[32], int limit)
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (j * 8 < limit) {
+            uint4 v;
+            v.x = pack_bf16(f[8 * j + 0], f[8 * j + 1]);
+            v.y = pack_bf16(f[8 * j + 2], f[8 * j + 3]);
+            v.z = pack_bf16(f[8 * j + 4], f[8 * j + 5]);
+            v.w = pack_bf16(f[8 * j + 6], f[8 * j + 7]);
+            reinterpret_cast<uint4 *>(dst)[j] = v;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- epilogues
+// Each runs on one epilogue warp: thread `lane` owns output row `row` of the
+// tile, whose accumulator row starts at TMEM address `taddr`.
+
+// out = bf16_rn(acc)
+__device__ __forceinline__ void epi_store(const GemmParams &p, uint32_t taddr, int row, int nb)
+{
+    const bool row_ok = row < p.M;
+    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(row) * p.N;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c, v);
+        tmem_wait_ld();
+        if (row_ok) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                f[i] = __uint_as_float(v[i]);
+            store_row32_bf16(orow + col, f, p.N - col);
+        }
+    }
+}
+
+// Cross-entropy partials of one 256-column tile of row `row` ("Allow reductions
+// in matmul epilogues", fusion example: the row max, exp(z - max) and its sum,
+// and the label logit selected by comparing the column index with the label):
+//   part_max = max_n z,  part_sum = sum_n exp(z - part_max)  over the tile's
+//   columns n < N; label_logit = z[label] if the label falls in this tile.
+// The running (max, sum) is rescaled chunk by chunk (32 columns at a time).
+__device__ __forceinline__ void epi_xent_partial(const GemmParams &p, uint32_t taddr, int row, int nb)
+{
+    const bool row_ok = row < p.M;
+    const int lab = row_ok ? p.labels[row] : -1;
+    const int lab_local = lab - nb * BN;
+    float mx = -CUDART_INF_F, s = 0.f, zl = 0.f;
+    bool have_label = false;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c, v);
+        tmem_wait_ld();
+        const int nvalid = p.N - col;  // >= 8 here; only the last tile is ragged
+        float cm = -CUDART_INF_F;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nvalid)
+                cm = fmaxf(cm, __uint_as_float(v[i]));
+        const int li = lab_local - c;
+        if (static_cast<unsigned>(li) < 32u) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i == li)
+                    zl = __uint_as_float(v[i]);
+            have_label = true;
+        }
+        const float nm = fmaxf(mx, cm);
+        s *= exp2f((mx - nm) * LOG2E);  // mx = -inf on the first chunk: factor 0, s is 0
+        float cs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nvalid)
+                cs += exp2f((__uint_as_float(v[i]) - nm) * LOG2E);
+        s += cs;
+        mx = nm;
+    }
+    if (row_ok) {
+        const size_t o = static_cast<size_t>(row) * p.num_n_blocks + nb;
+        p.part_max[o] = mx;
+        p.part_sum[o] = s;
+        if (have_label && lab < p.N)
+            p.label_logit[row] = zl;
+    }
+}
+
+// Gradient of one tile, recomputed from the accumulator ("Allow reductions in
+// matmul epilogues", the yhatminusy output):
+//   grad = bf16_rn(exp((z - row_max) - row_logsum) - [n == label])
+__device__ __forceinline__ void epi_xent_grad(const GemmParams &p, uint32_t taddr, int row, int nb)
+{
+    const bool row_ok = row < p.M;
+    const int lab = row_ok ? p.labels[row] : -1;
+    const int lab_local = lab - nb * BN;
+    const float rmax = row_ok ? p.row_max[row] : 0.f;
+    const float rls = row_ok ? p.row_logsum[row] : 0.f;
+    __nv_bfloat16 *grow = static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(row) * p.N;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c, v);
+        tmem_wait_ld();
+        if (row_ok) {
+            const int li = lab_local - c;
+            float g[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                g[i] = exp2f(((__uint_as_float(v[i]) - rmax) - rls) * LOG2E);
+                if (i == li)
+                    g[i] -= 1.f;
+            }
+            store_row32_bf16(grow + col, g, p.N - col);
+        }
+    }
+}
+
+}  // namespace
+}  // namespace lf

@@ -41,6 +41,13 @@ cudaError_t launch_gemm_nt(int epi, const CUtensorMap &ta, const CUtensorMap &tb
                            int grid, cudaStream_t s);
 int gemm_smem_bytes();
 
+// CTA-pair variant (cta_group::2, 256x256 tiles; p.num_m_blocks counts
+// 256-row blocks; X and W tensor maps both use 128-row boxes; grid even).
+cudaError_t launch_gemm_nt_pair(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
+                                int grid, cudaStream_t s);
+int gemm_pair_smem_bytes();
+int gemm_pair_max_active_clusters();
+
 cudaError_t launch_xent_combine(const float *part_max, const float *part_sum, const float *label_logit,
                                 const int32_t *labels, int M, int N, int num_n_blocks, float *loss,
                                 float *row_max, float *row_logsum, cudaStream_t s);

@@ -11,7 +11,7 @@ import layout_folding_gb300 as lf
 from layout_folding_gb300 import build as lfbuild
 
 EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
-            "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning"}
+            "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc"}
 
 
 @pytest.fixture(scope="module")

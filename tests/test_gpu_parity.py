@@ -68,9 +68,19 @@ def _device():
     lf.check_device_error()
 
 
+@pytest.fixture(params=[1, 2], ids=["cta1", "pair"])
+def variant(request):
+    """Run the test on the single-CTA (128x256) and the CTA-pair (256x256,
+    cta_group::2) tensor-core kernels."""
+    lf.set_tuning(-1, request.param)
+    yield request.param
+    lf.check_device_error()
+    lf.set_tuning(-1, -1)
+
+
 # -------------------------------------------------------------- gemm_nt
 
-def test_gemm_nt_tiny_full():
+def test_gemm_nt_tiny_full(variant):
     inp = workload("tiny")
     x, w = inp["x"], inp["w"]
     out = lf.gemm_nt(x.to(DEV), w.to(DEV))
@@ -80,14 +90,14 @@ def test_gemm_nt_tiny_full():
 
 
 @pytest.mark.parametrize("M,N,K", [(200, 520, 200), (130, 264, 72), (1, 8, 8), (257, 1032, 4104)])
-def test_gemm_nt_ragged_full(M, N, K):
+def test_gemm_nt_ragged_full(M, N, K, variant):
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
     out = lf.gemm_nt(x.to(DEV), w.to(DEV))
     torch.cuda.synchronize()
     assert_gemm_close(f64(out), oracle.gemm_nt(x, w), "ragged %dx%dx%d" % (M, N, K))
 
 
-def test_gemm_nt_persistent_many_tiles():
+def test_gemm_nt_persistent_many_tiles(variant):
     # more tiles than SMs: every CTA runs several tiles through both TMEM buffers
     M, N, K = 1280, 8192, 512
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
@@ -97,7 +107,7 @@ def test_gemm_nt_persistent_many_tiles():
     assert_gemm_close(f64(out)[rows], oracle.gemm_nt_rows(x, w, rows), "persistent")
 
 
-def test_gemm_nt_onehot_rows_select_weight_columns_exactly():
+def test_gemm_nt_onehot_rows_select_weight_columns_exactly(variant):
     M, N, K = 256, 512, 256
     w = synthetic.bf16_normal((N, K), 1.0, 5)
     ks = (np.arange(M) * 37 + 11) % K
@@ -108,7 +118,7 @@ def test_gemm_nt_onehot_rows_select_weight_columns_exactly():
     assert torch.equal(out.view(torch.int16), want.contiguous().view(torch.int16))
 
 
-def test_gemm_nt_projection_full_size():
+def test_gemm_nt_projection_full_size(variant):
     wl = synthetic.WORKLOADS["nt_projection"]
     inp = workload("nt_projection")
     x, w = inp["x"], inp["w"]
@@ -165,13 +175,13 @@ def _xent_check(x, w, lab, rows=None, what=""):
     return loss, grad
 
 
-def test_xent_tiny_full():
+def test_xent_tiny_full(variant):
     inp = workload("tiny")
     _xent_check(inp["x"], inp["w"], inp["labels"], what="tiny")
 
 
 @pytest.mark.parametrize("M,N,K", [(200, 1000, 136), (64, 8, 64), (129, 776, 520)])
-def test_xent_ragged_full(M, N, K):
+def test_xent_ragged_full(M, N, K, variant):
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
     lab = synthetic.labels_uniform(M, N)
     edges = [0, N - 1, min(255, N - 1), min(256, N - 1), min(767, N - 1), min(768, N - 1)]
@@ -180,7 +190,7 @@ def test_xent_ragged_full(M, N, K):
     _xent_check(x, w, lab, what="ragged %dx%dx%d" % (M, N, K))
 
 
-def test_xent_zero_weight_gives_ln_n():
+def test_xent_zero_weight_gives_ln_n(variant):
     M, N, K = 192, 2048, 128
     x = synthetic.bf16_normal((M, K), 1.0, 0)
     w = torch.zeros(N, K, dtype=torch.bfloat16)
@@ -192,7 +202,7 @@ def test_xent_zero_weight_gives_ln_n():
     assert_grad_close(f64(grad), want, "zero weight")
 
 
-def test_xent_large_logits():
+def test_xent_large_logits(variant):
     M, N, K = 256, 1536, 256
     x, w = synthetic.make_gemm_inputs(M, N, K, 30.0, 1.0 / math.sqrt(K))
     lab = synthetic.labels_uniform(M, N)
@@ -211,7 +221,7 @@ def test_xent_launch_counts():
     assert (b1 - b0, b2 - b1) == (2, 3)
 
 
-def test_xent_grad_full_size():
+def test_xent_grad_full_size(variant):
     wl = synthetic.WORKLOADS["xent_grad"]
     inp = workload("xent_grad")
     lab = inp["labels"].clone()
@@ -220,7 +230,7 @@ def test_xent_grad_full_size():
     _xent_check(inp["x"], inp["w"], lab, rows=rows, what="xent_grad")
 
 
-def test_xent_loss_only_full_size():
+def test_xent_loss_only_full_size(variant):
     wl = synthetic.WORKLOADS["xent_loss"]
     inp = workload("xent_loss")
     lab = inp["labels"].clone()

@@ -1,0 +1,46 @@
+"""Failure detection without a GPU fault: a device-side wait that nothing
+satisfies must run out after its limit, be reported through
+lf_check_device_error as LF_ERR_DEVICE_TIMEOUT, and leave the CUDA context
+usable.  The stall is made by the library's test hook (the first CTA never
+arms its first stage, so its MMA wait can never complete); every other wait is
+bounded too, so all CTAs unwind: copies in flight land, issued MMAs drain and
+TMEM is freed before they exit.  No trap, no assert, no bad address."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import layout_folding_gb300 as lf
+import oracle
+from layout_folding_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["cta1", "pair"])
+def test_stalled_wait_times_out_and_context_survives(variant):
+    torch.cuda.set_device(0)
+    M, N, K = 256, 1024, 512
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    xd, wd = x.to(DEV), w.to(DEV)
+    lf.check_device_error()                      # start from a clean error word
+    lf.set_tuning(-1, variant)
+    lf.set_test_hooks(True, 200_000_000)         # 200 ms limit per wait
+    try:
+        lf.gemm_nt(xd, wd)
+        with pytest.raises(lf.LayoutFoldError) as info:
+            lf.check_device_error()
+        assert info.value.status == 6            # LF_ERR_DEVICE_TIMEOUT
+    finally:
+        lf.set_test_hooks(False, 0)
+    try:
+        lf.check_device_error()                  # the word was cleared by the read
+        out = lf.gemm_nt(xd, wd)
+        lf.check_device_error()
+    finally:
+        lf.set_tuning(-1, -1)
+    ref = oracle.gemm_nt(x, w)
+    got = out.float().cpu().double().numpy()
+    assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
