@@ -58,7 +58,11 @@ typedef enum {
  *         as "Feature request: Schedule a small matmul op as a reduction (or
  *         pointwise) op" (NVIDIA/Fuser issue 3646) proposes; N % 8 == 0 is still required.
  *   x, w, out must be 16-byte aligned.  out must not overlap x or w.
- * One kernel launch per call.
+ * One kernel launch per call.  When the output has too few 256x256 tiles to
+ * keep every SM busy, the launch splits the K loop across SMs (stream-K) and
+ * uses a library-owned per-device workspace (about 20 MB, allocated on first
+ * such call); calls on one device must then not run concurrently on
+ * different streams.
  */
 lf_status gemm_nt(const void *x, const void *w, void *out,
                   int64_t M, int64_t N, int64_t K, cudaStream_t stream);
@@ -172,7 +176,10 @@ lf_status lf_device_query(int *num_sms, int *pair_clusters);
  *     shared-memory loads each GEMM CTA prefetches its operand slices into
  *     L2; 0 disables it, a negative value restores the default (off).
  *   gemm_variant: 1 = single-CTA 128x256 tiles, 2 = CTA-pair 256x256 tiles
- *     (tcgen05 cta_group::2), anything else = automatic (pairs when M > 128).
+ *     (tcgen05 cta_group::2) by whole tiles, 3 = CTA-pair tiles with the K
+ *     iterations split evenly over all pairs (stream-K), anything else =
+ *     automatic (pairs when M > 128; stream-K when whole tiles would leave
+ *     more than 15% of the pairs idle in the last wave).
  */
 void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant);
 

@@ -20,6 +20,8 @@ struct DeviceState {
     bool arch_ok = false;
     int num_sms = 0;
     int pair_clusters = 0;    // co-resident CTA pairs of the pair kernel
+    void *sk_ws = nullptr;    // stream-K partial slots + flags (fixed size, zeroed once)
+    unsigned sk_epoch = 0;    // last epoch handed to a stream-K launch
     int *err_word = nullptr;  // device int[64]; [0] = first error code
     void *ws = nullptr;       // cross-entropy workspace (grow-only)
     size_t ws_bytes = 0;
@@ -31,7 +33,7 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_inject{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_l2_prefetch{-1};  // -1: per-shape default
-std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA tiles, 2 CTA-pair tiles
+std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA, 2 CTA-pair whole tiles, 3 CTA-pair stream-K
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -112,6 +114,25 @@ lf_status ensure_workspace(DeviceState *d, size_t bytes, void **ws)
     return LF_OK;
 }
 
+// Stream-K partial slots (2 per pair) and their flags, allocated on first use.
+lf_status ensure_sk_workspace(DeviceState *d)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (d->sk_ws)
+        return LF_OK;
+    const size_t slots = static_cast<size_t>(2 * d->pair_clusters) * lf::SK_SLOT_FLOATS * sizeof(float);
+    const size_t bytes = slots + static_cast<size_t>(2 * d->pair_clusters) * sizeof(unsigned);
+    if (cudaMalloc(&d->sk_ws, bytes) != cudaSuccess || cudaMemset(d->sk_ws, 0, bytes) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        if (d->sk_ws)
+            cudaFree(d->sk_ws);
+        d->sk_ws = nullptr;
+        return LF_ERR_WORKSPACE;
+    }
+    return LF_OK;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -135,16 +156,18 @@ bool make_tmap(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, uint32_
 // Everything one GEMM launch needs: variant, tensor maps, parameters, grid.
 struct GemmPlan {
     bool pair = false;
+    DeviceState *dev = nullptr;
     CUtensorMap ta, tb;
     lf::GemmParams p;
     int grid = 0;
 };
 
-lf_status plan_gemm(const DeviceState *d, const void *x, const void *w, int64_t M, int64_t N, int64_t K,
+lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int64_t N, int64_t K,
                     GemmPlan *g)
 {
     const int variant = g_variant.load();
-    g->pair = d->pair_clusters > 0 && (variant == 2 || (variant < 0 && M > lf::BM));
+    g->dev = d;
+    g->pair = d->pair_clusters > 0 && (variant >= 2 || (variant < 0 && M > lf::BM));
     const int tile_m = g->pair ? 2 * lf::BM : lf::BM;
     if (!make_tmap(&g->ta, x, M, K, lf::BM) || !make_tmap(&g->tb, w, N, K, g->pair ? lf::BN / 2 : lf::BN))
         return LF_ERR_LAUNCH;
@@ -162,15 +185,42 @@ lf_status plan_gemm(const DeviceState *d, const void *x, const void *w, int64_t 
     p.inject = g_inject.load();
     const int pf = g_l2_prefetch.load();
     p.l2_prefetch = pf >= 0 ? pf : 0;
-    if (g->pair)
-        g->grid = 2 * (p.num_tiles < d->pair_clusters ? p.num_tiles : d->pair_clusters);
-    else
+    if (g->pair) {
+        // Whole tiles leave pairs idle when the last wave is short; then split
+        // the K iterations evenly over all pairs instead (stream-K).
+        const int P = d->pair_clusters;
+        const int waves = (p.num_tiles + P - 1) / P;
+        const double busy = static_cast<double>(p.num_tiles) / (static_cast<double>(waves) * P);
+        p.streamk = (variant == 3) ? 1 : 0;  // automatic choice waits for the M-block-grouped split
+        (void)busy;
+        if (p.streamk) {
+            lf_status st = ensure_sk_workspace(d);
+            if (st != LF_OK)
+                return st;
+            p.sk_partials = static_cast<float *>(d->sk_ws);
+            p.sk_flags = reinterpret_cast<unsigned *>(static_cast<char *>(d->sk_ws) + static_cast<size_t>(2 * P) *
+                                                                                         lf::SK_SLOT_FLOATS *
+                                                                                         sizeof(float));
+            // every pair must get at least one K iteration: a pair with an
+            // empty share would never write the flag its tile's owner waits on
+            const long long U = static_cast<long long>(p.num_tiles) * p.num_k_blocks;
+            g->grid = 2 * static_cast<int>(U < P ? U : P);
+        } else {
+            g->grid = 2 * (p.num_tiles < P ? p.num_tiles : P);
+        }
+    } else
         g->grid = p.num_tiles < d->num_sms ? p.num_tiles : d->num_sms;
     return LF_OK;
 }
 
-cudaError_t run_gemm(int epi, const GemmPlan &g, cudaStream_t stream)
+cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
 {
+    if (g.p.streamk) {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        g.p.epoch = ++g.dev->sk_epoch;  // each launch's flags are distinct from every earlier one
+        if (g.p.epoch == 0)
+            g.p.epoch = ++g.dev->sk_epoch;
+    }
     return g.pair ? lf::launch_gemm_nt_pair(epi, g.ta, g.tb, g.p, g.grid, stream)
                   : lf::launch_gemm_nt(epi, g.ta, g.tb, g.p, g.grid, stream);
 }

@@ -40,10 +40,69 @@ constexpr int PAIR_ACC_BUFS = 2;
 constexpr int PAIR_TMEM_COLS = PAIR_ACC_BUFS * BN;  // 512
 constexpr int PAIR_THREADS = 192;
 constexpr int PAIR_EPI_WARPS = 4;
-constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 1;
+constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2;
 constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + PAIR_NUM_BARS * 8 + 16;
 constexpr uint32_t PAIR_IDESC = idesc_bf16_f32(PAIR_M, BN);
 constexpr uint64_t ABORT_SETTLE_NS = 100000;  // after an abort: let copies in flight land
+
+// A run of K blocks [kb0, kb1) of one output tile.
+struct Seg {
+    int tile, kb0, kb1;
+};
+
+// The sequence of segments one pair works on.  Whole tiles: tiles pair,
+// pair + num_pairs, ...  Stream-K: the pair's contiguous share
+// [U*pair/P, U*(pair+1)/P) of the U = tiles x K-blocks iterations, cut at tile
+// boundaries -- so only a pair's first segment can start inside a tile and
+// only its last can end inside one.
+struct WorkIter {
+    bool sk;
+    int tile, step, ntiles, KB;
+    long long u, u_end;
+    __device__ WorkIter(const GemmParams &p, int pair, int num_pairs)
+    {
+        sk = p.streamk != 0;
+        KB = p.num_k_blocks;
+        ntiles = p.num_tiles;
+        tile = pair;
+        step = num_pairs;
+        const long long U = static_cast<long long>(p.num_tiles) * KB;
+        u = U * pair / num_pairs;
+        u_end = U * (pair + 1) / num_pairs;
+    }
+    __device__ bool next(Seg &g)
+    {
+        if (!sk) {
+            if (tile >= ntiles)
+                return false;
+            g.tile = tile;
+            g.kb0 = 0;
+            g.kb1 = KB;
+            tile += step;
+            return true;
+        }
+        if (u >= u_end)
+            return false;
+        g.tile = static_cast<int>(u / KB);
+        g.kb0 = static_cast<int>(u % KB);
+        const long long end = g.kb0 + (u_end - u);
+        g.kb1 = end < KB ? static_cast<int>(end) : KB;
+        u += g.kb1 - g.kb0;
+        return true;
+    }
+};
+
+// Stream-K: number of pairs after `pair` that hold the rest of `tile`
+// (K blocks [kb1, KB)), i.e. whose shares start before the tile ends.
+__device__ __forceinline__ int sk_contributors(const GemmParams &p, int pair, int num_pairs, int tile)
+{
+    const long long U = static_cast<long long>(p.num_tiles) * p.num_k_blocks;
+    const long long tile_end = static_cast<long long>(tile + 1) * p.num_k_blocks;
+    int n = 0;
+    for (int c = pair + 1; c < num_pairs && U * c / num_pairs < tile_end; ++c)
+        ++n;
+    return n;
+}
 
 template <int EPI>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
@@ -58,6 +117,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const uint32_t sB = base + PAIR_STAGES * PAIR_A_BYTES;
     const uint32_t bar0 = base + PAIR_STAGES * PAIR_STAGE_BYTES;
     const uint32_t drain_bar = bar0 + 8u * (2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS);
+    const uint32_t skw_bar = drain_bar + 8u;  // the 4 epilogue warps finished writing a partial
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 #define FULL_BAR(s) (bar0 + 8u * (s))
@@ -82,6 +142,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             mbar_init(TEMPTY_BAR(b), 2 * PAIR_EPI_WARPS);  // leader: one arrive per epilogue warp of each CTA
         }
         mbar_init(drain_bar, 1);
+        mbar_init(skw_bar, PAIR_EPI_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -110,12 +171,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             for (int s = 0; s < PAIR_STAGES; ++s)
                 armed[s] = 0;
             bool ok = true, first = true;
-            for (int tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
-                const int mb = tile % p.num_m_blocks;
-                const int nb = tile / p.num_m_blocks;
+            WorkIter it(p, pair, num_pairs);
+            for (Seg g; ok && it.next(g);) {
+                const int mb = g.tile % p.num_m_blocks;
+                const int nb = g.tile / p.num_m_blocks;
                 const int arow = mb * PAIR_M + static_cast<int>(rank) * BM;
                 const int brow = nb * BN + static_cast<int>(rank) * (BN / 2);
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = g.kb0; kb < g.kb1; ++kb) {
                     if (!wait_bar(EMPTY_BAR(stage), phase ^ 1u, abort_flag, p, ERR_PRODUCER, peer_abort)) {
                         ok = false;
                         break;
@@ -151,12 +213,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < p.num_tiles; tile += num_pairs) {
+            WorkIter it(p, pair, num_pairs);
+            for (Seg g; ok && it.next(g);) {
                 if (!wait_bar(TEMPTY_BAR(acc), acc_phase ^ 1u, abort_flag, p, ERR_MMA_ACC, peer_abort))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = g.kb0; kb < g.kb1; ++kb) {
                     if (!wait_bar(FULL_BAR(stage), phase, abort_flag, p, ERR_MMA_FULL, peer_abort)) {
                         ok = false;
                         break;
@@ -167,7 +230,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / PAIR_UMMA_K; ++k)
                         umma_f16_pair(d_tmem, smem_desc_k128(a0 + k * PAIR_UMMA_K * 2),
-                                      smem_desc_k128(b0 + k * PAIR_UMMA_K * 2), PAIR_IDESC, (kb | k) != 0 ? 1u : 0u);
+                                      smem_desc_k128(b0 + k * PAIR_UMMA_K * 2), PAIR_IDESC,
+                                      (kb != g.kb0 || k != 0) ? 1u : 0u);
                     umma_commit_pair_mc(EMPTY_BAR(stage), 0x3);  // both CTAs may refill this slot
                     if (++stage == PAIR_STAGES) {
                         stage = 0;
@@ -191,21 +255,56 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         const int q = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = pair; tile < p.num_tiles; tile += num_pairs) {
-            const int mb = tile % p.num_m_blocks;
-            const int nb = tile / p.num_m_blocks;
+        uint32_t skw_phase = 0;
+        WorkIter it(p, pair, num_pairs);
+        for (Seg g; it.next(g);) {
+            const int mb = g.tile % p.num_m_blocks;
+            const int nb = g.tile / p.num_m_blocks;
             const bool ok = wait_bar(TFULL_BAR(acc), acc_phase, abort_flag, p, ERR_EPI, peer_abort);
             if (!__all_sync(0xffffffffu, ok))
                 break;
             tc_fence_after();
-            const int row = mb * PAIR_M + static_cast<int>(rank) * BM + q * 32 + lane;
+            const int rloc = q * 32 + lane;
+            const int row = mb * PAIR_M + static_cast<int>(rank) * BM + rloc;
             const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
-            if (EPI == EPI_STORE)
-                epi_store(p, taddr, row, nb);
-            else if (EPI == EPI_XENT_PARTIAL)
-                epi_xent_partial(p, taddr, row, nb);
-            else
-                epi_xent_grad(p, taddr, row, nb);
+            if (g.kb0 != 0) {
+                // Not the tile's first K blocks: hand the partial sum to the
+                // pair that owns the tile's start.
+                epi_write_partial(taddr, p.sk_partials + static_cast<size_t>(pair * 2 + rank) * SK_SLOT_FLOATS, rloc);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(skw_bar);
+                if (warp == 2 && lane == 0 &&
+                    wait_bar(skw_bar, skw_phase, abort_flag, p, ERR_SK_SLOT, peer_abort)) {
+                    __threadfence();
+                    st_release_gpu(p.sk_flags + pair * 2 + rank, p.epoch);
+                }
+                skw_phase ^= 1u;
+            } else {
+                PartialAdd pa = {nullptr, 0, rloc};
+                if (g.kb1 < p.num_k_blocks) {
+                    // The tile's first K blocks, the rest held by the next pairs:
+                    // wait for their partials, then finish the tile.
+                    const int n = sk_contributors(p, pair, num_pairs, g.tile);
+                    bool got = true;
+                    if (lane == 0)
+                        for (int e = 0; e < n && got; ++e)
+                            got = wait_flag(p.sk_flags + (pair + 1 + e) * 2 + rank, p.epoch, abort_flag, p,
+                                            peer_abort);
+                    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                    if (!got)
+                        break;
+                    pa.slot = p.sk_partials + static_cast<size_t>((pair + 1) * 2 + rank) * SK_SLOT_FLOATS;
+                    pa.count = n;
+                }
+                if (EPI == EPI_STORE)
+                    epi_store(p, taddr, row, nb, pa);
+                else if (EPI == EPI_XENT_PARTIAL)
+                    epi_xent_partial(p, taddr, row, nb, pa);
+                else
+                    epi_xent_grad(p, taddr, row, nb, pa);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)

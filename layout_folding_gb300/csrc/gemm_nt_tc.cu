@@ -202,12 +202,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const int row = mb * BM + q * 32 + lane;
             const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
+            const PartialAdd none = {nullptr, 0, 0};
             if (EPI == EPI_STORE)
-                epi_store(p, taddr, row, nb);
+                epi_store(p, taddr, row, nb, none);
             else if (EPI == EPI_XENT_PARTIAL)
-                epi_xent_partial(p, taddr, row, nb);
+                epi_xent_partial(p, taddr, row, nb, none);
             else
-                epi_xent_grad(p, taddr, row, nb);
+                epi_xent_grad(p, taddr, row, nb, none);
             tc_fence_before();
             mbar_arrive(TEMPTY_BAR(acc));
             if (++acc == ACC_BUFS) {

@@ -25,6 +25,8 @@ constexpr int ERR_MMA_FULL = 0x102;   // stage never landed
 constexpr int ERR_MMA_ACC = 0x103;    // accumulator never released by the epilogue
 constexpr int ERR_EPI = 0x104;        // accumulator never completed
 constexpr int ERR_DRAIN = 0x105;      // copies / MMAs did not finish while unwinding
+constexpr int ERR_SK_FLAG = 0x106;    // a stream-K partial never arrived
+constexpr int ERR_SK_SLOT = 0x107;    // a CTA's own partial write did not complete
 
 // Record `code` (first writer wins), raise this CTA's abort flag and, in a
 // CTA pair, the peer's (peer_abort: its shared::cluster address, 0 if none).
@@ -96,12 +98,76 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16 *dst, const float
     }
 }
 
+// Partial accumulators of other CTA pairs to add to this tile (stream-K
+// fix-up): `count` slots starting at `slot`, consecutive pairs 2 slots apart.
+struct PartialAdd {
+    const float *slot;
+    int count;
+    int row;  // this thread's row within its CTA's 128 rows
+};
+
+// Read 32 accumulator columns [c, c+32) of this thread's row from TMEM and
+// add the partials, in pair order.
+__device__ __forceinline__ void load_chunk(uint32_t taddr, int c, const PartialAdd &pa, uint32_t (&v)[32])
+{
+    tmem_ld_32x32b_x32(taddr + c, v);
+    tmem_wait_ld();
+    for (int e = 0; e < pa.count; ++e) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(pa.slot + static_cast<size_t>(e) * 2 * SK_SLOT_FLOATS);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 f = __ldcg(s4 + (c / 4 + i) * BM + pa.row);
+            v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) + f.x);
+            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + f.y);
+            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + f.z);
+            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + f.w);
+        }
+    }
+}
+
+// Store this thread's whole accumulator row (256 fp32) into a stream-K slot.
+__device__ __forceinline__ void epi_write_partial(uint32_t taddr, float *slot, int row)
+{
+    float4 *s4 = reinterpret_cast<float4 *>(slot);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            __stcg(s4 + (c / 4 + i) * BM + row,
+                   make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                               __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+    }
+}
+
+// Bounded wait until *flag == epoch (acquire); false on abort or time-out.
+__device__ __noinline__ bool wait_flag(const unsigned *flag, unsigned epoch, volatile int *abort_flag,
+                                       const GemmParams &p, uint32_t peer_abort)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_gpu(flag) == epoch)
+            return true;
+        if ((it & 15u) == 15u) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+                raise_error(p, abort_flag, ERR_SK_FLAG, peer_abort);
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- epilogues
 // Each runs on one epilogue warp: thread `lane` owns output row `row` of the
 // tile, whose accumulator row starts at TMEM address `taddr`.
 
 // out = bf16_rn(acc)
-__device__ __forceinline__ void epi_store(const GemmParams &p, uint32_t taddr, int row, int nb)
+__device__ __forceinline__ void epi_store(const GemmParams &p, uint32_t taddr, int row, int nb,
+                                          const PartialAdd &pa)
 {
     const bool row_ok = row < p.M;
     __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(row) * p.N;
@@ -111,8 +177,7 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, uint32_t taddr, i
         if (col >= p.N)
             break;  // warp-uniform
         uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + c, v);
-        tmem_wait_ld();
+        load_chunk(taddr, c, pa, v);
         if (row_ok) {
             float f[32];
 #pragma unroll
@@ -129,7 +194,8 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, uint32_t taddr, i
 //   part_max = max_n z,  part_sum = sum_n exp(z - part_max)  over the tile's
 //   columns n < N; label_logit = z[label] if the label falls in this tile.
 // The running (max, sum) is rescaled chunk by chunk (32 columns at a time).
-__device__ __forceinline__ void epi_xent_partial(const GemmParams &p, uint32_t taddr, int row, int nb)
+__device__ __forceinline__ void epi_xent_partial(const GemmParams &p, uint32_t taddr, int row, int nb,
+                                                 const PartialAdd &pa)
 {
     const bool row_ok = row < p.M;
     const int lab = row_ok ? p.labels[row] : -1;
@@ -142,8 +208,7 @@ __device__ __forceinline__ void epi_xent_partial(const GemmParams &p, uint32_t t
         if (col >= p.N)
             break;  // warp-uniform
         uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + c, v);
-        tmem_wait_ld();
+        load_chunk(taddr, c, pa, v);
         const int nvalid = p.N - col;  // >= 8 here; only the last tile is ragged
         float cm = -CUDART_INF_F;
 #pragma unroll
@@ -180,7 +245,8 @@ __device__ __forceinline__ void epi_xent_partial(const GemmParams &p, uint32_t t
 // Gradient of one tile, recomputed from the accumulator ("Allow reductions in
 // matmul epilogues", the yhatminusy output):
 //   grad = bf16_rn(exp((z - row_max) - row_logsum) - [n == label])
-__device__ __forceinline__ void epi_xent_grad(const GemmParams &p, uint32_t taddr, int row, int nb)
+__device__ __forceinline__ void epi_xent_grad(const GemmParams &p, uint32_t taddr, int row, int nb,
+                                              const PartialAdd &pa)
 {
     const bool row_ok = row < p.M;
     const int lab = row_ok ? p.labels[row] : -1;
@@ -194,8 +260,7 @@ __device__ __forceinline__ void epi_xent_grad(const GemmParams &p, uint32_t tadd
         if (col >= p.N)
             break;  // warp-uniform
         uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + c, v);
-        tmem_wait_ld();
+        load_chunk(taddr, c, pa, v);
         if (row_ok) {
             const int li = lab_local - c;
             float g[32];

@@ -34,7 +34,18 @@ struct GemmParams {
     unsigned long long timeout_ns;
     int inject;                 // test hook: 1 = CTA 0 never loads its first stage
     int l2_prefetch;            // k-blocks the L2 prefetch stream runs ahead of the loads (0 = off)
+    // stream-K (pair kernel): the tiles' K iterations are split evenly over
+    // the pairs; a tile split across pairs is finished by the pair holding its
+    // first K block, which adds the other pairs' fp32 partials.
+    int streamk;                // 1 = stream-K split, 0 = whole tiles
+    unsigned epoch;             // value the flags of this launch carry
+    float *sk_partials;         // [2 * pairs][128 * 256] fp32 partial accumulators
+    unsigned *sk_flags;         // [2 * pairs] = epoch once the slot is written
 };
+
+// One stream-K partial slot: a CTA's 128 rows x 256 columns of fp32,
+// stored as [column / 4][row][4] so each warp access is contiguous.
+constexpr int SK_SLOT_FLOATS = BM * BN;
 
 // Launchers (host).  Return cudaSuccess or the launch error.
 cudaError_t launch_gemm_nt(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,

@@ -68,10 +68,11 @@ def _device():
     lf.check_device_error()
 
 
-@pytest.fixture(params=[1, 2], ids=["cta1", "pair"])
+@pytest.fixture(params=[1, 2, 3], ids=["cta1", "pair", "pair_streamk"])
 def variant(request):
-    """Run the test on the single-CTA (128x256) and the CTA-pair (256x256,
-    cta_group::2) tensor-core kernels."""
+    """Run the test on the single-CTA (128x256) kernel, the CTA-pair (256x256,
+    cta_group::2) kernel by whole tiles, and the CTA-pair kernel with the K
+    iterations split evenly over all pairs (stream-K)."""
     lf.set_tuning(-1, request.param)
     yield request.param
     lf.check_device_error()

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-@pytest.mark.parametrize("variant", [1, 2], ids=["cta1", "pair"])
+@pytest.mark.parametrize("variant", [1, 2, 3], ids=["cta1", "pair", "pair_streamk"])
 def test_stalled_wait_times_out_and_context_survives(variant):
     torch.cuda.set_device(0)
     M, N, K = 256, 1024, 512
