@@ -191,8 +191,17 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
         const int P = d->pair_clusters;
         const int waves = (p.num_tiles + P - 1) / P;
         const double busy = static_cast<double>(p.num_tiles) / (static_cast<double>(waves) * P);
-        p.streamk = (variant == 3) ? 1 : 0;  // automatic choice waits for the M-block-grouped split
-        (void)busy;
+        // Stream-K groups: G groups of MB pairs (one per M block), G <= V so
+        // that no pair gets an empty share -- a tile's owner waits on every
+        // later group's partial, so each must write one.
+        const long long V = static_cast<long long>(p.num_n_blocks) * p.num_k_blocks;
+        long long G = p.num_m_blocks <= P ? P / p.num_m_blocks : 0;
+        if (G > V)
+            G = V;
+        const double sk_busy = static_cast<double>(G * p.num_m_blocks) / P;
+        p.streamk = (G > 0 && (variant == 3 || (variant < 0 && p.num_k_blocks >= 8 && sk_busy > busy + 0.05)))
+                        ? 1
+                        : 0;
         if (p.streamk) {
             lf_status st = ensure_sk_workspace(d);
             if (st != LF_OK)
@@ -201,10 +210,7 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
             p.sk_flags = reinterpret_cast<unsigned *>(static_cast<char *>(d->sk_ws) + static_cast<size_t>(2 * P) *
                                                                                          lf::SK_SLOT_FLOATS *
                                                                                          sizeof(float));
-            // every pair must get at least one K iteration: a pair with an
-            // empty share would never write the flag its tile's owner waits on
-            const long long U = static_cast<long long>(p.num_tiles) * p.num_k_blocks;
-            g->grid = 2 * static_cast<int>(U < P ? U : P);
+            g->grid = 2 * static_cast<int>(G * p.num_m_blocks);
         } else {
             g->grid = 2 * (p.num_tiles < P ? p.num_tiles : P);
         }

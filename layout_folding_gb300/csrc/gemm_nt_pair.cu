@@ -32,7 +32,7 @@ namespace {
 
 constexpr int PAIR_M = 2 * BM;          // 256 rows of X per pair tile
 constexpr int PAIR_UMMA_K = 16;
-constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_STAGES = 7;
 constexpr int PAIR_A_BYTES = BM * BK * 2;          // 16 KiB: this CTA's 128 rows of X
 constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;    // 16 KiB: this CTA's 128 rows of W
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
@@ -50,56 +50,68 @@ struct Seg {
     int tile, kb0, kb1;
 };
 
-// The sequence of segments one pair works on.  Whole tiles: tiles pair,
-// pair + num_pairs, ...  Stream-K: the pair's contiguous share
-// [U*pair/P, U*(pair+1)/P) of the U = tiles x K-blocks iterations, cut at tile
-// boundaries -- so only a pair's first segment can start inside a tile and
-// only its last can end inside one.
+// The sequence of segments one pair works on.
+// Whole tiles: tiles pair, pair + num_pairs, ... (M-block fastest).
+// Stream-K: the pairs form G = num_pairs / MB groups of MB pairs (MB = M
+// blocks); pair m of group g works on M block m.  The V = N-tiles x K-blocks
+// "column iterations" are split evenly over the groups -- group g takes
+// [V*g/G, V*(g+1)/G), cut at N-tile boundaries -- so the MB pairs of a group
+// walk the same K slices of the same W tile in lockstep and W is fetched from
+// HBM once, while every pair gets an equal share.  Only a pair's first
+// segment can start inside a tile and only its last can end inside one.
 struct WorkIter {
     bool sk;
-    int tile, step, ntiles, KB;
-    long long u, u_end;
+    int tile, step, ntiles, KB, MB, m;
+    long long v, v_end;
     __device__ WorkIter(const GemmParams &p, int pair, int num_pairs)
     {
         sk = p.streamk != 0;
         KB = p.num_k_blocks;
+        MB = p.num_m_blocks;
         ntiles = p.num_tiles;
         tile = pair;
         step = num_pairs;
-        const long long U = static_cast<long long>(p.num_tiles) * KB;
-        u = U * pair / num_pairs;
-        u_end = U * (pair + 1) / num_pairs;
+        const int G = num_pairs / MB;
+        const int g = pair / MB;
+        m = pair % MB;
+        const long long V = static_cast<long long>(p.num_n_blocks) * KB;
+        v = V * g / G;
+        v_end = V * (g + 1) / G;
     }
-    __device__ bool next(Seg &g)
+    __device__ bool next(Seg &s)
     {
         if (!sk) {
             if (tile >= ntiles)
                 return false;
-            g.tile = tile;
-            g.kb0 = 0;
-            g.kb1 = KB;
+            s.tile = tile;
+            s.kb0 = 0;
+            s.kb1 = KB;
             tile += step;
             return true;
         }
-        if (u >= u_end)
+        if (v >= v_end)
             return false;
-        g.tile = static_cast<int>(u / KB);
-        g.kb0 = static_cast<int>(u % KB);
-        const long long end = g.kb0 + (u_end - u);
-        g.kb1 = end < KB ? static_cast<int>(end) : KB;
-        u += g.kb1 - g.kb0;
+        const int nb = static_cast<int>(v / KB);
+        s.tile = m + nb * MB;
+        s.kb0 = static_cast<int>(v % KB);
+        const long long end = s.kb0 + (v_end - v);
+        s.kb1 = end < KB ? static_cast<int>(end) : KB;
+        v += s.kb1 - s.kb0;
         return true;
     }
 };
 
-// Stream-K: number of pairs after `pair` that hold the rest of `tile`
-// (K blocks [kb1, KB)), i.e. whose shares start before the tile ends.
+// Stream-K: number of groups after this pair's group that hold the rest of
+// `tile` (their shares start before the tile's N-tile ends).  Contributor e is
+// pair (g + 1 + e) * MB + m.
 __device__ __forceinline__ int sk_contributors(const GemmParams &p, int pair, int num_pairs, int tile)
 {
-    const long long U = static_cast<long long>(p.num_tiles) * p.num_k_blocks;
-    const long long tile_end = static_cast<long long>(tile + 1) * p.num_k_blocks;
+    const int MB = p.num_m_blocks;
+    const int G = num_pairs / MB;
+    const long long V = static_cast<long long>(p.num_n_blocks) * p.num_k_blocks;
+    const long long tile_end = static_cast<long long>(tile / MB + 1) * p.num_k_blocks;
     int n = 0;
-    for (int c = pair + 1; c < num_pairs && U * c / num_pairs < tile_end; ++c)
+    for (int g = pair / MB + 1; g < G && V * g / G < tile_end; ++g)
         ++n;
     return n;
 }
@@ -282,20 +294,23 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 }
                 skw_phase ^= 1u;
             } else {
-                PartialAdd pa = {nullptr, 0, rloc};
+                PartialAdd pa = {nullptr, 0, 0, rloc};
                 if (g.kb1 < p.num_k_blocks) {
                     // The tile's first K blocks, the rest held by the next pairs:
                     // wait for their partials, then finish the tile.
                     const int n = sk_contributors(p, pair, num_pairs, g.tile);
                     bool got = true;
+                    const int MB = p.num_m_blocks;
+                    const int first = (pair / MB + 1) * MB + pair % MB;  // first contributor pair
                     if (lane == 0)
                         for (int e = 0; e < n && got; ++e)
-                            got = wait_flag(p.sk_flags + (pair + 1 + e) * 2 + rank, p.epoch, abort_flag, p,
+                            got = wait_flag(p.sk_flags + (first + e * MB) * 2 + rank, p.epoch, abort_flag, p,
                                             peer_abort);
                     got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
                     if (!got)
                         break;
-                    pa.slot = p.sk_partials + static_cast<size_t>((pair + 1) * 2 + rank) * SK_SLOT_FLOATS;
+                    pa.slot = p.sk_partials + static_cast<size_t>(first * 2 + rank) * SK_SLOT_FLOATS;
+                    pa.stride = static_cast<size_t>(MB) * 2 * SK_SLOT_FLOATS;
                     pa.count = n;
                 }
                 if (EPI == EPI_STORE)

@@ -99,9 +99,10 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16 *dst, const float
 }
 
 // Partial accumulators of other CTA pairs to add to this tile (stream-K
-// fix-up): `count` slots starting at `slot`, consecutive pairs 2 slots apart.
+// fix-up): `count` slots starting at `slot`, `stride` floats apart.
 struct PartialAdd {
     const float *slot;
+    size_t stride;
     int count;
     int row;  // this thread's row within its CTA's 128 rows
 };
@@ -113,7 +114,7 @@ __device__ __forceinline__ void load_chunk(uint32_t taddr, int c, const PartialA
     tmem_ld_32x32b_x32(taddr + c, v);
     tmem_wait_ld();
     for (int e = 0; e < pa.count; ++e) {
-        const float4 *s4 = reinterpret_cast<const float4 *>(pa.slot + static_cast<size_t>(e) * 2 * SK_SLOT_FLOATS);
+        const float4 *s4 = reinterpret_cast<const float4 *>(pa.slot + static_cast<size_t>(e) * pa.stride);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float4 f = __ldcg(s4 + (c / 4 + i) * BM + pa.row);
