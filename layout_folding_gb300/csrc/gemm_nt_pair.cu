@@ -32,7 +32,7 @@ namespace {
 
 constexpr int PAIR_M = 2 * BM;          // 256 rows of X per pair tile
 constexpr int PAIR_UMMA_K = 16;
-constexpr int PAIR_STAGES = 7;
+constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_A_BYTES = BM * BK * 2;          // 16 KiB: this CTA's 128 rows of X
 constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;    // 16 KiB: this CTA's 128 rows of W
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
