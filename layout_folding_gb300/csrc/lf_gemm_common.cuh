@@ -39,13 +39,12 @@ __device__ __forceinline__ void raise_error(const GemmParams &p, volatile int *a
     atomicCAS(p.err, 0, code);
 }
 
-// Wait for phase `parity` of `bar`; false if the CTA is aborting or the time
-// limit passed (then the error is recorded and the abort flag raised).
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                      const GemmParams &p, int code, uint32_t peer_abort = 0)
+// Slow path of wait_bar, out of line: poll until the phase completes, the CTA
+// aborts or the time limit passes (then the error is recorded and the abort
+// flag raised).
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           const GemmParams &p, int code, uint32_t peer_abort)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity))
@@ -59,6 +58,17 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
             }
         }
     }
+}
+
+// Wait for phase `parity` of `bar`; false if the CTA is aborting or the time
+// limit passed.  The ready case stays inline: an out-of-line call on the
+// MMA-issuing thread, made every K block, measurably starves the tensor pipe.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         const GemmParams &p, int code, uint32_t peer_abort = 0)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    return wait_bar_slow(bar, parity, abort_flag, p, code, peer_abort);
 }
 
 // Same, used while unwinding: ignores the abort flag, keeps the time limit.
