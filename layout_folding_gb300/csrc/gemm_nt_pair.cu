@@ -25,6 +25,8 @@
 //            lane per warp arrives on the leader's accumulator-free barrier.
 // Bounded waits everywhere; an abort raised in either CTA is mirrored into the
 // peer, and both meet at a final cluster barrier before TMEM is freed.
+#include <atomic>
+
 #include "lf_gemm_common.cuh"
 
 namespace lf {
@@ -367,12 +369,30 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t s, cudaLaunchAttribute *at
     return cfg;
 }
 
+// The dynamic shared-memory opt-in is a per-device function attribute: set it
+// once per device and kernel instead of on every launch.
+template <int EPI>
+cudaError_t set_smem_attr_once()
+{
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load() & bit)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(k_gemm_nt_pair<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
+    if (e == cudaSuccess)
+        done.fetch_or(bit);
+    return e;
+}
+
 template <int EPI>
 cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid,
                           cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_nt_pair<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PAIR_SMEM_BYTES);
+    cudaError_t e = set_smem_attr_once<EPI>();
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[1];

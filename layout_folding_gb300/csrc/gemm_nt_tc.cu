@@ -24,6 +24,8 @@
 // an error code in the device error word, raises a CTA-wide abort flag, and
 // all roles unwind -- copies in flight are waited for, issued MMAs are drained
 // and TMEM is freed before the CTA exits.  No trap, no assert.
+#include <atomic>
+
 #include "lf_gemm_common.cuh"
 
 namespace lf {
@@ -231,9 +233,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <int EPI>
+cudaError_t set_smem_attr_once()
+{
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load() & bit)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(k_gemm_nt<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess)
+        done.fetch_or(bit);
+    return e;
+}
+
+template <int EPI>
 cudaError_t launch_t(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid, cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_nt<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = set_smem_attr_once<EPI>();
     if (e != cudaSuccess)
         return e;
     k_gemm_nt<EPI><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, p);
