@@ -349,23 +349,26 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
 # ------------------------------------------------------- CPU oracle legs
 
 def cpu_baseline_gemm(x, w, wl, budget_s=15.0):
-    """Time the oracle (as it stands) on a bounded sample of rows of the workload."""
+    """Time the oracle (as it stands) on a bounded sample of rows of the workload:
+    a probe of 2 rows per thread sizes the sample to about `budget_s` seconds."""
     import numpy as np
 
     import oracle
     xb = oracle._bits(x)
     wb = oracle._bits(w)
-    rows = np.arange(2, dtype=np.int64)
+    threads = oracle.num_threads()
+    probe = np.arange(min(wl.M, 2 * threads), dtype=np.int64)
     t0 = time.perf_counter()
-    oracle.gemm_nt_rows(xb, wb, rows, )
+    oracle.gemm_nt_rows(xb, wb, probe)
     t_probe = max(time.perf_counter() - t0, 1e-3)
-    nrows = int(max(2, min(wl.M, 2 * budget_s / t_probe)))
+    nrows = int(max(probe.size, min(wl.M, probe.size * budget_s / t_probe)))
+    nrows -= nrows % threads if nrows > threads else 0
     rows = np.arange(nrows, dtype=np.int64)
     t0 = time.perf_counter()
     oracle.gemm_nt_rows(xb, wb, rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * nrows * wl.N * wl.K
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle", "seconds": round(dt, 2),
             "sample": "%d of %d rows of X (all %d columns of W, K=%d), fp64 plain loops" % (nrows, wl.M, wl.N, wl.K)}
 
@@ -379,10 +382,13 @@ def run_reference(args, rank, world):
     import oracle
     xb = oracle._bits(inp["x"].reshape(wl.M, wl.K))
     wb = oracle._bits(inp["w"])
-    # size one step to about (budget / (warmup + steps)) seconds
+    # size one step to about (6 * budget / (warmup + steps)) seconds, from a
+    # probe of 2 rows per thread
+    threads = oracle.num_threads()
+    probe = np.arange(min(wl.M, 2 * threads), dtype=np.int64)
     t0 = time.perf_counter()
-    oracle.gemm_nt_rows(xb, wb, np.arange(1, dtype=np.int64))
-    per_row = max(time.perf_counter() - t0, 1e-3)
+    oracle.gemm_nt_rows(xb, wb, probe)
+    per_row = max(time.perf_counter() - t0, 1e-3) / probe.size
     per_step_s = args.cpu_budget * 6 / max(1, args.steps + args.warmup)
     nrows = int(max(1, min(wl.M, per_step_s / per_row)))
     times = []
