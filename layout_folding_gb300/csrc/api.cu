@@ -21,6 +21,7 @@ struct DeviceState {
     int num_sms = 0;
     int pair_clusters = 0;    // co-resident CTA pairs of the pair kernel
     void *sk_ws = nullptr;    // stream-K partial slots + flags (fixed size, zeroed once)
+    void *op_flags = nullptr; // one-pass cross-entropy round flags (2 per pair, zeroed once)
     unsigned sk_epoch = 0;    // last epoch handed to a stream-K launch
     int *err_word = nullptr;  // device int[64]; [0] = first error code
     void *ws = nullptr;       // cross-entropy workspace (grow-only)
@@ -133,6 +134,33 @@ lf_status ensure_sk_workspace(DeviceState *d)
     return LF_OK;
 }
 
+// One-pass cross-entropy round flags, allocated and zeroed on first use.
+lf_status ensure_onepass_flags(DeviceState *d)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (d->op_flags)
+        return LF_OK;
+    const size_t bytes = static_cast<size_t>(2 * d->pair_clusters) * sizeof(unsigned long long);
+    if (cudaMalloc(&d->op_flags, bytes) != cudaSuccess || cudaMemset(d->op_flags, 0, bytes) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        if (d->op_flags)
+            cudaFree(d->op_flags);
+        d->op_flags = nullptr;
+        return LF_ERR_WORKSPACE;
+    }
+    return LF_OK;
+}
+
+unsigned next_epoch(DeviceState *d)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    unsigned e = ++d->sk_epoch;
+    if (e == 0)
+        e = ++d->sk_epoch;
+    return e;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -221,12 +249,8 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
 
 cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
 {
-    if (g.p.streamk) {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        g.p.epoch = ++g.dev->sk_epoch;  // each launch's flags are distinct from every earlier one
-        if (g.p.epoch == 0)
-            g.p.epoch = ++g.dev->sk_epoch;
-    }
+    if (g.p.streamk)
+        g.p.epoch = next_epoch(g.dev);  // each launch's flags are distinct from every earlier one
     return g.pair ? lf::launch_gemm_nt_pair(epi, g.ta, g.tb, g.p, g.grid, stream)
                   : lf::launch_gemm_nt(epi, g.ta, g.tb, g.p, g.grid, stream);
 }
@@ -307,6 +331,24 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
     float *row_max = reinterpret_cast<float *>(wsb + 2 * part + vec);
     float *row_logsum = reinterpret_cast<float *>(wsb + 2 * part + 2 * vec);
     p.labels = labels;
+    // With a gradient on CTA pairs: one pass, when a whole 256-row block of
+    // tiles (two per pair) fits on the resident pairs -- no recompute GEMM and
+    // no combine kernel.
+    if (grad_or_null && g.pair && (p.num_n_blocks + 1) / 2 <= d->pair_clusters) {
+        if ((st = ensure_onepass_flags(d)) != LF_OK)
+            return st;
+        p.streamk = 0;
+        p.op_Q = (p.num_n_blocks + 1) / 2;
+        p.op_k = d->pair_clusters / p.op_Q;
+        if (p.op_k > p.num_m_blocks)
+            p.op_k = p.num_m_blocks;
+        p.op_rounds = (p.num_m_blocks + p.op_k - 1) / p.op_k;
+        p.round_flags = static_cast<unsigned long long *>(d->op_flags);
+        p.loss = loss;
+        p.out = grad_or_null;
+        p.epoch = next_epoch(d);
+        return launched(lf::launch_xent_onepass(g.ta, g.tb, p, 2 * p.op_k * p.op_Q, stream), 1);
+    }
     if ((st = launched(run_gemm(lf::EPI_XENT_PARTIAL, g, stream), 1)) != LF_OK)
         return st;
     if ((st = launched(lf::launch_xent_combine(p.part_max, p.part_sum, p.label_logit, labels, p.M, p.N,

@@ -1,0 +1,462 @@
+// gemm_xent_onepass.cu -- GEMM + row-wise cross-entropy + gradient in ONE
+// pass over the tensor cores: the logits are computed once, never written to
+// memory, and the gradient comes straight from the accumulators.
+//
+// Source: "Allow reductions in matmul epilogues" (NVIDIA/Fuser issue 2213):
+// the fusion example (row max, sum-exp, log-sum-exp, label logit, and the
+// softmax-minus-onehot output) and the follow-up: a row reduction across the
+// tiles of a row needs a grid reduction, and when the epilogue must reuse the
+// reduced value (here: the gradient needs the row's log-sum-exp) every CTA of
+// a row of tiles has to be resident at once so the result can be broadcast
+// back.  That is what this kernel does, one 256-row block of rows at a time.
+//
+// Schedule: CTA pairs (tcgen05 cta_group::2, M=256 x N=256 MMAs) form groups
+// of Q = ceil(N_tiles / 2) pairs; pair qi of a group owns N tiles 2qi and
+// 2qi+1 of the group's M block and keeps both 256-column accumulators in TMEM
+// (all 512 columns).  k = floor(pairs / Q) groups run side by side, so a round
+// covers k M blocks; round r of group g is M block r*k + g.  Per round:
+//   1. mainloop of the pair's one or two tiles (same TMA/MMA machinery as the
+//      pair GEMM kernel);
+//   2. epilogue, one warpgroup per tile (8 epilogue warps; a thread owns a
+//      row of its tile): per-(row, tile) statistics (max, sum exp(z - max),
+//      label logit); warpgroup 1 hands its row statistics to warpgroup 0
+//      through shared memory, which merges the pair's two tiles and stores one
+//      partial per row in slot [row, qi]; then the CTA releases a flag
+//      (epoch << 32 | round+1);
+//   3. the lanes poll the flags of the group's Q pairs in parallel (acquire,
+//      bounded), each thread merges its row's Q pair partials into (row max,
+//      log sum) with float4 loads, 32 partials per round trip -- the
+//      warpgroup holding tile 0 also writes loss[row] -- and writes
+//      grad = exp(z - lse) - onehot for its tile from TMEM; the accumulator is
+//      released for the next round.
+// Measured per round at 4096x32768x4096 (pair 0, one GB300): mainloop ~47 us,
+// then, serialised because the two accumulators fill TMEM: statistics of the
+// second tile + hand-off ~6 us, the group's slowest pair ~5 us, merge and
+// gradient ~11 us.
+// The producer streams the next round's first K slices into the ring while
+// the epilogue runs.  Waits only go to the same round of the same group, whose
+// pairs never wait on anything later, so there is no cycle; every wait is
+// bounded (2 s) and an abort is mirrored into the peer CTA.
+#include <atomic>
+
+#include "lf_gemm_common.cuh"
+
+namespace lf {
+namespace {
+
+constexpr int OP_M = 2 * BM;  // 256 rows per pair
+constexpr int OP_UMMA_K = 16;
+constexpr int OP_STAGES = 6;
+constexpr int OP_A_BYTES = BM * BK * 2;        // this CTA's 128 rows of X
+constexpr int OP_B_BYTES = (BN / 2) * BK * 2;  // this CTA's 128 rows of W
+constexpr int OP_STAGE_BYTES = OP_A_BYTES + OP_B_BYTES;
+constexpr int OP_TMEM_COLS = 2 * BN;  // tile A: columns [0, 256), tile B: [256, 512)
+constexpr int OP_THREADS = 320;     // producer, MMA, and one epilogue warpgroup per tile
+constexpr int OP_EPI_WARPS = 4;    // per warpgroup (= per tile)
+constexpr int OP_NUM_BARS = 2 * OP_STAGES + 2 + 2 + 3;  // ring, tfull[2], tempty[2], drain, publish, exchange
+constexpr int OP_XCH_BYTES = 2 * BM * 4;                  // tile-1 row statistics handed to warpgroup 0
+constexpr int OP_SMEM_BYTES = OP_STAGES * OP_STAGE_BYTES + 1024 + OP_NUM_BARS * 8 + 16 + OP_XCH_BYTES;
+constexpr uint32_t OP_IDESC = idesc_bf16_f32(OP_M, BN);
+constexpr uint64_t OP_ABORT_SETTLE_NS = 100000;
+constexpr int ERR_OP_FLAG = 0x108;  // a group member never published its partials
+
+struct OpWork {
+    int mb, nb0, ntile;
+};
+
+// Round r of `pair`: its M block and its N tiles nb0 (and nb0 + 1 if ntile == 2).
+__device__ __forceinline__ bool op_work(const GemmParams &p, int pair, int r, OpWork &w)
+{
+    const int grp = pair / p.op_Q;
+    const int qi = pair % p.op_Q;
+    w.mb = r * p.op_k + grp;
+    if (w.mb >= p.num_m_blocks)
+        return false;
+    w.nb0 = 2 * qi;  // < num_n_blocks because op_Q = ceil(num_n_blocks / 2)
+    w.ntile = (w.nb0 + 1 < p.num_n_blocks) ? 2 : 1;
+    return true;
+}
+
+// Merge n (max, sum) partials of one row, pm[j], ps[j] for j < n, into the
+// row's max `m` and sum `s` of exp(z - m): online rescaling, 32 partials per
+// batch (8 float4 loads of each array in flight when vec4), so a row costs
+// ceil(n / 32) dependent L2 round trips.
+__device__ __forceinline__ void merge_row_partials(const float *pm, const float *ps, int n, bool vec4, float &m,
+                                                   float &s)
+{
+    m = -CUDART_INF_F;
+    s = 0.f;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+        float a[32], b[32];
+        if (vec4) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = j0 + 4 * i;
+                float4 fa = make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
+                float4 fb = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < n) {
+                    fa = __ldcg(reinterpret_cast<const float4 *>(pm + j));
+                    fb = __ldcg(reinterpret_cast<const float4 *>(ps + j));
+                }
+                a[4 * i] = fa.x, a[4 * i + 1] = fa.y, a[4 * i + 2] = fa.z, a[4 * i + 3] = fa.w;
+                b[4 * i] = fb.x, b[4 * i + 1] = fb.y, b[4 * i + 2] = fb.z, b[4 * i + 3] = fb.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int j = j0 + i;
+                a[i] = j < n ? __ldcg(pm + j) : -CUDART_INF_F;
+                b[i] = j < n ? __ldcg(ps + j) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (j0 + i >= n) {  // the tail of a float4 past n
+                a[i] = -CUDART_INF_F;
+                b[i] = 0.f;
+            }
+        float cm = a[0];
+#pragma unroll
+        for (int i = 1; i < 32; ++i)
+            cm = fmaxf(cm, a[i]);
+        const float nm = fmaxf(m, cm);
+        s *= exp2f((m - nm) * LOG2E);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            s += b[i] * exp2f((a[i] - nm) * LOG2E);
+        m = nm;
+    }
+}
+
+// Bounded wait until *flag >= target (acquire).
+__device__ __noinline__ bool wait_flag64(const unsigned long long *flag, unsigned long long target,
+                                         volatile int *abort_flag, const GemmParams &p, uint32_t peer_abort)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_gpu_u64(flag) >= target)
+            return true;
+        if ((it & 15u) == 15u) {
+            if (*abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+                raise_error(p, abort_flag, ERR_OP_FLAG, peer_abort);
+                return false;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(OP_THREADS, 1)
+    k_xent_onepass(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + OP_STAGES * OP_A_BYTES;
+    const uint32_t bar0 = base + OP_STAGES * OP_STAGE_BYTES;
+    const uint32_t drain_bar = bar0 + 8u * (2 * OP_STAGES + 4);
+    const uint32_t pub_bar = drain_bar + 8u;  // warpgroup 0 wrote the pair's merged partials
+    const uint32_t xch_bar = pub_bar + 8u;    // warpgroup 1 handed over its tile's statistics
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *xch_mx = reinterpret_cast<float *>(gbase + OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8 + 16);
+    float *xch_se = xch_mx + BM;
+#define FULL_BAR(s) (bar0 + 8u * (s))
+#define EMPTY_BAR(s) (bar0 + 8u * (OP_STAGES + (s)))
+#define TFULL_BAR(t) (bar0 + 8u * (2 * OP_STAGES + (t)))
+#define TEMPTY_BAR(t) (bar0 + 8u * (2 * OP_STAGES + 2 + (t)))
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < OP_STAGES; ++s) {
+            mbar_init(FULL_BAR(s), 1);
+            mbar_init(EMPTY_BAR(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(TFULL_BAR(t), 1);
+            mbar_init(TEMPTY_BAR(t), 2 * OP_EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        mbar_init(pub_bar, OP_EPI_WARPS);
+        mbar_init(xch_bar, OP_EPI_WARPS);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), OP_TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed[OP_STAGES];
+#pragma unroll
+            for (int s = 0; s < OP_STAGES; ++s)
+                armed[s] = 0;
+            bool ok = true, first = true;
+            OpWork w;
+            for (int r = 0; ok && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
+                const int arow = w.mb * OP_M + static_cast<int>(rank) * BM;
+                for (int t = 0; ok && t < w.ntile; ++t) {
+                    const int brow = (w.nb0 + t) * BN + static_cast<int>(rank) * (BN / 2);
+                    for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                        if (!wait_bar(EMPTY_BAR(stage), phase ^ 1u, abort_flag, p, ERR_PRODUCER, peer_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t full_leader = mapa_shared(FULL_BAR(stage), 0u);
+                        const bool skip = first && p.inject == 1 && blockIdx.x == 0;  // test hook
+                        first = false;
+                        if (!skip) {
+                            if (leader) {
+                                mbar_arrive_expect_tx(FULL_BAR(stage), 2 * OP_STAGE_BYTES);
+                                ++armed[stage];
+                            }
+                            tma_load_2d_pair(sA + stage * OP_A_BYTES, &tmA, kb * BK, arow, full_leader);
+                            tma_load_2d_pair(sB + stage * OP_B_BYTES, &tmB, kb * BK, brow, full_leader);
+                        }
+                        if (++stage == OP_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            if (leader)
+                for (int s = 0; s < OP_STAGES; ++s)
+                    if (armed[s])
+                        wait_bar_drain(FULL_BAR(s), (armed[s] - 1u) & 1u, abort_flag, p, peer_abort);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t tph[2] = {0u, 0u};
+            bool ok = true;
+            OpWork w;
+            for (int r = 0; ok && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
+                for (int t = 0; ok && t < w.ntile; ++t) {
+                    if (!wait_bar(TEMPTY_BAR(t), tph[t] ^ 1u, abort_flag, p, ERR_MMA_ACC, peer_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(t * BN);
+                    for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                        if (!wait_bar(FULL_BAR(stage), phase, abort_flag, p, ERR_MMA_FULL, peer_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = sA + stage * OP_A_BYTES;
+                        const uint32_t b0 = sB + stage * OP_B_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / OP_UMMA_K; ++k)
+                            umma_f16_pair(d_tmem, smem_desc_k128(a0 + k * OP_UMMA_K * 2),
+                                          smem_desc_k128(b0 + k * OP_UMMA_K * 2), OP_IDESC, (kb | k) != 0 ? 1u : 0u);
+                        umma_commit_pair_mc(EMPTY_BAR(stage), 0x3);
+                        if (++stage == OP_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    umma_commit_pair_mc(TFULL_BAR(t), 0x3);
+                    tph[t] ^= 1u;
+                }
+            }
+            umma_commit_pair_mc(drain_bar, 0x1);
+            wait_bar_drain(drain_bar, 0u, abort_flag, p, peer_abort);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs)
+        // warpgroup t (warps 2..5: t = 0, warps 6..9: t = 1) owns tile t; warp
+        // w reads TMEM lanes 32 * (w % 4) .., one row per thread.
+        const int t = (warp - 2) >> 2;
+        const int q = warp & 3;
+        const int rloc = q * 32 + lane;
+        const PartialAdd none = {nullptr, 0, 0, 0};
+        uint32_t eph = 0;
+        uint32_t pub_phase = 0;
+        const unsigned long long epoch_hi = static_cast<unsigned long long>(p.epoch) << 32;
+        const uint32_t taddr = tmem_base + static_cast<uint32_t>(t * BN) + (static_cast<uint32_t>(q * 32) << 16);
+        uint32_t xch_phase = 0;
+        OpWork w;
+        for (int r = 0; r < p.op_rounds && op_work(p, pair, r, w); ++r) {
+            const int row = w.mb * OP_M + static_cast<int>(rank) * BM + rloc;
+            const bool row_ok = row < p.M;
+            const bool mine = t < w.ntile;  // the pair's last tile may be missing (odd tile count)
+            const int nb = w.nb0 + t;
+            const int qi = pair % p.op_Q;
+            // 1. statistics of this warpgroup's tile for its 128 rows
+            float mx = -CUDART_INF_F, se = 0.f;
+            if (mine) {
+                const bool got = wait_bar(TFULL_BAR(t), eph, abort_flag, p, ERR_EPI, peer_abort);
+                if (!__all_sync(0xffffffffu, got))
+                    break;
+                eph ^= 1u;
+                tc_fence_after();
+                const int lab = row_ok ? p.labels[row] : -1;
+                float zl = 0.f;
+                bool have;
+                xent_tile_stats(p, taddr, lab, nb, none, mx, se, zl, have);
+                if (row_ok && have && lab < p.N)
+                    p.label_logit[row] = zl;
+            }
+            // 2. warpgroup 1 hands its statistics to warpgroup 0, which merges
+            //    the pair's two tiles per row, stores the partial in slot
+            //    [row, qi] and publishes the CTA's flag for the group
+            if (t == 1) {
+                if (mine) {
+                    xch_mx[rloc] = mx;
+                    xch_se[rloc] = se;
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(xch_bar);
+                }
+            } else {
+                if (w.ntile == 2) {
+                    const bool got = wait_bar(xch_bar, xch_phase, abort_flag, p, ERR_SK_SLOT, peer_abort);
+                    if (!__all_sync(0xffffffffu, got))
+                        break;
+                    xch_phase ^= 1u;
+                    const float m1 = xch_mx[rloc], s1 = xch_se[rloc];
+                    const float nm = fmaxf(mx, m1);
+                    se = se * exp2f((mx - nm) * LOG2E) + s1 * exp2f((m1 - nm) * LOG2E);
+                    mx = nm;
+                }
+                if (row_ok) {
+                    p.part_max[static_cast<size_t>(row) * p.num_n_blocks + qi] = mx;
+                    p.part_sum[static_cast<size_t>(row) * p.num_n_blocks + qi] = se;
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(pub_bar);
+                if (warp == 2 && lane == 0 &&
+                    wait_bar(pub_bar, pub_phase, abort_flag, p, ERR_SK_SLOT, peer_abort)) {
+                    __threadfence();
+                    st_release_gpu_u64(p.round_flags + pair * 2 + rank, epoch_hi | static_cast<unsigned>(r + 1));
+                }
+                pub_phase ^= 1u;
+            }
+            // 3. wait for the group's pairs (same CTA rank holds the same rows);
+            //    the lanes poll the flags in parallel.  A warpgroup without a
+            //    tile waits too: the flags include its own pair's, so it cannot
+            //    arrive on the publish barrier for the next round early.
+            bool got = true;
+            {
+                const int first = (pair / p.op_Q) * p.op_Q;
+                const unsigned long long target = epoch_hi | static_cast<unsigned>(r + 1);
+                for (int j = lane; j < p.op_Q && got; j += 32)
+                    got = wait_flag64(p.round_flags + (first + j) * 2 + rank, target, abort_flag, p, peer_abort);
+            }
+            if (!__all_sync(0xffffffffu, got))
+                break;
+            __syncwarp();
+            if (!mine)
+                continue;
+            // 4. merge the row's op_Q pair partials
+            float m = -CUDART_INF_F, s = 0.f;
+            if (row_ok)
+                merge_row_partials(p.part_max + static_cast<size_t>(row) * p.num_n_blocks,
+                                   p.part_sum + static_cast<size_t>(row) * p.num_n_blocks, p.op_Q,
+                                   (p.num_n_blocks & 3) == 0, m, s);
+            const float ls = logf(s);
+            if (row_ok && nb == 0) {
+                const int lab = p.labels[row];
+                p.loss[row] = (lab >= 0 && lab < p.N) ? (m - __ldcg(p.label_logit + row)) + ls : CUDART_NAN_F;
+            }
+            // 5. gradient of this tile straight from TMEM, then free the accumulator
+            epi_xent_grad_rows(p, taddr, row, nb, none, m, ls);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(mapa_shared(TEMPTY_BAR(t), 0u));
+        }
+    }
+#undef FULL_BAR
+#undef EMPTY_BAR
+#undef TFULL_BAR
+#undef TEMPTY_BAR
+
+    if (*abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < OP_ABORT_SETTLE_NS) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, OP_TMEM_COLS);
+    }
+}
+
+cudaError_t set_onepass_smem_attr_once()
+{
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load() & bit)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(k_xent_onepass, cudaFuncAttributeMaxDynamicSharedMemorySize, OP_SMEM_BYTES);
+    if (e == cudaSuccess)
+        done.fetch_or(bit);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid,
+                                cudaStream_t s)
+{
+    cudaError_t e = set_onepass_smem_attr_once();
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(OP_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = OP_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_xent_onepass, ta, tb, p);
+}
+
+}  // namespace lf

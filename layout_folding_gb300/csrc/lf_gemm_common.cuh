@@ -199,20 +199,19 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, uint32_t taddr, i
     }
 }
 
-// Cross-entropy partials of one 256-column tile of row `row` ("Allow reductions
-// in matmul epilogues", fusion example: the row max, exp(z - max) and its sum,
-// and the label logit selected by comparing the column index with the label):
-//   part_max = max_n z,  part_sum = sum_n exp(z - part_max)  over the tile's
-//   columns n < N; label_logit = z[label] if the label falls in this tile.
+// Cross-entropy statistics of one 256-column tile of row `row` ("Allow
+// reductions in matmul epilogues", fusion example: the row max, exp(z - max)
+// and its sum, and the label logit selected by comparing the column index
+// with the label), over the tile's columns n < N:
+//   mx = max_n z,  se = sum_n exp(z - mx),  zl = z[label] if the label is here.
 // The running (max, sum) is rescaled chunk by chunk (32 columns at a time).
-__device__ __forceinline__ void epi_xent_partial(const GemmParams &p, uint32_t taddr, int row, int nb,
-                                                 const PartialAdd &pa)
+__device__ __forceinline__ void xent_tile_stats(const GemmParams &p, uint32_t taddr, int lab, int nb,
+                                                const PartialAdd &pa, float &mx_out, float &se_out, float &zl,
+                                                bool &have_label)
 {
-    const bool row_ok = row < p.M;
-    const int lab = row_ok ? p.labels[row] : -1;
     const int lab_local = lab - nb * BN;
-    float mx = -CUDART_INF_F, s = 0.f, zl = 0.f;
-    bool have_label = false;
+    float mx = -CUDART_INF_F, s = 0.f;
+    have_label = false;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
         const int col = nb * BN + c;
@@ -244,26 +243,38 @@ __device__ __forceinline__ void epi_xent_partial(const GemmParams &p, uint32_t t
         s += cs;
         mx = nm;
     }
+    mx_out = mx;
+    se_out = s;
+}
+
+// Partials of one tile to the workspace: part_max/part_sum[row, nb] and, if
+// the label falls in this tile, label_logit[row].
+__device__ __forceinline__ void epi_xent_partial(const GemmParams &p, uint32_t taddr, int row, int nb,
+                                                 const PartialAdd &pa)
+{
+    const bool row_ok = row < p.M;
+    const int lab = row_ok ? p.labels[row] : -1;
+    float mx, se, zl = 0.f;
+    bool have_label;
+    xent_tile_stats(p, taddr, lab, nb, pa, mx, se, zl, have_label);
     if (row_ok) {
         const size_t o = static_cast<size_t>(row) * p.num_n_blocks + nb;
         p.part_max[o] = mx;
-        p.part_sum[o] = s;
+        p.part_sum[o] = se;
         if (have_label && lab < p.N)
             p.label_logit[row] = zl;
     }
 }
 
-// Gradient of one tile, recomputed from the accumulator ("Allow reductions in
-// matmul epilogues", the yhatminusy output):
+// Gradient of one tile from the accumulator ("Allow reductions in matmul
+// epilogues", the yhatminusy output), given the row's max and log-sum:
 //   grad = bf16_rn(exp((z - row_max) - row_logsum) - [n == label])
-__device__ __forceinline__ void epi_xent_grad(const GemmParams &p, uint32_t taddr, int row, int nb,
-                                              const PartialAdd &pa)
+__device__ __forceinline__ void epi_xent_grad_rows(const GemmParams &p, uint32_t taddr, int row, int nb,
+                                                   const PartialAdd &pa, float rmax, float rls)
 {
     const bool row_ok = row < p.M;
     const int lab = row_ok ? p.labels[row] : -1;
     const int lab_local = lab - nb * BN;
-    const float rmax = row_ok ? p.row_max[row] : 0.f;
-    const float rls = row_ok ? p.row_logsum[row] : 0.f;
     __nv_bfloat16 *grow = static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(row) * p.N;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
@@ -284,6 +295,14 @@ __device__ __forceinline__ void epi_xent_grad(const GemmParams &p, uint32_t tadd
             store_row32_bf16(grow + col, g, p.N - col);
         }
     }
+}
+
+// Gradient pass of the two-pass form: the row statistics come from the combine kernel.
+__device__ __forceinline__ void epi_xent_grad(const GemmParams &p, uint32_t taddr, int row, int nb,
+                                              const PartialAdd &pa)
+{
+    const bool row_ok = row < p.M;
+    epi_xent_grad_rows(p, taddr, row, nb, pa, row_ok ? p.row_max[row] : 0.f, row_ok ? p.row_logsum[row] : 0.f);
 }
 
 }  // namespace

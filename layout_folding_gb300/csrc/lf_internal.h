@@ -41,6 +41,11 @@ struct GemmParams {
     unsigned epoch;             // value the flags of this launch carry
     float *sk_partials;         // [2 * pairs][128 * 256] fp32 partial accumulators
     unsigned *sk_flags;         // [2 * pairs] = epoch once the slot is written
+    // one-pass cross-entropy with gradient (pair kernel): groups of op_Q pairs
+    // each hold one 256-row M block (two 256-column tiles per pair) per round.
+    float *loss;                      // [M]
+    unsigned long long *round_flags;  // [2 * pairs]: (epoch << 32) | rounds published
+    int op_Q, op_k, op_rounds;        // pairs per M block, M blocks per round, rounds
 };
 
 // One stream-K partial slot: a CTA's 128 rows x 256 columns of fp32,
@@ -58,6 +63,11 @@ cudaError_t launch_gemm_nt_pair(int epi, const CUtensorMap &ta, const CUtensorMa
                                 int grid, cudaStream_t s);
 int gemm_pair_smem_bytes();
 int gemm_pair_max_active_clusters();
+
+// One-pass GEMM + cross-entropy + gradient on CTA pairs (no recompute GEMM,
+// no combine kernel).  Requires op_k * op_Q co-resident pairs; grid = 2 * op_k * op_Q.
+cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid,
+                                cudaStream_t s);
 
 cudaError_t launch_xent_combine(const float *part_max, const float *part_sum, const float *label_logit,
                                 const int32_t *labels, int M, int N, int num_n_blocks, float *loss,

@@ -181,7 +181,7 @@ def test_xent_tiny_full(variant):
     _xent_check(inp["x"], inp["w"], inp["labels"], what="tiny")
 
 
-@pytest.mark.parametrize("M,N,K", [(200, 1000, 136), (64, 8, 64), (129, 776, 520)])
+@pytest.mark.parametrize("M,N,K", [(200, 1000, 136), (64, 8, 64), (129, 776, 520), (600, 1032, 264), (1240, 18952, 136)])
 def test_xent_ragged_full(M, N, K, variant):
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
     lab = synthetic.labels_uniform(M, N)
@@ -220,6 +220,31 @@ def test_xent_launch_counts():
     lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
     b2 = lf.launch_count()
     assert (b1 - b0, b2 - b1) == (2, 3)
+
+
+def test_xent_onepass_gradient_is_one_launch():
+    # on CTA pairs the gradient comes from the same pass (no combine kernel,
+    # no recompute GEMM); without a gradient it stays partials + combine
+    M, N, K = 512, 2048, 256
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N)
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    lf.set_tuning(-1, 2)
+    try:
+        lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        b0 = lf.launch_count()
+        loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        b1 = lf.launch_count()
+        lf.gemm_nt_xent(xd, wd, ld, want_grad=False)
+        b2 = lf.launch_count()
+        lf.check_device_error()
+    finally:
+        lf.set_tuning(-1, -1)
+    assert (b1 - b0, b2 - b1) == (1, 2)
+    rows = sample_rows(M, k=16, seed=9)
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    assert_loss_close(f64(loss)[rows], rloss, "one-pass")
+    assert_grad_close(f64(grad)[rows], rgrad, "one-pass")
 
 
 def test_xent_grad_full_size(variant):

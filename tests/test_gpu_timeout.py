@@ -44,3 +44,31 @@ def test_stalled_wait_times_out_and_context_survives(variant):
     ref = oracle.gemm_nt(x, w)
     got = out.float().cpu().double().numpy()
     assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
+
+
+def test_stalled_wait_in_onepass_cross_entropy_times_out():
+    # the one-pass gradient kernel: a stalled pair also stalls its group's
+    # flag waits; every wait is bounded, the error is reported, the context lives
+    torch.cuda.set_device(0)
+    M, N, K = 512, 2048, 256
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N)
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    lf.check_device_error()
+    lf.set_tuning(-1, 2)
+    lf.set_test_hooks(True, 200_000_000)
+    try:
+        lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        with pytest.raises(lf.LayoutFoldError) as info:
+            lf.check_device_error()
+        assert info.value.status == 6
+    finally:
+        lf.set_test_hooks(False, 0)
+    try:
+        loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        lf.check_device_error()
+    finally:
+        lf.set_tuning(-1, -1)
+    _, rloss, _, _ = oracle.xent(x, w, lab.numpy(), want_grad=False)
+    got = loss.double().cpu().numpy()
+    assert np.max(np.abs(got - rloss) / np.abs(rloss)) <= 1e-3
