@@ -62,6 +62,7 @@ constexpr int ERR_OP_FLAG = 0x108;  // a group member never published its partia
 
 struct OpWork {
     int mb, nb0, ntile;
+    bool swap;  // process the pair's second tile first this round
 };
 
 // Round r of `pair`: its M block and its N tiles nb0 (and nb0 + 1 if ntile == 2).
@@ -74,6 +75,9 @@ __device__ __forceinline__ bool op_work(const GemmParams &p, int pair, int r, Op
         return false;
     w.nb0 = 2 * qi;  // < num_n_blocks because op_Q = ceil(num_n_blocks / 2)
     w.ntile = (w.nb0 + 1 < p.num_n_blocks) ? 2 : 1;
+    // Alternate the order of the two tiles every round: the W rows of the tile
+    // processed last are what L2 still holds, so the next round starts there.
+    w.swap = (r & 1) && w.ntile == 2;
     return true;
 }
 
@@ -219,7 +223,8 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             OpWork w;
             for (int r = 0; ok && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
                 const int arow = w.mb * OP_M + static_cast<int>(rank) * BM;
-                for (int t = 0; ok && t < w.ntile; ++t) {
+                for (int i = 0; ok && i < w.ntile; ++i) {
+                    const int t = w.swap ? w.ntile - 1 - i : i;
                     const int brow = (w.nb0 + t) * BN + static_cast<int>(rank) * (BN / 2);
                     for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                         if (!wait_bar(EMPTY_BAR(stage), phase ^ 1u, abort_flag, p, ERR_PRODUCER, peer_abort)) {
@@ -259,7 +264,8 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             bool ok = true;
             OpWork w;
             for (int r = 0; ok && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
-                for (int t = 0; ok && t < w.ntile; ++t) {
+                for (int i = 0; ok && i < w.ntile; ++i) {
+                    const int t = w.swap ? w.ntile - 1 - i : i;
                     if (!wait_bar(TEMPTY_BAR(t), tph[t] ^ 1u, abort_flag, p, ERR_MMA_ACC, peer_abort)) {
                         ok = false;
                         break;
@@ -314,18 +320,22 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             const bool mine = t < w.ntile;  // the pair's last tile may be missing (odd tile count)
             const int nb = w.nb0 + t;
             const int qi = pair % p.op_Q;
-            // 1. statistics of this warpgroup's tile for its 128 rows
+            // 1. statistics of this warpgroup's tile for its 128 rows; the tile
+            //    is left in TMEM as e = exp(z - tile max) for the gradient
+            const int lab = row_ok ? p.labels[row] : -1;
             float mx = -CUDART_INF_F, se = 0.f;
+            float tmax = 0.f;
             if (mine) {
                 const bool got = wait_bar(TFULL_BAR(t), eph, abort_flag, p, ERR_EPI, peer_abort);
                 if (!__all_sync(0xffffffffu, got))
                     break;
                 eph ^= 1u;
                 tc_fence_after();
-                const int lab = row_ok ? p.labels[row] : -1;
                 float zl = 0.f;
                 bool have;
-                xent_tile_stats(p, taddr, lab, nb, none, mx, se, zl, have);
+                tmax = xent_tile_max(p, taddr, lab, nb, zl, have);
+                se = xent_tile_exp_store(p, taddr, nb, tmax);
+                mx = tmax;
                 if (row_ok && have && lab < p.N)
                     p.label_logit[row] = zl;
             }
@@ -394,7 +404,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                 p.loss[row] = (lab >= 0 && lab < p.N) ? (m - __ldcg(p.label_logit + row)) + ls : CUDART_NAN_F;
             }
             // 5. gradient of this tile straight from TMEM, then free the accumulator
-            epi_xent_grad_rows(p, taddr, row, nb, none, m, ls);
+            xent_grad_from_exp(p, taddr, row, nb, lab, exp2f(((tmax - m) - ls) * LOG2E));
             tc_fence_before();
             __syncwarp();
             if (lane == 0)

@@ -247,6 +247,98 @@ __device__ __forceinline__ void xent_tile_stats(const GemmParams &p, uint32_t ta
     se_out = s;
 }
 
+// Two-pass form for the one-pass gradient kernel, which keeps the tile in
+// TMEM until the row's log-sum-exp is known: pass 1 finds the tile max (and
+// the label logit), pass 2 replaces each accumulator value by
+// e = exp(z - tile_max) (0 past column N) and returns sum e, so the gradient
+// pass needs no second exponential: grad = e * exp(tile_max - lse) - onehot.
+__device__ __forceinline__ float xent_tile_max(const GemmParams &p, uint32_t taddr, int lab, int nb, float &zl,
+                                               bool &have_label)
+{
+    const int lab_local = lab - nb * BN;
+    float mx = -CUDART_INF_F;
+    have_label = false;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c, v);
+        tmem_wait_ld();
+        const int nvalid = p.N - col;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nvalid)
+                mx = fmaxf(mx, __uint_as_float(v[i]));
+        const int li = lab_local - c;
+        if (static_cast<unsigned>(li) < 32u) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i == li)
+                    zl = __uint_as_float(v[i]);
+            have_label = true;
+        }
+    }
+    return mx;
+}
+
+__device__ __forceinline__ float xent_tile_exp_store(const GemmParams &p, uint32_t taddr, int nb, float tmax)
+{
+    float s = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c, v);
+        tmem_wait_ld();
+        const int nvalid = p.N - col;
+        float cs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float e = i < nvalid ? exp2f((__uint_as_float(v[i]) - tmax) * LOG2E) : 0.f;
+            cs += e;
+            v[i] = __float_as_uint(e);
+        }
+        s += cs;
+        tmem_st_32x32b_x32(taddr + c, v);
+    }
+    tmem_wait_st();
+    return s;
+}
+
+// grad = bf16_rn(e * scale - [n == label]) with e = exp(z - tile_max) from
+// TMEM and scale = exp(tile_max - lse).
+__device__ __forceinline__ void xent_grad_from_exp(const GemmParams &p, uint32_t taddr, int row, int nb, int lab,
+                                                   float scale)
+{
+    const bool row_ok = row < p.M;
+    const int lab_local = lab - nb * BN;
+    __nv_bfloat16 *grow = static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(row) * p.N;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c, v);
+        tmem_wait_ld();
+        if (row_ok) {
+            const int li = lab_local - c;
+            float g[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                g[i] = __uint_as_float(v[i]) * scale;
+                if (i == li)
+                    g[i] -= 1.f;
+            }
+            store_row32_bf16(grow + col, g, p.N - col);
+        }
+    }
+}
+
 // Partials of one tile to the workspace: part_max/part_sum[row, nb] and, if
 // the label falls in this tile, label_logit[row].
 __device__ __forceinline__ void epi_xent_partial(const GemmParams &p, uint32_t taddr, int row, int nb,
