@@ -42,7 +42,7 @@ constexpr int PAIR_ACC_BUFS = 2;
 constexpr int PAIR_TMEM_COLS = PAIR_ACC_BUFS * BN;  // 512
 constexpr int PAIR_THREADS = 192;
 constexpr int PAIR_EPI_WARPS = 4;
-constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2;
+constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 3;
 constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + PAIR_NUM_BARS * 8 + 16;
 constexpr uint32_t PAIR_IDESC = idesc_bf16_f32(PAIR_M, BN);
 constexpr uint64_t ABORT_SETTLE_NS = 100000;  // after an abort: let copies in flight land
@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const uint32_t bar0 = base + PAIR_STAGES * PAIR_STAGE_BYTES;
     const uint32_t drain_bar = bar0 + 8u * (2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS);
     const uint32_t skw_bar = drain_bar + 8u;  // the 4 epilogue warps finished writing a partial
+    const uint32_t skc_bar = skw_bar + 8u;    // a contributor's partial landed in shared memory
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 #define FULL_BAR(s) (bar0 + 8u * (s))
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         }
         mbar_init(drain_bar, 1);
         mbar_init(skw_bar, PAIR_EPI_WARPS);
+        mbar_init(skc_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -314,6 +316,20 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                     pa.slot = p.sk_partials + static_cast<size_t>(first * 2 + rank) * SK_SLOT_FLOATS;
                     pa.stride = static_cast<size_t>(MB) * 2 * SK_SLOT_FLOATS;
                     pa.count = n;
+                    if (n > 0) {
+                        // This is the pair's last segment, so its MMAs are done and
+                        // the operand ring is idle: pull the first contributor's
+                        // 128 KiB slot into it with one bulk copy instead of eight
+                        // dependent L2 round trips during the epilogue.
+                        if (warp == 2 && lane == 0) {
+                            mbar_arrive_expect_tx(skc_bar, SK_SLOT_FLOATS * 4);
+                            bulk_load_g2s(sA, pa.slot, SK_SLOT_FLOATS * 4, skc_bar);
+                        }
+                        const bool landed = wait_bar(skc_bar, 0u, abort_flag, p, ERR_SK_COPY, peer_abort);
+                        if (!__all_sync(0xffffffffu, landed))
+                            break;
+                        pa.smem0 = reinterpret_cast<const float4 *>(gbase);
+                    }
                 }
                 if (EPI == EPI_STORE)
                     epi_store(p, taddr, row, nb, pa);

@@ -27,6 +27,7 @@ constexpr int ERR_EPI = 0x104;        // accumulator never completed
 constexpr int ERR_DRAIN = 0x105;      // copies / MMAs did not finish while unwinding
 constexpr int ERR_SK_FLAG = 0x106;    // a stream-K partial never arrived
 constexpr int ERR_SK_SLOT = 0x107;    // a CTA's own partial write did not complete
+constexpr int ERR_SK_COPY = 0x109;    // the copy of a partial into shared memory did not land
 
 // Record `code` (first writer wins), raise this CTA's abort flag and, in a
 // CTA pair, the peer's (peer_abort: its shared::cluster address, 0 if none).
@@ -114,7 +115,8 @@ struct PartialAdd {
     const float *slot;
     size_t stride;
     int count;
-    int row;  // this thread's row within its CTA's 128 rows
+    int row;                // this thread's row within its CTA's 128 rows
+    const float4 *smem0;    // if set: contributor 0's slot, already copied to shared memory
 };
 
 // Read 32 accumulator columns [c, c+32) of this thread's row from TMEM and
@@ -124,6 +126,17 @@ __device__ __forceinline__ void load_chunk(uint32_t taddr, int c, const PartialA
     tmem_ld_32x32b_x32(taddr + c, v);
     tmem_wait_ld();
     for (int e = 0; e < pa.count; ++e) {
+        if (e == 0 && pa.smem0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 f = pa.smem0[(c / 4 + i) * BM + pa.row];
+                v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) + f.x);
+                v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + f.y);
+                v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + f.z);
+                v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + f.w);
+            }
+            continue;
+        }
         const float4 *s4 = reinterpret_cast<const float4 *>(pa.slot + static_cast<size_t>(e) * pa.stride);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
