@@ -62,6 +62,7 @@ def _load():
             "oracle_matmul_k1": [P, P, I64, I64, P],
             "oracle_matmul_k1_bf16": [P, P, I64, I64, P],
             "oracle_set_num_threads": [ctypes.c_int],
+            "oracle_fp8_cast_dual": [P, I64, I64, ctypes.c_float, P, P],
         }
         for name, argtypes in sig.items():
             fn = getattr(lib, name)
@@ -69,6 +70,8 @@ def _load():
             fn.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
         lib.oracle_bf16_round.argtypes = [ctypes.c_float]
         lib.oracle_bf16_round.restype = ctypes.c_uint16
         _lib = lib
@@ -226,3 +229,23 @@ def matmul_k1_bf16(x, w) -> np.ndarray:
     out = np.empty((M, N), dtype=np.uint16)
     _load().oracle_matmul_k1_bf16(_p(x), _p(w), M, N, _p(out))
     return out
+
+
+def f32_to_e4m3(values) -> np.ndarray:
+    """fp32 -> float8 E4M3 codes (round to nearest even), element by element."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32).ravel()
+    out = np.empty(v.shape, dtype=np.uint8)
+    for i, f in enumerate(v):
+        out[i] = lib.oracle_f32_to_e4m3(float(f))
+    return out.reshape(np.shape(values))
+
+
+def fp8_cast_dual(x, scale: float):
+    """(out [M,K], out_t [K,M]) E4M3 codes of clamp(x * scale, -448, 448)."""
+    x = _bits(x)
+    M, K = x.shape
+    out = np.empty((M, K), dtype=np.uint8)
+    out_t = np.empty((K, M), dtype=np.uint8)
+    _load().oracle_fp8_cast_dual(_p(x), M, K, float(scale), _p(out), _p(out_t))
+    return out, out_t

@@ -243,3 +243,67 @@ void oracle_matmul_k1_bf16(const uint16_t *x, const uint16_t *w, int64_t M, int6
             out[i * N + j] = f32_to_bf16_rne((float)p);
         }
 }
+
+/*
+ * fp32 -> float8 E4M3 ("fn" variant: 1 sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities, S.1111.111 is NaN, largest finite 448),
+ * round to nearest, ties to even, by the definition: find the representable
+ * neighbours of |f| and pick the nearer one (the even mantissa on a tie).
+ * Inputs are clamped to +-448 by the caller; NaN maps to 0x7F.
+ */
+uint8_t oracle_f32_to_e4m3(float f)
+{
+    if (f != f)
+        return 0x7F;
+    uint8_t sign = (f < 0.0f || (f == 0.0f && 1.0f / f < 0.0f)) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a == 0.0)
+        return sign;
+    /* value of code c (c in 0..126, positive): subnormal for exponent field 0 */
+    double best = 0.0;
+    int best_code = 0;
+    for (int c = 0; c <= 126; ++c) {
+        int e = c >> 3, m = c & 7;
+        double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+        if (v <= a) {
+            best = v;
+            best_code = c;
+        }
+    }
+    if (best_code == 126) /* at or above 448 */
+        return (uint8_t)(sign | 126);
+    {
+        int c_hi = best_code + 1;
+        int e = c_hi >> 3, m = c_hi & 7;
+        double hi = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+        double dlo = a - best, dhi = hi - a;
+        int code = best_code;
+        if (dhi < dlo || (dhi == dlo && (c_hi & 1) == 0))
+            code = c_hi;
+        return (uint8_t)(sign | code);
+    }
+}
+
+/*
+ * The float8 training cast of "Improve the Inductor generated kernel for the
+ * pattern of output1 = pointwise(intput); output2 = transpose(output1)"
+ * (pytorch issue 130015), Examples: x = input * scale (bf16 times an fp32
+ * scale: one fp32 multiply), clamped to [-448, 448], converted to E4M3; the
+ * page returns the result both as is ([M,K] row-major) and as
+ * t().contiguous().t() -- the same values stored column-major, i.e. the
+ * [K,M] row-major array out_t[k*M + m] = out[m*K + k].
+ */
+void oracle_fp8_cast_dual(const uint16_t *x, int64_t M, int64_t K, float scale, uint8_t *out, uint8_t *out_t)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            float v = (float)(bf16_to_f64(x[m * K + k]) * (double)scale); /* exact product, one rounding */
+            if (v > 448.0f)
+                v = 448.0f;
+            if (v < -448.0f)
+                v = -448.0f;
+            uint8_t q = oracle_f32_to_e4m3(v);
+            out[m * K + k] = q;
+            out_t[k * M + m] = q;
+        }
+}

@@ -332,3 +332,47 @@ def test_page_shapes_fixture_matches_workloads():
     pk = pages["k1_rope"]
     assert [k1.M, k1.K] == pk["a"][1:] and [k1.K, k1.N] == pk["b"][1:]
     assert [k1.M, k1.N] == pk["out"][1:] and [k1.N, k1.M] == pk["out_permuted"][1:]
+
+
+# ------------------------------------------------ fp8 cast + dual layout pins
+# "Improve the Inductor generated kernel for the pattern of output1 =
+# pointwise(intput); output2 = transpose(output1)" (pytorch issue 130015).
+
+def test_e4m3_hand_derived_codes():
+    with open(os.path.join(GOLDEN, "e4m3_codes.json")) as f:
+        cases = json.load(f)["cases"]
+    vals = np.array([v for v, _ in cases], dtype=np.float32)
+    want = np.array([c for _, c in cases], dtype=np.uint8)
+    assert np.array_equal(oracle.f32_to_e4m3(vals), want)
+
+
+def test_e4m3_matches_library_conversion():
+    rng = np.random.default_rng(11)
+    vals = np.concatenate([
+        rng.uniform(-448, 448, 3000), rng.normal(0, 1, 3000), rng.normal(0, 0.01, 2000),
+        np.ldexp(rng.integers(0, 8, 500), -9) + np.ldexp(1, -10),     # subnormal midpoints
+        np.arange(-448, 449, 0.5)]).astype(np.float32)
+    got = oracle.f32_to_e4m3(vals)
+    want = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want)
+
+
+def test_fp8_cast_dual_layout_and_clamp():
+    x = synthetic.bf16_normal((37, 53), 30.0, 3)          # |x * 10| often > 448: exercises the clamp
+    out, out_t = oracle.fp8_cast_dual(x, 10.0)
+    assert out.shape == (37, 53) and out_t.shape == (53, 37)
+    assert np.array_equal(out_t, out.T)                    # the column-major copy holds the same codes
+    ref = (x.float() * torch.tensor(10.0)).clamp(-448, 448).to(torch.float8_e4m3fn)
+    assert np.array_equal(out, ref.view(torch.uint8).numpy())
+    assert np.sum(out == 126) + np.sum(out == 254) > 0     # some values clamped to +-448
+
+
+def test_fp8_cast_dual_mutants_fail():
+    x = synthetic.bf16_normal((16, 24), 30.0, 4)
+    out, out_t = oracle.fp8_cast_dual(x, 10.0)
+    ref = (x.float() * 10.0).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    no_clamp = (x.float() * 10.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()   # forgotten clamp
+    truncating = np.sign(x.float().numpy()) * np.floor(np.abs(x.float().numpy() * 10.0))  # wrong rounding
+    assert not np.array_equal(no_clamp, ref)
+    assert not np.array_equal(oracle.f32_to_e4m3(np.clip(truncating, -448, 448)), ref)
+    assert not np.array_equal(out_t, out)                  # the second layout really is transposed
