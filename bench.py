@@ -350,6 +350,23 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
                       "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes}
         del ad, bd, out
     torch.cuda.empty_cache()
+    # fused fp8 cast, both layouts: the page's 4096 x 4096 and a scaled case larger than L2
+    scale = torch.tensor([10.0], dtype=torch.float32, device="cuda")
+    for label, (M, K) in (("fp8_cast_page", (4096, 4096)), ("fp8_cast_scaled", (16384, 16384))):
+        x = synthetic.bf16_normal((M, K), 1.0, 15).to("cuda")
+        out = torch.empty(M, K, dtype=torch.float8_e4m3fn, device="cuda")
+        out_t = torch.empty(K, M, dtype=torch.float8_e4m3fn, device="cuda").t()
+
+        def step():
+            lf.fp8_cast_dual(x, scale, out=out, out_t=out_t, stream=stream)
+        times = timer.run(step, max(steps, 10), 3)
+        ms = statistics.median(times)
+        nbytes = M * K * (2 + 1 + 1)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[label] = {"M": M, "K": K, "scale": 10.0, "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes}
+        del x, out, out_t
+    torch.cuda.empty_cache()
     return res
 
 

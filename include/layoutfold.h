@@ -115,6 +115,36 @@ lf_status matmul_k1(const float *a, const float *b, float *out,
                     int64_t M, int64_t N, cudaStream_t stream);
 
 /*
+ * fp8_cast_dual -- the float8 training cast, written in both layouts by one
+ * kernel.
+ *
+ * Source: "Improve the Inductor generated kernel for the pattern of output1 =
+ * pointwise(intput); output2 = transpose(output1)" (pytorch issue 130015),
+ * Examples and "The issue in test_pattern1": the input times a scale,
+ * clamped to the largest finite float8_e4m3fn magnitude (448), converted to
+ * float8_e4m3fn, and returned both as is and as t().contiguous().t(), which
+ * the page's compiler produced with a second kernel that re-reads the fp8
+ * tensor.  Here the input is read once and both outputs are written from it.
+ *
+ *   x     : bf16 [M,K], device, row-major, 2-byte aligned.
+ *   scale : fp32, ONE element, device (the page keeps it in a device tensor).
+ *   out   : float8_e4m3fn [M,K], device, row-major:
+ *             out[m*K + k] = e4m3(clamp(x[m,k] * scale, -448, 448))
+ *           one fp32 multiply of the exact bf16 value, round-to-nearest-even
+ *           to E4M3 (bit-exact).  A NaN input stays NaN (code 0x7F or 0xFF).
+ *   out_t : float8_e4m3fn, the same values column-major, i.e. the [K,M]
+ *           row-major array out_t[k*M + m] = out[m*K + k] (the storage of
+ *           the page's tensor_fp8_t, whose strides are (1, M)).
+ *   1 <= M, K < 2^31.  Any alignment is accepted; M % 16 == 0, K % 16 == 0
+ *   and 16-byte aligned x, out and out_t take the vectorised kernel.
+ * The caller owns all four buffers; nothing is allocated.  out and out_t
+ * must not overlap each other or x.  Host-side checks return LF_ERR_NULL /
+ * LF_ERR_SHAPE / LF_ERR_ALIGN (x odd) before anything is enqueued.
+ */
+lf_status fp8_cast_dual(const void *x, const float *scale, void *out, void *out_t,
+                        int64_t M, int64_t K, cudaStream_t stream);
+
+/*
  * gemm_nt_xent_noalloc -- the same computation and outputs as gemm_nt_xent,
  * for callers that cannot allocate device memory during the call.  The pages
  * have no counterpart to this entry point: it is an interface addition.

@@ -9,6 +9,7 @@ Entry points (same names as the C ABI):
   gemm_nt(x, w, out=None)                       -> out = x @ w.T   (bf16)
   gemm_nt_xent(x, w, labels, want_grad=False)   -> (loss fp32 [M], grad bf16 [M,N] | None)
   matmul_k1(a, b, out=None)                     -> out = a * b     (fp32, K=1)
+  fp8_cast_dual(x, scale)                       -> (out e4m3 [M,K], out_t e4m3 [M,K] column-major)
 """
 from __future__ import annotations
 
@@ -53,6 +54,8 @@ def lib():
         L.gemm_nt_xent.restype = I32
         L.matmul_k1.argtypes = [P, P, P, I64, I64, P]
         L.matmul_k1.restype = I32
+        L.fp8_cast_dual.argtypes = [P, P, P, P, I64, I64, P]
+        L.fp8_cast_dual.restype = I32
         L.lf_status_string.argtypes = [I32]
         L.lf_status_string.restype = ctypes.c_char_p
         L.lf_check_device_error.argtypes = [P]
@@ -158,6 +161,36 @@ def matmul_k1(a, b, out=None, stream=None):
         raise ValueError("out must be [M, N]")
     _check(lib().matmul_k1(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, _stream(stream)), "matmul_k1")
     return out
+
+
+def fp8_cast_dual(x, scale, out=None, out_t=None, stream=None):
+    """The float8 training cast in both layouts: x bf16 [M, K] (contiguous),
+    scale fp32 one-element device tensor.  Returns (out, out_t), both
+    float8_e4m3fn [M, K] holding clamp(x * scale, -448, 448) rounded to E4M3;
+    out is row-major, out_t column-major (strides (1, M)).  Raw [M, K] / [K, M]
+    uint8 buffers may be passed as out / out_t."""
+    import torch
+    _require(x, torch.bfloat16, "x")
+    _require(scale, torch.float32, "scale")
+    if x.dim() != 2 or scale.numel() != 1:
+        raise ValueError("x must be 2-D and scale must hold one element")
+    M, K = x.shape
+    fp8 = torch.float8_e4m3fn
+    if out is None:
+        out = torch.empty(M, K, dtype=fp8, device=x.device)
+    if out_t is None:
+        out_t = torch.empty(K, M, dtype=fp8, device=x.device).t()
+    for t, name in ((out, "out"), (out_t, "out_t")):
+        if t.dtype not in (fp8, torch.uint8) or t.device != x.device or t.numel() != M * K:
+            raise ValueError("%s must be a 1-byte tensor of M*K elements on x's device" % name)
+    if tuple(out.shape) != (M, K) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, K] tensor")
+    col_major = tuple(out_t.shape) == (M, K) and (M == 1 or out_t.stride() == (1, M))
+    if not col_major and not (tuple(out_t.shape) == (K, M) and out_t.is_contiguous()):
+        raise ValueError("out_t must be [M, K] column-major or a contiguous [K, M] tensor")
+    _check(lib().fp8_cast_dual(x.data_ptr(), scale.data_ptr(), out.data_ptr(), out_t.data_ptr(), M, K,
+                               _stream(stream)), "fp8_cast_dual")
+    return out, out_t
 
 
 def check_device_error(stream=None):

@@ -380,6 +380,22 @@ lf_status matmul_k1(const float *a, const float *b, float *out, int64_t M, int64
     return launched(lf::launch_matmul_k1_f32(a, b, out, M, N, d->num_sms, stream), 1);
 }
 
+lf_status fp8_cast_dual(const void *x, const float *scale, void *out, void *out_t, int64_t M, int64_t K,
+                        cudaStream_t stream)
+{
+    if (!x || !scale || !out || !out_t)
+        return LF_ERR_NULL;
+    if (M <= 0 || K <= 0 || M > MAX_DIM || K > MAX_DIM)
+        return LF_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(x) & 1u) != 0)
+        return LF_ERR_ALIGN;
+    DeviceState *d = nullptr;
+    lf_status st = current_device(&d);
+    if (st != LF_OK)
+        return st;
+    return launched(lf::launch_fp8_cast_dual(x, scale, out, out_t, M, K, d->num_sms, stream), 1);
+}
+
 const char *lf_status_string(lf_status s)
 {
     switch (s) {

@@ -1,0 +1,136 @@
+// fp8_cast.cu -- the float8 training cast with both layouts in one pass.
+//
+// Source: "Improve the Inductor generated kernel for the pattern of output1 =
+// pointwise(intput); output2 = transpose(output1)" (pytorch issue 130015):
+// x = input * scale, clamped to +-E4M3_MAX (448), converted to
+// float8_e4m3fn, returned both as is and as t().contiguous().t() -- the same
+// values stored column-major.  The page reports that the compiler emits two
+// kernels (the cast, then a transposing copy that re-reads the fp8 tensor) and
+// that the authors used a hand-written fused kernel instead.  This is that
+// fusion: the bf16 input is read once, and both outputs are written from the
+// same registers -- the row-major tile directly, the column-major tile after a
+// transpose through shared memory, so every global access is a coalesced
+// 16-byte access.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "lf_internal.h"
+
+namespace lf {
+namespace {
+
+constexpr int T = 64;  // tile: 64 rows (m) x 64 columns (k)
+constexpr int THREADS = 256;
+
+// One fp32 multiply (exact bf16 times the fp32 scale, rounded once), then the
+// clamp to the largest finite E4M3 magnitude.  Written with comparisons so a
+// NaN passes through unchanged, as a tensor clamp leaves it.
+__device__ __forceinline__ float scaled_clamped(float v, float scale)
+{
+    v = v * scale;
+    v = v > 448.f ? 448.f : v;
+    return v < -448.f ? -448.f : v;
+}
+
+// Two floats -> two E4M3 codes (x in the low byte), round to nearest even.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b)
+{
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Vector path: M % 16 == 0, K % 16 == 0, 16-byte aligned pointers.
+__global__ void __launch_bounds__(THREADS) k_fp8_cast_dual_v16(const __nv_bfloat16 *__restrict__ x,
+                                                                const float *__restrict__ scale_ptr,
+                                                                uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
+                                                                int64_t M, int64_t K)
+{
+    // tile[k - k0][m - m0]; the 16-byte chunk holding m is chunk (m / 16) ^ ((k / 16) % 4) of row k, so
+    // the byte stores below (four rows k 16 apart per warp instruction) and the 16-byte reads after
+    // them hit distinct banks.
+    __shared__ __align__(16) uint8_t tile[T][T];
+    const float scale = __ldg(scale_ptr);
+    const int64_t tiles_m = (M + T - 1) / T, tiles_k = (K + T - 1) / T;
+    const int r = threadIdx.x >> 2;         // row of the tile this thread loads (0..63)
+    const int c = (threadIdx.x & 3) * 16;   // first of its 16 columns
+    for (int64_t t = blockIdx.x; t < tiles_m * tiles_k; t += gridDim.x) {
+        const int64_t m0 = (t / tiles_k) * T, k0 = (t % tiles_k) * T;
+        const int64_t m = m0 + r, k = k0 + c;
+        const bool in = m < M && k < K;     // K % 16 == 0: a 16-column group is all in or all out
+        uint32_t q[4] = {0u, 0u, 0u, 0u};
+        if (in) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + m * K + k);
+            const uint4 lo = __ldg(src), hi = __ldg(src + 1);
+            const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            float f[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                f[2 * i] = scaled_clamped(__uint_as_float(w[i] << 16), scale);
+                f[2 * i + 1] = scaled_clamped(__uint_as_float(w[i] & 0xffff0000u), scale);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                q[i] = e4m3x2(f[4 * i], f[4 * i + 1]) | (e4m3x2(f[4 * i + 2], f[4 * i + 3]) << 16);
+            *reinterpret_cast<uint4 *>(out + m * K + k) = make_uint4(q[0], q[1], q[2], q[3]);
+        }
+        // transpose through shared memory
+        const int swz_r = (((r >> 4) ^ (c >> 4)) << 4) | (r & 15);  // rows c..c+15 share c / 16
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            tile[c + i][swz_r] = static_cast<uint8_t>(q[i >> 2] >> (8 * (i & 3)));
+        __syncthreads();
+        {
+            const int kr = threadIdx.x >> 2;        // column of the input = row of out_t
+            const int mc = (threadIdx.x & 3) * 16;  // first of 16 rows of the input
+            const int64_t kk = k0 + kr, mm = m0 + mc;
+            if (kk < K && mm < M)
+                *reinterpret_cast<uint4 *>(out_t + kk * M + mm) =
+                    *reinterpret_cast<const uint4 *>(&tile[kr][mc ^ (((kr >> 4) & 3) << 4)]);
+        }
+        __syncthreads();
+    }
+}
+
+// Any shape / alignment: one element per thread step.
+__global__ void __launch_bounds__(THREADS) k_fp8_cast_dual_scalar(const __nv_bfloat16 *__restrict__ x,
+                                                                  const float *__restrict__ scale_ptr,
+                                                                  uint8_t *__restrict__ out,
+                                                                  uint8_t *__restrict__ out_t, int64_t M, int64_t K)
+{
+    const float scale = __ldg(scale_ptr);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * K;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / K, k = i % K;
+        const float v = scaled_clamped(__bfloat162float(x[i]), scale);
+        const uint8_t qv = static_cast<uint8_t>(e4m3x2(v, 0.f) & 0xffu);
+        out[i] = qv;
+        out_t[k * M + m] = qv;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_cast_dual(const void *x, const float *scale, void *out, void *out_t, int64_t M, int64_t K,
+                                 int num_sms, cudaStream_t s)
+{
+    const bool vec = M % 16 == 0 && K % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0 && (reinterpret_cast<uintptr_t>(out_t) & 15u) == 0;
+    if (vec) {
+        const int64_t tiles = ((M + T - 1) / T) * ((K + T - 1) / T);
+        const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+        k_fp8_cast_dual_v16<<<static_cast<unsigned>(tiles < cap ? tiles : cap), THREADS, 0, s>>>(
+            static_cast<const __nv_bfloat16 *>(x), scale, static_cast<uint8_t *>(out), static_cast<uint8_t *>(out_t),
+            M, K);
+    } else {
+        const int64_t n = M * K;
+        int64_t blocks = (n + THREADS - 1) / THREADS;
+        const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+        if (blocks > cap)
+            blocks = cap;
+        k_fp8_cast_dual_scalar<<<static_cast<unsigned>(blocks), THREADS, 0, s>>>(
+            static_cast<const __nv_bfloat16 *>(x), scale, static_cast<uint8_t *>(out), static_cast<uint8_t *>(out_t),
+            M, K);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace lf

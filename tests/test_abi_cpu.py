@@ -11,7 +11,8 @@ import layout_folding_gb300 as lf
 from layout_folding_gb300 import build as lfbuild
 
 EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
-            "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc"}
+            "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
+            "fp8_cast_dual"}
 
 
 @pytest.fixture(scope="module")
@@ -76,6 +77,17 @@ def test_gemm_nt_rejects_on_host(L, args, want):
 def test_gemm_nt_xent_rejects_on_host(L, args, want):
     ptrs = [P(a) if a is not None else None for a in args[:5]]
     assert L.gemm_nt_xent(*ptrs, *args[5:], None) == want
+
+
+def test_fp8_cast_dual_rejects_on_host(L):
+    L.fp8_cast_dual.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 2 + [ctypes.c_void_p]
+    assert L.fp8_cast_dual(None, P(A16), P(A16), P(A16), 4, 4, None) == 1
+    assert L.fp8_cast_dual(P(A16), None, P(A16), P(A16), 4, 4, None) == 1
+    assert L.fp8_cast_dual(P(A16), P(A16), P(A16), None, 4, 4, None) == 1
+    assert L.fp8_cast_dual(P(A16), P(A16), P(A16), P(A16), 0, 4, None) == 2
+    assert L.fp8_cast_dual(P(A16), P(A16), P(A16), P(A16), 4, -1, None) == 2
+    assert L.fp8_cast_dual(P(A16), P(A16), P(A16), P(A16), 1 << 31, 4, None) == 2
+    assert L.fp8_cast_dual(P(A16 + 1), P(A16), P(A16), P(A16), 4, 4, None) == 3
 
 
 def test_matmul_k1_rejects_on_host(L):
