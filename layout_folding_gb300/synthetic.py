@@ -50,6 +50,18 @@ def k1_operands(M: int = 64, N: int = 4096, head_dim: int = 128):
     return a, b
 
 
+def rope_operands(H: int = 64, S: int = 4096, max_position: int = 0):
+    """Inputs of the RoPE segment: inv_freq bf16 [H] = 1/10000^(2i/(2H)) (fp64,
+    rounded to fp32, then to bf16) and int64 position ids [S] = 0, 1, ..., wrapping at
+    `max_position` when it is positive (several sequences back to back)."""
+    inv = torch.tensor([10000.0 ** (-(2.0 * i) / (2 * H)) for i in range(H)],
+                       dtype=torch.float64).to(torch.float32).to(torch.bfloat16)
+    pos = torch.arange(S, dtype=torch.int64)
+    if max_position > 0:
+        pos = pos % max_position
+    return inv, pos
+
+
 @dataclass(frozen=True)
 class Workload:
     name: str

@@ -63,6 +63,7 @@ def _load():
             "oracle_matmul_k1_bf16": [P, P, I64, I64, P],
             "oracle_set_num_threads": [ctypes.c_int],
             "oracle_fp8_cast_dual": [P, I64, I64, ctypes.c_float, P, P],
+            "oracle_rope_cos_sin": [P, P, I64, I64, P, P],
         }
         for name, argtypes in sig.items():
             fn = getattr(lib, name)
@@ -249,3 +250,15 @@ def fp8_cast_dual(x, scale: float):
     out_t = np.empty((K, M), dtype=np.uint8)
     _load().oracle_fp8_cast_dual(_p(x), M, K, float(scale), _p(out), _p(out_t))
     return out, out_t
+
+
+def rope_cos_sin(inv_freq, positions, with_sin: bool = True):
+    """(cos [S, 2H], sin [S, 2H] | None) as bf16 bit patterns (uint16) of the
+    RoPE segment: angle[s, c] = fp32(inv_freq[c mod H] * float(positions[s]))."""
+    inv = _bits(inv_freq).ravel()
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64).ravel())
+    H, S = inv.shape[0], pos.shape[0]
+    cos_out = np.empty((S, 2 * H), dtype=np.uint16)
+    sin_out = np.empty((S, 2 * H), dtype=np.uint16) if with_sin else None
+    _load().oracle_rope_cos_sin(_p(inv), _p(pos), H, S, _p(cos_out), _p(sin_out))
+    return cos_out, sin_out

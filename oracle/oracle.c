@@ -15,6 +15,9 @@
  *  [P2] "Feature request: Schedule a small matmul op as a reduction (or
  *       pointwise) op" (NVIDIA/Fuser issue 3646) -- the T19 matmul and its
  *       broadcast/mul/squeeze rewrite.
+ *  [P3] "Improve the Inductor generated kernel for the pattern of output1 =
+ *       pointwise(intput); output2 = transpose(output1)" (pytorch issue
+ *       130015) -- the float8 cast and its column-major copy (Examples).
  *  [P4] "Allow reductions in matmul epilogues" (NVIDIA/Fuser issue 2213) --
  *       the fused matmul + cross-entropy fusion definition.
  */
@@ -242,6 +245,43 @@ void oracle_matmul_k1_bf16(const uint16_t *x, const uint16_t *w, int64_t M, int6
             double p = bf16_to_f64(x[i]) * bf16_to_f64(w[j]);
             out[i * N + j] = f32_to_bf16_rne((float)p);
         }
+}
+
+/*
+ * The RoPE segment around the K=1 matmul [P2, the kernel_math listing of the
+ * Mistral forward, T3 .. T26], one step per tensor:
+ *   T13[i]    = float(T3[i])             inv_freq, bf16 -> fp32 (exact)
+ *   T18[s]    = float(T4[s])             position id, int64 -> fp32 (round to nearest)
+ *   T19[i,s]  = T13[i] * T18[s]          the K=1 matmul: one fp32 multiply
+ *   T20[s,i]  = T19[i,s]                 permute to [S, H]
+ *   T21[s,c]  = c <  H ? T20[s,c]   : 0  pad H zeros on the right
+ *   T22[s,c]  = c >= H ? T20[s,c-H] : 0  pad H zeros on the left
+ *   T23[s,c]  = c < H ? T21[s,c] : T22[s,c]   cat of the padded halves (2H columns)
+ *   T24[s,c]  = cosf(T23[s,c])           fp32 cosine: cos of the fp32 argument,
+ *                                        rounded to fp32 (here from fp64 libm)
+ *   T26[s,c]  = bf16(T24[s,c])           round to nearest even
+ * cos_out is T26 as [S, 2H] row-major.  sin_out (may be NULL) is the same chain
+ * with sinf in place of cosf: the listing prints only the cosine branch; the
+ * segment's second [4096,128] output, T31, is read as the sine (the RoPE module
+ * returns the cosine and the sine of the same angles).
+ */
+void oracle_rope_cos_sin(const uint16_t *inv_freq, const int64_t *pos, int64_t H, int64_t S,
+                         uint16_t *cos_out, uint16_t *sin_out)
+{
+    for (int64_t s = 0; s < S; ++s) {
+        float t18 = (float)pos[s];
+        for (int64_t c = 0; c < 2 * H; ++c) {
+            float t21 = 0.0f, t22 = 0.0f;
+            if (c < H)
+                t21 = (float)(bf16_to_f64(inv_freq[c]) * (double)t18);       /* T20[s,c] */
+            else
+                t22 = (float)(bf16_to_f64(inv_freq[c - H]) * (double)t18);   /* T20[s,c-H] */
+            float t23 = c < H ? t21 : t22;
+            cos_out[s * 2 * H + c] = f32_to_bf16_rne((float)cos((double)t23));
+            if (sin_out)
+                sin_out[s * 2 * H + c] = f32_to_bf16_rne((float)sin((double)t23));
+        }
+    }
 }
 
 /*

@@ -376,3 +376,100 @@ def test_fp8_cast_dual_mutants_fail():
     assert not np.array_equal(no_clamp, ref)
     assert not np.array_equal(oracle.f32_to_e4m3(np.clip(truncating, -448, 448)), ref)
     assert not np.array_equal(out_t, out)                  # the second layout really is transposed
+
+
+# --------------------------------------------------------------- RoPE segment
+# "Feature request: Schedule a small matmul op as a reduction (or pointwise)
+# op", the Mistral forward listing T3 .. T26: angle = fp32(inv_freq[i] *
+# float(position)), the permute to [S, H], the pad/cat duplicate to 2H
+# columns, cos (and sin) in fp32, rounded to bf16.
+
+def _bf16_bits_to_f64(b):
+    return oracle.bf16_bits_to_f64(np.asarray(b, dtype=np.uint16))
+
+
+def rope_pin_failures(rope):
+    """Names of the pins `rope(inv_freq_bf16_tensor, positions) -> (cos, sin)`
+    (uint16 bf16 codes, [S, 2H]) violates."""
+    failed = []
+    with open(os.path.join(GOLDEN, "rope_cos_sin.json")) as f:
+        g = json.load(f)
+    inv = torch.tensor(g["inv_freq"], dtype=torch.bfloat16)
+    c, s = rope(inv, g["positions"])
+    H = len(g["inv_freq"])
+    want_c = np.array([[int(v, 16) for v in r] for r in g["cos_first_half"]], dtype=np.uint16)
+    want_s = np.array([[int(v, 16) for v in r] for r in g["sin_first_half"]], dtype=np.uint16)
+    if c.shape != (4, 2 * H) or not np.array_equal(c[:, :H], want_c) or not np.array_equal(s[:, :H], want_s):
+        failed.append("golden")
+    # the second half of the row repeats the first (pad + cat of the same freqs)
+    inv64, pos = synthetic.rope_operands(64, 300)
+    c, s = rope(inv64, pos.numpy())
+    if c.shape != (300, 128) or not (np.array_equal(c[:, :64], c[:, 64:]) and np.array_equal(s[:, :64], s[:, 64:])):
+        failed.append("duplicate halves")
+    # position 0: angle 0 for every frequency
+    if not (np.all(c[0] == 0x3F80) and np.all(s[0] == 0)):
+        failed.append("position zero")
+    # cos^2 + sin^2 = 1 within two bf16 roundings
+    cf, sf = _bf16_bits_to_f64(c), _bf16_bits_to_f64(s)
+    if np.max(np.abs(cf * cf + sf * sf - 1.0)) > 2 * 2.0 ** -8:
+        failed.append("pythagoras")
+    # double angle with power-of-two frequencies: angle(2p) = 2 * angle(p) exactly
+    inv_p2 = torch.tensor([2.0 ** -k for k in range(8)], dtype=torch.bfloat16)
+    p = np.arange(0, 200, dtype=np.int64)
+    c1, s1 = rope(inv_p2, p)
+    c2, s2 = rope(inv_p2, 2 * p)
+    a_c, a_s = _bf16_bits_to_f64(c1), _bf16_bits_to_f64(s1)
+    b_c, b_s = _bf16_bits_to_f64(c2), _bf16_bits_to_f64(s2)
+    if (np.max(np.abs(b_c - (2 * a_c * a_c - 1))) > 0.02 or np.max(np.abs(b_s - 2 * a_s * a_c)) > 0.02):
+        failed.append("double angle")
+    # negative positions: cos even, sin odd, bit for bit
+    cn, sn = rope(inv_p2, -p)
+    if not (np.array_equal(cn, c1) and np.array_equal(sn[1:], s1[1:] ^ 0x8000)):
+        failed.append("parity")
+    return failed
+
+
+def _oracle_rope(inv, pos):
+    return oracle.rope_cos_sin(inv, pos)
+
+
+def test_rope_pins():
+    assert rope_pin_failures(_oracle_rope) == []
+
+
+def test_rope_operands_follow_the_page_shapes():
+    inv, pos = synthetic.rope_operands()
+    assert inv.dtype == torch.bfloat16 and inv.shape == (64,) and pos.dtype == torch.int64 and pos.shape == (4096,)
+    assert float(inv[0]) == 1.0 and np.all(np.diff(inv.float().numpy()) < 0)
+    c, s = oracle.rope_cos_sin(inv, pos)
+    assert c.shape == (4096, 128) and s.shape == (4096, 128)
+
+
+def test_rope_mutants_fail_pins():
+    def swapped(inv, pos):
+        c, s = _oracle_rope(inv, pos)
+        return s, c
+
+    def no_cat(inv, pos):
+        c, s = _oracle_rope(inv, pos)
+        H = c.shape[1] // 2
+        c, s = c.copy(), s.copy()
+        c[:, H:] = 0
+        s[:, H:] = 0
+        return c, s
+
+    def reversed_freqs(inv, pos):                  # wrong index into inv_freq
+        return _oracle_rope(torch.flip(inv, [0]), pos)
+
+    def no_freq(inv, pos):                         # angle = position (dropped factor)
+        return _oracle_rope(torch.ones_like(inv), pos)
+
+    def off_by_one(inv, pos):
+        return _oracle_rope(inv, np.asarray(pos) + 1)
+
+    def sin_negated(inv, pos):
+        c, s = _oracle_rope(inv, pos)
+        return c, s ^ np.uint16(0x8000)
+
+    for m in (swapped, no_cat, reversed_freqs, no_freq, off_by_one, sin_negated):
+        assert rope_pin_failures(m), m.__name__
