@@ -350,6 +350,24 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
                       "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes}
         del ad, bd, out
     torch.cuda.empty_cache()
+    # RoPE segment (K=1 matmul + permute + cat + cos/sin -> bf16): the page's 4096
+    # positions, and 2^20 positions (32 sequences of 32768) for bandwidth
+    for label, (S, maxp) in (("rope_page", (4096, 0)), ("rope_scaled", (1 << 20, 32768))):
+        inv, pos = synthetic.rope_operands(64, S, max_position=maxp)
+        inv, pos = inv.to("cuda"), pos.to("cuda")
+        co = torch.empty(S, 128, dtype=torch.bfloat16, device="cuda")
+        so = torch.empty(S, 128, dtype=torch.bfloat16, device="cuda")
+
+        def step():
+            lf.rope_cos_sin(inv, pos, cos_out=co, sin_out=so, stream=stream)
+        times = timer.run(step, max(steps, 10), 3)
+        ms = statistics.median(times)
+        nbytes = 64 * 2 + S * 8 + 2 * S * 128 * 2
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[label] = {"H": 64, "S": S, "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes,
+                      "angles_per_s": round(S * 64 / (ms * 1e-3), 1)}
+        del inv, pos, co, so
     # fused fp8 cast, both layouts: the page's 4096 x 4096 and a scaled case larger than L2
     scale = torch.tensor([10.0], dtype=torch.float32, device="cuda")
     for label, (M, K) in (("fp8_cast_page", (4096, 4096)), ("fp8_cast_scaled", (16384, 16384))):

@@ -115,6 +115,38 @@ lf_status matmul_k1(const float *a, const float *b, float *out,
                     int64_t M, int64_t N, cudaStream_t stream);
 
 /*
+ * rope_cos_sin -- the RoPE segment around the K=1 matmul, in one kernel.
+ *
+ * Source: "Feature request: Schedule a small matmul op as a reduction (or
+ * pointwise) op" (NVIDIA/Fuser issue 3646), the Mistral forward listing from
+ * the bf16 inverse frequencies T3 and int64 position ids T4 to the bf16
+ * output T26: the K=1 matmul T19 (one fp32 multiply per element), its
+ * permute to [S, H] (T20), the pads and cat that repeat it to 2H columns
+ * (T21..T23), cosf (T24) and the cast to bf16 (T26).  The page asks for this
+ * segment to run without the matmul splitting it; here it is one launch with
+ * the permuted layout written directly.
+ *
+ *   inv_freq : bf16 [H], device, 2-byte aligned.
+ *   positions: int64 [S], device, 8-byte aligned (a batch of sequences is
+ *              passed flattened).
+ *   cos_out  : bf16 [S, 2H], device, row-major:
+ *                angle[s,i] = fp32(float(inv_freq[i]) * float(positions[s]))
+ *                cos_out[s, i] = cos_out[s, H + i] = bf16_rn(cosf(angle[s,i]))
+ *              (float(int64) rounds to nearest; cosf is CUDA's, within 2
+ *              fp32 ulp, so an element can differ from the bf16 rounding of
+ *              the exact cosine by one bf16 ulp).
+ *   sin_out  : bf16 [S, 2H] or NULL: the same with sinf -- the listing prints
+ *              only the cosine branch; the segment's second [4096,128] output
+ *              is taken to be the sine of the same angles.
+ *   1 <= H, S < 2^31.  H % 8 == 0 with 16-byte aligned inv_freq and outputs
+ *   takes the vectorised kernel; anything else the element-wise one.
+ * The caller owns every buffer; nothing is allocated.  Host-side checks return
+ * LF_ERR_NULL / LF_ERR_SHAPE / LF_ERR_ALIGN before anything is enqueued.
+ */
+lf_status rope_cos_sin(const void *inv_freq, const int64_t *positions, void *cos_out, void *sin_out_or_null,
+                       int64_t H, int64_t S, cudaStream_t stream);
+
+/*
  * fp8_cast_dual -- the float8 training cast, written in both layouts by one
  * kernel.
  *

@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
   gemm_nt_xent(x, w, labels, want_grad=False)   -> (loss fp32 [M], grad bf16 [M,N] | None)
   matmul_k1(a, b, out=None)                     -> out = a * b     (fp32, K=1)
   fp8_cast_dual(x, scale)                       -> (out e4m3 [M,K], out_t e4m3 [M,K] column-major)
+  rope_cos_sin(inv_freq, positions)             -> (cos bf16 [S,2H], sin bf16 [S,2H])
 """
 from __future__ import annotations
 
@@ -56,6 +57,8 @@ def lib():
         L.matmul_k1.restype = I32
         L.fp8_cast_dual.argtypes = [P, P, P, P, I64, I64, P]
         L.fp8_cast_dual.restype = I32
+        L.rope_cos_sin.argtypes = [P, P, P, P, I64, I64, P]
+        L.rope_cos_sin.restype = I32
         L.lf_status_string.argtypes = [I32]
         L.lf_status_string.restype = ctypes.c_char_p
         L.lf_check_device_error.argtypes = [P]
@@ -191,6 +194,30 @@ def fp8_cast_dual(x, scale, out=None, out_t=None, stream=None):
     _check(lib().fp8_cast_dual(x.data_ptr(), scale.data_ptr(), out.data_ptr(), out_t.data_ptr(), M, K,
                                _stream(stream)), "fp8_cast_dual")
     return out, out_t
+
+
+def rope_cos_sin(inv_freq, positions, cos_out=None, sin_out=None, want_sin=True, stream=None):
+    """The RoPE segment: inv_freq bf16 [H], positions int64 (any shape, S
+    elements, contiguous).  Returns (cos, sin) bf16 [S, 2H] with
+    cos[s, i] = cos[s, H + i] = bf16(cosf(fp32(inv_freq[i] * float(positions[s])))),
+    sin likewise (None when want_sin is False and no sin_out is given)."""
+    import torch
+    _require(inv_freq, torch.bfloat16, "inv_freq")
+    _require(positions, torch.int64, "positions")
+    H, S = inv_freq.numel(), positions.numel()
+    if cos_out is None:
+        cos_out = torch.empty(S, 2 * H, dtype=torch.bfloat16, device=inv_freq.device)
+    if sin_out is None and want_sin:
+        sin_out = torch.empty(S, 2 * H, dtype=torch.bfloat16, device=inv_freq.device)
+    for t, name in ((cos_out, "cos_out"), (sin_out, "sin_out")):
+        if t is not None:
+            _require(t, torch.bfloat16, name)
+            if t.numel() != S * 2 * H:
+                raise ValueError("%s must hold S * 2H elements" % name)
+    _check(lib().rope_cos_sin(inv_freq.data_ptr(), positions.data_ptr(), cos_out.data_ptr(),
+                              None if sin_out is None else sin_out.data_ptr(), H, S, _stream(stream)),
+           "rope_cos_sin")
+    return cos_out, sin_out
 
 
 def check_device_error(stream=None):

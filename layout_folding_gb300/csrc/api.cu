@@ -380,6 +380,25 @@ lf_status matmul_k1(const float *a, const float *b, float *out, int64_t M, int64
     return launched(lf::launch_matmul_k1_f32(a, b, out, M, N, d->num_sms, stream), 1);
 }
 
+lf_status rope_cos_sin(const void *inv_freq, const int64_t *positions, void *cos_out, void *sin_out_or_null,
+                       int64_t H, int64_t S, cudaStream_t stream)
+{
+    if (!inv_freq || !positions || !cos_out)
+        return LF_ERR_NULL;
+    if (H <= 0 || S <= 0 || H > MAX_DIM || S > MAX_DIM)
+        return LF_ERR_SHAPE;
+    const auto misaligned = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+    if (misaligned(inv_freq, 2) || misaligned(positions, 8) || misaligned(cos_out, 2) ||
+        (sin_out_or_null && misaligned(sin_out_or_null, 2)))
+        return LF_ERR_ALIGN;
+    DeviceState *d = nullptr;
+    lf_status st = current_device(&d);
+    if (st != LF_OK)
+        return st;
+    return launched(lf::launch_rope_cos_sin(inv_freq, positions, cos_out, sin_out_or_null, H, S, d->num_sms, stream),
+                    1);
+}
+
 lf_status fp8_cast_dual(const void *x, const float *scale, void *out, void *out_t, int64_t M, int64_t K,
                         cudaStream_t stream)
 {

@@ -77,6 +77,8 @@ cudaError_t launch_matmul_k1_f32(const float *a, const float *b, float *out, int
                                  int num_sms, cudaStream_t s);
 cudaError_t launch_matmul_k1_bf16(const void *x, const void *w, void *out, int64_t M, int64_t N,
                                   int num_sms, cudaStream_t s);
+cudaError_t launch_rope_cos_sin(const void *inv_freq, const int64_t *pos, void *cos_out, void *sin_out, int64_t H,
+                                int64_t S, int num_sms, cudaStream_t s);
 cudaError_t launch_fp8_cast_dual(const void *x, const float *scale, void *out, void *out_t, int64_t M, int64_t K,
                                  int num_sms, cudaStream_t s);
 

@@ -12,7 +12,7 @@ from layout_folding_gb300 import build as lfbuild
 
 EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
             "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
-            "fp8_cast_dual"}
+            "fp8_cast_dual", "rope_cos_sin"}
 
 
 @pytest.fixture(scope="module")
@@ -88,6 +88,18 @@ def test_fp8_cast_dual_rejects_on_host(L):
     assert L.fp8_cast_dual(P(A16), P(A16), P(A16), P(A16), 4, -1, None) == 2
     assert L.fp8_cast_dual(P(A16), P(A16), P(A16), P(A16), 1 << 31, 4, None) == 2
     assert L.fp8_cast_dual(P(A16 + 1), P(A16), P(A16), P(A16), 4, 4, None) == 3
+
+
+def test_rope_cos_sin_rejects_on_host(L):
+    L.rope_cos_sin.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 2 + [ctypes.c_void_p]
+    assert L.rope_cos_sin(None, P(A16), P(A16), None, 64, 16, None) == 1
+    assert L.rope_cos_sin(P(A16), None, P(A16), None, 64, 16, None) == 1
+    assert L.rope_cos_sin(P(A16), P(A16), None, P(A16), 64, 16, None) == 1
+    assert L.rope_cos_sin(P(A16), P(A16), P(A16), None, 0, 16, None) == 2
+    assert L.rope_cos_sin(P(A16), P(A16), P(A16), None, 64, 0, None) == 2
+    assert L.rope_cos_sin(P(A16), P(A16 + 4), P(A16), None, 64, 16, None) == 3
+    assert L.rope_cos_sin(P(A16 + 1), P(A16), P(A16), None, 64, 16, None) == 3
+    assert L.rope_cos_sin(P(A16), P(A16), P(A16), P(A16 + 1), 64, 16, None) == 3
 
 
 def test_matmul_k1_rejects_on_host(L):

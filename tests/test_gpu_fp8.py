@@ -121,3 +121,22 @@ def test_launches_one_kernel():
     n0 = lf.launch_count()
     lf.fp8_cast_dual(x, s)
     assert lf.launch_count() - n0 == 1
+
+
+def test_four_row_tiles_with_ragged_tails():
+    """Large enough for the 256-row tile variant (at least 16 tiles per SM),
+    with a partial last row slab (M % 256 = 48) and a partial last column tile
+    (K % 64 = 16): sampled rows against the oracle, all of out_t by transposition."""
+    M, K = 256 * 40 + 48, 64 * 63 + 16
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ((M + 255) // 256) * ((K + 63) // 64) >= 16 * sms
+    x_cpu = synthetic.bf16_normal((M, K), 1.0, 17)
+    out, out_t = run(x_cpu, 10.0)
+    assert torch.equal(out.view(torch.uint8), out_t.contiguous().view(torch.uint8))
+    rows = sorted({0, 63, 64, 191, 255, 256, M - 49, M - 48, M - 17, M - 16, M - 1}
+                  | set(np.random.default_rng(4).integers(0, M, 40).tolist()))
+    ref, _ = oracle.fp8_cast_dual(x_cpu[rows], 10.0)
+    np.testing.assert_array_equal(out.view(torch.uint8)[rows].cpu().numpy(), ref)
+    cols = [0, 63, 64, K - 17, K - 16, K - 1]
+    ref_cols, _ = oracle.fp8_cast_dual(x_cpu[:, cols].contiguous(), 10.0)
+    np.testing.assert_array_equal(out_t.view(torch.uint8)[:, cols].cpu().numpy(), ref_cols)
