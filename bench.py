@@ -309,7 +309,8 @@ def run_ours(args, rank, world, local_rank):
 def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
     res = {}
     steps = max(3, min(args.steps, 10))
-    for name, want_grad in (("xent_grad", True), ("xent_loss", False)):
+    want = {p.strip() for p in args.paths.split(",") if p.strip()}
+    for name, want_grad in ((("xent_grad", True), ("xent_loss", False)) if "xent" in want else ()):
         wl = synthetic.WORKLOADS[name]
         inp = synthetic.make_workload(name)
         x, w, lab = inp["x"].to("cuda"), inp["w"].to("cuda"), inp["labels"].to("cuda")
@@ -335,7 +336,7 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
         torch.cuda.empty_cache()
     # K=1: the page's [64,1]x[1,4096] (latency regime) and a scaled column count for bandwidth
     a, b = synthetic.k1_operands(64, 4096)
-    for label, N in (("k1_rope", 4096), ("k1_scaled", 1 << 23)):
+    for label, N in ((("k1_rope", 4096), ("k1_scaled", 1 << 23)) if "k1" in want else ()):
         bb = torch.arange(N, dtype=torch.float32).reshape(1, N) if N != 4096 else b
         ad, bd = a.to("cuda"), bb.to("cuda")
         out = torch.empty(64, N, dtype=torch.float32, device="cuda")
@@ -352,7 +353,7 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
     torch.cuda.empty_cache()
     # RoPE segment (K=1 matmul + permute + cat + cos/sin -> bf16): the page's 4096
     # positions, and 2^20 positions (32 sequences of 32768) for bandwidth
-    for label, (S, maxp) in (("rope_page", (4096, 0)), ("rope_scaled", (1 << 20, 32768))):
+    for label, (S, maxp) in ((("rope_page", (4096, 0)), ("rope_scaled", (1 << 20, 32768))) if "rope" in want else ()):
         inv, pos = synthetic.rope_operands(64, S, max_position=maxp)
         inv, pos = inv.to("cuda"), pos.to("cuda")
         co = torch.empty(S, 128, dtype=torch.bfloat16, device="cuda")
@@ -370,7 +371,8 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
         del inv, pos, co, so
     # fused fp8 cast, both layouts: the page's 4096 x 4096 and a scaled case larger than L2
     scale = torch.tensor([10.0], dtype=torch.float32, device="cuda")
-    for label, (M, K) in (("fp8_cast_page", (4096, 4096)), ("fp8_cast_scaled", (16384, 16384))):
+    for label, (M, K) in ((("fp8_cast_page", (4096, 4096)), ("fp8_cast_scaled", (16384, 16384))) if "fp8" in want
+                          else ()):
         x = synthetic.bf16_normal((M, K), 1.0, 15).to("cuda")
         out = torch.empty(M, K, dtype=torch.float8_e4m3fn, device="cuda")
         out_t = torch.empty(K, M, dtype=torch.float8_e4m3fn, device="cuda").t()
@@ -464,7 +466,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--headline-only", action="store_true", help="skip the xent and K=1 paths")
+    ap.add_argument("--headline-only", action="store_true", help="skip every secondary path")
+    ap.add_argument("--paths", default="xent,k1,rope,fp8",
+                    help="secondary paths to time after the headline (comma list of xent, k1, rope, fp8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     args = ap.parse_args(argv)
