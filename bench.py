@@ -39,6 +39,12 @@ L2_FLUSH_BYTES = 256 << 20
 LAUNCH_SHADOW_CYCLES = 200_000   # ~0.1 ms of device-side delay before each timed step
 KERNEL_SOURCES = ["layout_folding_gb300/csrc/gemm_nt_pair.cu", "layout_folding_gb300/csrc/lf_gemm_common.cuh",
                   "layout_folding_gb300/csrc/lf_ptx.cuh", "layout_folding_gb300/csrc/lf_internal.h"]
+# source files whose hash a recorded DRAM figure is tied to, per kernel
+TRAFFIC_SOURCES = {
+    "k_gemm_nt_pair<EPI_STORE>": KERNEL_SOURCES,
+    "k_fp8_cast_dual_v16": ["layout_folding_gb300/csrc/fp8_cast.cu"],
+    "k_rope_cos_sin_v8": ["layout_folding_gb300/csrc/rope.cu"],
+}
 HEADLINE_KERNEL = "k_gemm_nt_pair<EPI_STORE>"   # CTA-pair tiles, stream-K split (chosen automatically here)
 
 
@@ -78,9 +84,9 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (sources or KERNEL_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -95,7 +101,7 @@ def recorded_traffic(kernel: str, workload: str):
     with open(path) as f:
         rec = json.load(f)
     e = rec.get(kernel, {}).get(workload)
-    if not e or e.get("kernel_hash") != kernel_hash():
+    if not e or e.get("kernel_hash") != kernel_hash(TRAFFIC_SOURCES.get(kernel)):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -367,7 +373,8 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[label] = {"H": 64, "S": S, "ms": round(ms, 5), "GB/s": round(gbs, 1),
                       "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes,
-                      "angles_per_s": round(S * 64 / (ms * 1e-3), 1)}
+                      "angles_per_s": round(S * 64 / (ms * 1e-3), 1),
+                      "traffic": recorded_traffic("k_rope_cos_sin_v8", label)}
         del inv, pos, co, so
     # fused fp8 cast, both layouts: the page's 4096 x 4096 and a scaled case larger than L2
     scale = torch.tensor([10.0], dtype=torch.float32, device="cuda")
@@ -384,7 +391,8 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
         nbytes = M * K * (2 + 1 + 1)
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[label] = {"M": M, "K": K, "scale": 10.0, "ms": round(ms, 5), "GB/s": round(gbs, 1),
-                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes}
+                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes,
+                      "traffic": recorded_traffic("k_fp8_cast_dual_v16", label)}
         del x, out, out_t
     torch.cuda.empty_cache()
     return res
