@@ -19,15 +19,18 @@
 //      pair GEMM kernel);
 //   2. epilogue, one warpgroup per tile (8 epilogue warps; a thread owns a
 //      row of its tile): per-(row, tile) statistics (max, sum exp(z - max),
-//      label logit); warpgroup 1 hands its row statistics to warpgroup 0
+//      label logit) in one pass over TMEM with a running max, leaving
+//      exp(z - running max) in TMEM; warpgroup 1 hands its row statistics to warpgroup 0
 //      through shared memory, which merges the pair's two tiles and stores one
 //      partial per row in slot [row, qi]; then the CTA releases a flag
 //      (epoch << 32 | round+1);
 //   3. the lanes poll the flags of the group's Q pairs in parallel (acquire,
 //      bounded), each thread merges its row's Q pair partials into (row max,
-//      log sum) with float4 loads, 32 partials per round trip -- the
+//      log sum), 32 partials per round trip (stored partial-major, so the
+//      loads of a warp are coalesced) -- the
 //      warpgroup holding tile 0 also writes loss[row] -- and writes
-//      grad = exp(z - lse) - onehot for its tile from TMEM; the accumulator is
+//      grad = exp(z - lse) - onehot for its tile from TMEM, staged per warp in
+//      shared memory so the stores are row-contiguous; the accumulator is
 //      released for the next round.
 // Measured per round at 4096x32768x4096 (pair 0, one GB300): mainloop ~47 us,
 // then, serialised because the two accumulators fill TMEM: statistics of the
@@ -55,7 +58,11 @@ constexpr int OP_THREADS = 320;     // producer, MMA, and one epilogue warpgroup
 constexpr int OP_EPI_WARPS = 4;    // per warpgroup (= per tile)
 constexpr int OP_NUM_BARS = 2 * OP_STAGES + 2 + 2 + 3;  // ring, tfull[2], tempty[2], drain, publish, exchange
 constexpr int OP_XCH_BYTES = 2 * BM * 4;                  // tile-1 row statistics handed to warpgroup 0
-constexpr int OP_SMEM_BYTES = OP_STAGES * OP_STAGE_BYTES + 1024 + OP_NUM_BARS * 8 + 16 + OP_XCH_BYTES;
+constexpr int OP_CHUNKS = BN / 32;                        // 32-column chunks of a tile row
+constexpr int OP_STG_WARP_BYTES = 32 * 32 * 2;            // a warp's 32 rows x 32 bf16 gradient columns
+constexpr int OP_STG_OFF =
+    ((OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8 + 16 + OP_XCH_BYTES + 127) / 128) * 128;
+constexpr int OP_SMEM_BYTES = 1024 + OP_STG_OFF + 2 * OP_EPI_WARPS * OP_STG_WARP_BYTES;
 constexpr uint32_t OP_IDESC = idesc_bf16_f32(OP_M, BN);
 constexpr uint64_t OP_ABORT_SETTLE_NS = 100000;
 constexpr int ERR_OP_FLAG = 0x108;  // a group member never published its partials
@@ -81,54 +88,221 @@ __device__ __forceinline__ bool op_work(const GemmParams &p, int pair, int r, Op
     return true;
 }
 
-// Merge n (max, sum) partials of one row, pm[j], ps[j] for j < n, into the
-// row's max `m` and sum `s` of exp(z - m): online rescaling, 32 partials per
-// batch (8 float4 loads of each array in flight when vec4), so a row costs
-// ceil(n / 32) dependent L2 round trips.
-__device__ __forceinline__ void merge_row_partials(const float *pm, const float *ps, int n, bool vec4, float &m,
+// 2^x with the PTX approximation (relative error about 2^-22; results below
+// 2^-126 flush to zero, which no sum or gradient here can see).
+__device__ __forceinline__ float op_ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Tree max / sum of the first `n` (all when FULL) of 32 values held as bits.
+template <bool FULL>
+__device__ __forceinline__ float op_tree_max_bits(const uint32_t (&u)[32], int n)
+{
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float lo = (FULL || i < n) ? __uint_as_float(u[i]) : -CUDART_INF_F;
+        const float hi = (FULL || i + 16 < n) ? __uint_as_float(u[i + 16]) : -CUDART_INF_F;
+        t[i] = fmaxf(lo, hi);
+    }
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            t[i] = fmaxf(t[i], t[i + w]);
+    return t[0];
+}
+
+__device__ __forceinline__ float op_tree_sum_bits(const uint32_t (&u)[32])
+{
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        t[i] = __uint_as_float(u[i]) + __uint_as_float(u[i + 16]);
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            t[i] += t[i + w];
+    return t[0];
+}
+
+__device__ __forceinline__ float op_tree_max(const float (&a)[32])
+{
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        t[i] = fmaxf(a[i], a[i + 16]);
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            t[i] = fmaxf(t[i], t[i + w]);
+    return t[0];
+}
+
+__device__ __forceinline__ float op_tree_sum(const float (&a)[32])
+{
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        t[i] = a[i] + a[i + 16];
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            t[i] += t[i + w];
+    return t[0];
+}
+
+// Merge n (max, sum) partials of one row, pm[j * stride], ps[j * stride] for
+// j < n, into the row's max `m` and sum `s` of exp(z - m): online rescaling,
+// 32 partials per batch.  The partials are stored partial-major, so the 32
+// rows of a warp read 128 contiguous bytes per partial.
+__device__ __forceinline__ void merge_row_partials(const float *pm, const float *ps, size_t stride, int n, float &m,
                                                    float &s)
 {
     m = -CUDART_INF_F;
     s = 0.f;
     for (int j0 = 0; j0 < n; j0 += 32) {
         float a[32], b[32];
-        if (vec4) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = j0 + 4 * i;
-                float4 fa = make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
-                float4 fb = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (j < n) {
-                    fa = __ldcg(reinterpret_cast<const float4 *>(pm + j));
-                    fb = __ldcg(reinterpret_cast<const float4 *>(ps + j));
-                }
-                a[4 * i] = fa.x, a[4 * i + 1] = fa.y, a[4 * i + 2] = fa.z, a[4 * i + 3] = fa.w;
-                b[4 * i] = fb.x, b[4 * i + 1] = fb.y, b[4 * i + 2] = fb.z, b[4 * i + 3] = fb.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int j = j0 + i;
-                a[i] = j < n ? __ldcg(pm + j) : -CUDART_INF_F;
-                b[i] = j < n ? __ldcg(ps + j) : 0.f;
-            }
+        for (int i = 0; i < 32; ++i) {
+            const int j = j0 + i;
+            a[i] = j < n ? __ldcg(pm + j * stride) : -CUDART_INF_F;
+            b[i] = j < n ? __ldcg(ps + j * stride) : 0.f;
         }
+        const float nm = fmaxf(m, op_tree_max(a));
+        const float nml = nm * LOG2E;
+        s *= op_ex2((m - nm) * LOG2E);
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-            if (j0 + i >= n) {  // the tail of a float4 past n
-                a[i] = -CUDART_INF_F;
-                b[i] = 0.f;
-            }
-        float cm = a[0];
-#pragma unroll
-        for (int i = 1; i < 32; ++i)
-            cm = fmaxf(cm, a[i]);
-        const float nm = fmaxf(m, cm);
-        s *= exp2f((m - nm) * LOG2E);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            s += b[i] * exp2f((a[i] - nm) * LOG2E);
+            b[i] *= op_ex2(fmaf(a[i], LOG2E, -nml));
+        s += op_tree_sum(b);
         m = nm;
+    }
+}
+
+// Makes the 32 registers of a TMEM load depend on a point after
+// tcgen05.wait::ld, so no use of them is scheduled before the wait.
+__device__ __forceinline__ void op_regs_after_wait(uint32_t (&v)[32])
+{
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                   "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
+}
+
+// Statistics of this thread's row of one tile in a single pass over TMEM
+// ("Allow reductions in matmul epilogues", fusion example: row max, exp(z -
+// max) and its sum, the label logit).  Chunk c is taken relative to the
+// running max m_c (the max over chunks 0..c): e = exp(z - m_c) is written
+// back over z, and the sum is rescaled whenever the max grows, so the tile
+// is read once.  Returns the tile's max and sum of exp(z - max); cm[c] = m_c,
+// from which the gradient rescales chunk c.  The next chunk's TMEM load is in
+// flight while the current one is processed; max and sum are tree reductions.
+// FULL: every column of the tile is < N (all tiles but a ragged last one).
+template <bool FULL>
+__device__ __forceinline__ void op_tile_stats(const GemmParams &p, uint32_t taddr, int nb, int lab,
+                                              float (&cm)[OP_CHUNKS], float &mx, float &se, float &zl, bool &have)
+{
+    const int col0 = nb * BN;
+    const int lab_local = lab - col0;
+    mx = -CUDART_INF_F;
+    se = 0.f;
+    have = false;
+    uint32_t v[2][32];
+    tmem_ld_32x32b_x32(taddr, v[0]);
+#pragma unroll
+    for (int c = 0; c < OP_CHUNKS; ++c) {
+        const int nvalid = FULL ? 32 * (OP_CHUNKS - c) : p.N - (col0 + c * 32);  // <= 0 past the last column
+        tmem_wait_ld();
+        if (c + 1 < OP_CHUNKS && nvalid > 32)
+            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>((c + 1) * 32), v[(c + 1) & 1]);
+        cm[c] = mx;
+        if (nvalid > 0) {
+            uint32_t(&u)[32] = v[c & 1];
+            op_regs_after_wait(u);
+            const int li = lab_local - c * 32;
+            if (static_cast<unsigned>(li) < 32u) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i == li)
+                        zl = __uint_as_float(u[i]);
+                have = true;
+            }
+            const float m_c = fmaxf(mx, op_tree_max_bits<FULL>(u, nvalid));
+            const float mcl = m_c * LOG2E;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                u[i] = __float_as_uint((FULL || i < nvalid) ? op_ex2(fmaf(__uint_as_float(u[i]), LOG2E, -mcl)) : 0.f);
+            se = se * op_ex2((mx - m_c) * LOG2E) + op_tree_sum_bits(u);
+            mx = m_c;
+            cm[c] = m_c;
+            tmem_st_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), u);
+        }
+    }
+    tmem_wait_st();
+}
+
+// grad = bf16_rn(e * scale[c] - [n == label]) for this thread's row of one
+// tile, e = exp(z - m_c) read back from TMEM, scale[c] = exp(m_c - lse).
+// The warp's 32 rows x 32 columns of a chunk are staged in shared memory
+// (16-byte pieces XOR-swizzled by row pair, conflict-free both ways) and
+// stored 8 rows x 64 bytes per instruction instead of 32 rows x 16 bytes.
+// (Double-buffering these TMEM loads spilled registers: 168 is the limit at
+// 10 warps per CTA.)
+__device__ __forceinline__ void op_tile_grad(const GemmParams &p, uint32_t taddr, int row0, int nb, int lab,
+                                             const float (&scale)[OP_CHUNKS], uint8_t *stg)
+{
+    const int lane = threadIdx.x & 31;
+    const int col0 = nb * BN;
+    const int lab_local = lab - col0;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+#pragma unroll
+    for (int c = 0; c < OP_CHUNKS; ++c) {
+        const int col = col0 + c * 32;
+        const int nvalid = p.N - col;  // warp-uniform
+        if (nvalid > 0) {
+            uint32_t u[32];
+            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), u);
+            tmem_wait_ld();
+            op_regs_after_wait(u);
+            const int li = lab_local - c * 32;
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float g0 = __uint_as_float(u[2 * i]) * scale[c];
+                float g1 = __uint_as_float(u[2 * i + 1]) * scale[c];
+                if (2 * i == li)
+                    g0 -= 1.f;
+                if (2 * i + 1 == li)
+                    g1 -= 1.f;
+                pk[i] = pack_bf16(g0, g1);
+            }
+            // row `lane`, piece j (8 columns) at slot j ^ ((lane >> 1) & 3)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = 8 * i + (lane >> 2);  // row of the warp's 32
+                const int pc = lane & 3;            // 8-column piece
+                const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((pc ^ ((r >> 1) & 3)) << 4));
+                const int grow = row0 + r;
+                const int gcol = col + pc * 8;  // N % 8 == 0: a piece is all in or all out
+                if (grow < p.M && gcol < p.N)
+                    *reinterpret_cast<uint4 *>(out + static_cast<size_t>(grow) * p.N + gcol) = val;
+            }
+            __syncwarp();
+        }
     }
 }
 
@@ -306,8 +480,8 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
         // w reads TMEM lanes 32 * (w % 4) .., one row per thread.
         const int t = (warp - 2) >> 2;
         const int q = warp & 3;
+        uint8_t *stg = gbase + OP_STG_OFF + (warp - 2) * OP_STG_WARP_BYTES;
         const int rloc = q * 32 + lane;
-        const PartialAdd none = {nullptr, 0, 0, 0};
         uint32_t eph = 0;
         uint32_t pub_phase = 0;
         const unsigned long long epoch_hi = static_cast<unsigned long long>(p.epoch) << 32;
@@ -315,7 +489,8 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
         uint32_t xch_phase = 0;
         OpWork w;
         for (int r = 0; r < p.op_rounds && op_work(p, pair, r, w); ++r) {
-            const int row = w.mb * OP_M + static_cast<int>(rank) * BM + rloc;
+            const int row0 = w.mb * OP_M + static_cast<int>(rank) * BM + q * 32;  // lane 0's row
+            const int row = row0 + lane;
             const bool row_ok = row < p.M;
             const bool mine = t < w.ntile;  // the pair's last tile may be missing (odd tile count)
             const int nb = w.nb0 + t;
@@ -324,7 +499,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             //    is left in TMEM as e = exp(z - tile max) for the gradient
             const int lab = row_ok ? p.labels[row] : -1;
             float mx = -CUDART_INF_F, se = 0.f;
-            float tmax = 0.f;
+            float cm[OP_CHUNKS];
             if (mine) {
                 const bool got = wait_bar(TFULL_BAR(t), eph, abort_flag, p, ERR_EPI, peer_abort);
                 if (!__all_sync(0xffffffffu, got))
@@ -333,9 +508,10 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                 tc_fence_after();
                 float zl = 0.f;
                 bool have;
-                tmax = xent_tile_max(p, taddr, lab, nb, zl, have);
-                se = xent_tile_exp_store(p, taddr, nb, tmax);
-                mx = tmax;
+                if ((nb + 1) * BN <= p.N)
+                    op_tile_stats<true>(p, taddr, nb, lab, cm, mx, se, zl, have);
+                else
+                    op_tile_stats<false>(p, taddr, nb, lab, cm, mx, se, zl, have);
                 if (row_ok && have && lab < p.N)
                     p.label_logit[row] = zl;
             }
@@ -358,12 +534,12 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                     xch_phase ^= 1u;
                     const float m1 = xch_mx[rloc], s1 = xch_se[rloc];
                     const float nm = fmaxf(mx, m1);
-                    se = se * exp2f((mx - nm) * LOG2E) + s1 * exp2f((m1 - nm) * LOG2E);
+                    se = se * op_ex2((mx - nm) * LOG2E) + s1 * op_ex2((m1 - nm) * LOG2E);
                     mx = nm;
                 }
-                if (row_ok) {
-                    p.part_max[static_cast<size_t>(row) * p.num_n_blocks + qi] = mx;
-                    p.part_sum[static_cast<size_t>(row) * p.num_n_blocks + qi] = se;
+                if (row_ok) {  // partial-major: slot [qi][row]
+                    p.part_max[static_cast<size_t>(qi) * p.M + row] = mx;
+                    p.part_sum[static_cast<size_t>(qi) * p.M + row] = se;
                 }
                 __threadfence();
                 __syncwarp();
@@ -395,16 +571,18 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             // 4. merge the row's op_Q pair partials
             float m = -CUDART_INF_F, s = 0.f;
             if (row_ok)
-                merge_row_partials(p.part_max + static_cast<size_t>(row) * p.num_n_blocks,
-                                   p.part_sum + static_cast<size_t>(row) * p.num_n_blocks, p.op_Q,
-                                   (p.num_n_blocks & 3) == 0, m, s);
+                merge_row_partials(p.part_max + row, p.part_sum + row, static_cast<size_t>(p.M), p.op_Q, m, s);
             const float ls = logf(s);
             if (row_ok && nb == 0) {
                 const int lab = p.labels[row];
                 p.loss[row] = (lab >= 0 && lab < p.N) ? (m - __ldcg(p.label_logit + row)) + ls : CUDART_NAN_F;
             }
             // 5. gradient of this tile straight from TMEM, then free the accumulator
-            xent_grad_from_exp(p, taddr, row, nb, lab, exp2f(((tmax - m) - ls) * LOG2E));
+            float scale[OP_CHUNKS];
+#pragma unroll
+            for (int c = 0; c < OP_CHUNKS; ++c)
+                scale[c] = op_ex2(((cm[c] - m) - ls) * LOG2E);
+            op_tile_grad(p, taddr, row0, nb, lab, scale, stg);
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
