@@ -17,25 +17,26 @@
 // covers k M blocks; round r of group g is M block r*k + g.  Per round:
 //   1. mainloop of the pair's one or two tiles (same TMA/MMA machinery as the
 //      pair GEMM kernel);
-//   2. epilogue, one warpgroup per tile (8 epilogue warps; a thread owns a
-//      row of its tile): per-(row, tile) statistics (max, sum exp(z - max),
-//      label logit) in one pass over TMEM with a running max, leaving
-//      exp(z - running max) in TMEM; warpgroup 1 hands its row statistics to warpgroup 0
-//      through shared memory, which merges the pair's two tiles and stores one
-//      partial per row in slot [row, qi]; then the CTA releases a flag
-//      (epoch << 32 | round+1);
+//   2. epilogue (8 warps; a thread owns a row, warpgroup h takes columns
+//      [128h, 128h + 128) of every tile): per-(row, half tile) statistics
+//      (max, sum exp(z - max), label logit) in one pass over TMEM with a
+//      running max, leaving exp(z - running max) in TMEM; warpgroup 1 hands
+//      its statistics to warpgroup 0 through shared memory, which merges the
+//      pair's four per row, stores one partial per row in slot [qi][row]
+//      (partial-major) and releases the CTA's flag (epoch << 32 | round+1);
 //   3. the lanes poll the flags of the group's Q pairs in parallel (acquire,
-//      bounded), each thread merges its row's Q pair partials into (row max,
-//      log sum), 32 partials per round trip (stored partial-major, so the
-//      loads of a warp are coalesced) -- the
-//      warpgroup holding tile 0 also writes loss[row] -- and writes
-//      grad = exp(z - lse) - onehot for its tile from TMEM, staged per warp in
-//      shared memory so the stores are row-contiguous; the accumulator is
-//      released for the next round.
-// Measured per round at 4096x32768x4096 (pair 0, one GB300): mainloop ~47 us,
-// then, serialised because the two accumulators fill TMEM: statistics of the
-// second tile + hand-off ~6 us, the group's slowest pair ~5 us, merge and
-// gradient ~11 us.
+//      bounded); each warpgroup merges half of the row's Q partials
+//      (coalesced loads, 16 per round trip), the halves are exchanged through
+//      shared memory, warpgroup 0 of the group's first pair writes loss[row];
+//   4. grad = exp(z - lse) - onehot from TMEM, staged per warp in shared
+//      memory so the stores are row-contiguous, first for the tile the next
+//      round's MMAs start with; each accumulator is released as soon as both
+//      warpgroups of both CTAs are done with it.
+// Measured per round at 4096x32768x4096 (one GB300): mainloop ~47 us; after
+// its last MMA, statistics ~1.6 us, publish ~2 us, the group's slowest pair
+// ~5 us (mainloop skew between pairs), merge ~2.7 us, gradient ~3.5 us (before
+// the column split: the split halves the statistics, merge and the wait for
+// the first freed accumulator).
 // The producer streams the next round's first K slices into the ring while
 // the epilogue runs.  Waits only go to the same round of the same group, whose
 // pairs never wait on anything later, so there is no cycle; every wait is
@@ -56,9 +57,10 @@ constexpr int OP_STAGE_BYTES = OP_A_BYTES + OP_B_BYTES;
 constexpr int OP_TMEM_COLS = 2 * BN;  // tile A: columns [0, 256), tile B: [256, 512)
 constexpr int OP_THREADS = 320;     // producer, MMA, and one epilogue warpgroup per tile
 constexpr int OP_EPI_WARPS = 4;    // per warpgroup (= per tile)
-constexpr int OP_NUM_BARS = 2 * OP_STAGES + 2 + 2 + 3;  // ring, tfull[2], tempty[2], drain, publish, exchange
-constexpr int OP_XCH_BYTES = 2 * BM * 4;                  // tile-1 row statistics handed to warpgroup 0
-constexpr int OP_CHUNKS = BN / 32;                        // 32-column chunks of a tile row
+constexpr int OP_NUM_BARS = 2 * OP_STAGES + 2 + 2 + 4;  // ring, tfull[2], tempty[2], drain, publish, exchange, merge
+constexpr int OP_XCH_BYTES = 8 * BM * 4;  // (max, sum) per row: 2 half-tile statistics + 2 half merges
+constexpr int OP_HALF = BN / 2;           // columns of a tile taken by one epilogue warpgroup
+constexpr int OP_HCH = OP_HALF / 32;      // 32-column chunks of a half
 constexpr int OP_STG_WARP_BYTES = 32 * 32 * 2;            // a warp's 32 rows x 32 bf16 gradient columns
 constexpr int OP_STG_OFF =
     ((OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8 + 16 + OP_XCH_BYTES + 127) / 128) * 128;
@@ -130,58 +132,58 @@ __device__ __forceinline__ float op_tree_sum_bits(const uint32_t (&u)[32])
     return t[0];
 }
 
-__device__ __forceinline__ float op_tree_max(const float (&a)[32])
+// Merge n (max, sum) partials of one row, pm[j * stride], ps[j * stride] for
+// j < n, into the row's max `m` and sum `s` of exp(z - m): online rescaling,
+// 16 partials per batch (32 kept too many registers live).  The partials are stored partial-major, so the 32
+// rows of a warp read 128 contiguous bytes per partial.
+__device__ __forceinline__ float op_tree_max16(const float (&a)[16])
 {
-    float t[16];
+    float t[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        t[i] = fmaxf(a[i], a[i + 16]);
+    for (int i = 0; i < 8; ++i)
+        t[i] = fmaxf(a[i], a[i + 8]);
 #pragma unroll
-    for (int w = 8; w > 0; w >>= 1)
+    for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
         for (int i = 0; i < w; ++i)
             t[i] = fmaxf(t[i], t[i + w]);
     return t[0];
 }
 
-__device__ __forceinline__ float op_tree_sum(const float (&a)[32])
+__device__ __forceinline__ float op_tree_sum16(const float (&a)[16])
 {
-    float t[16];
+    float t[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        t[i] = a[i] + a[i + 16];
+    for (int i = 0; i < 8; ++i)
+        t[i] = a[i] + a[i + 8];
 #pragma unroll
-    for (int w = 8; w > 0; w >>= 1)
+    for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
         for (int i = 0; i < w; ++i)
             t[i] += t[i + w];
     return t[0];
 }
 
-// Merge n (max, sum) partials of one row, pm[j * stride], ps[j * stride] for
-// j < n, into the row's max `m` and sum `s` of exp(z - m): online rescaling,
-// 32 partials per batch.  The partials are stored partial-major, so the 32
-// rows of a warp read 128 contiguous bytes per partial.
 __device__ __forceinline__ void merge_row_partials(const float *pm, const float *ps, size_t stride, int n, float &m,
                                                    float &s)
 {
     m = -CUDART_INF_F;
     s = 0.f;
-    for (int j0 = 0; j0 < n; j0 += 32) {
-        float a[32], b[32];
+    for (int j0 = 0; j0 < n; j0 += 16) {
+        float a[16], b[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
             const int j = j0 + i;
             a[i] = j < n ? __ldcg(pm + j * stride) : -CUDART_INF_F;
             b[i] = j < n ? __ldcg(ps + j * stride) : 0.f;
         }
-        const float nm = fmaxf(m, op_tree_max(a));
+        const float nm = fmaxf(m, op_tree_max16(a));
         const float nml = nm * LOG2E;
         s *= op_ex2((m - nm) * LOG2E);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 16; ++i)
             b[i] *= op_ex2(fmaf(a[i], LOG2E, -nml));
-        s += op_tree_sum(b);
+        s += op_tree_sum16(b);
         m = nm;
     }
 }
@@ -198,7 +200,8 @@ __device__ __forceinline__ void op_regs_after_wait(uint32_t (&v)[32])
                    "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
 }
 
-// Statistics of this thread's row of one tile in a single pass over TMEM
+// Statistics of this thread's row of one half tile (128 columns from col0)
+// in a single pass over TMEM
 // ("Allow reductions in matmul epilogues", fusion example: row max, exp(z -
 // max) and its sum, the label logit).  Chunk c is taken relative to the
 // running max m_c (the max over chunks 0..c): e = exp(z - m_c) is written
@@ -206,12 +209,11 @@ __device__ __forceinline__ void op_regs_after_wait(uint32_t (&v)[32])
 // is read once.  Returns the tile's max and sum of exp(z - max); cm[c] = m_c,
 // from which the gradient rescales chunk c.  The next chunk's TMEM load is in
 // flight while the current one is processed; max and sum are tree reductions.
-// FULL: every column of the tile is < N (all tiles but a ragged last one).
+// FULL: every column of the half is < N (all but a ragged last tile).
 template <bool FULL>
-__device__ __forceinline__ void op_tile_stats(const GemmParams &p, uint32_t taddr, int nb, int lab,
-                                              float (&cm)[OP_CHUNKS], float &mx, float &se, float &zl, bool &have)
+__device__ __forceinline__ void op_half_stats(const GemmParams &p, uint32_t taddr, int col0, int lab,
+                                              float (&cm)[OP_HCH], float &mx, float &se, float &zl, bool &have)
 {
-    const int col0 = nb * BN;
     const int lab_local = lab - col0;
     mx = -CUDART_INF_F;
     se = 0.f;
@@ -219,10 +221,10 @@ __device__ __forceinline__ void op_tile_stats(const GemmParams &p, uint32_t tadd
     uint32_t v[2][32];
     tmem_ld_32x32b_x32(taddr, v[0]);
 #pragma unroll
-    for (int c = 0; c < OP_CHUNKS; ++c) {
-        const int nvalid = FULL ? 32 * (OP_CHUNKS - c) : p.N - (col0 + c * 32);  // <= 0 past the last column
+    for (int c = 0; c < OP_HCH; ++c) {
+        const int nvalid = FULL ? 32 * (OP_HCH - c) : p.N - (col0 + c * 32);  // <= 0 past the last column
         tmem_wait_ld();
-        if (c + 1 < OP_CHUNKS && nvalid > 32)
+        if (c + 1 < OP_HCH && nvalid > 32)
             tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>((c + 1) * 32), v[(c + 1) & 1]);
         cm[c] = mx;
         if (nvalid > 0) {
@@ -251,21 +253,20 @@ __device__ __forceinline__ void op_tile_stats(const GemmParams &p, uint32_t tadd
 }
 
 // grad = bf16_rn(e * scale[c] - [n == label]) for this thread's row of one
-// tile, e = exp(z - m_c) read back from TMEM, scale[c] = exp(m_c - lse).
+// half tile, e = exp(z - m_c) read back from TMEM, scale[c] = exp(m_c - lse).
 // The warp's 32 rows x 32 columns of a chunk are staged in shared memory
 // (16-byte pieces XOR-swizzled by row pair, conflict-free both ways) and
 // stored 8 rows x 64 bytes per instruction instead of 32 rows x 16 bytes.
 // (Double-buffering these TMEM loads spilled registers: 168 is the limit at
 // 10 warps per CTA.)
-__device__ __forceinline__ void op_tile_grad(const GemmParams &p, uint32_t taddr, int row0, int nb, int lab,
-                                             const float (&scale)[OP_CHUNKS], uint8_t *stg)
+__device__ __forceinline__ void op_half_grad(const GemmParams &p, uint32_t taddr, int row0, int col0, int lab,
+                                             const float (&scale)[OP_HCH], uint8_t *stg)
 {
     const int lane = threadIdx.x & 31;
-    const int col0 = nb * BN;
     const int lab_local = lab - col0;
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 #pragma unroll
-    for (int c = 0; c < OP_CHUNKS; ++c) {
+    for (int c = 0; c < OP_HCH; ++c) {
         const int col = col0 + c * 32;
         const int nvalid = p.N - col;  // warp-uniform
         if (nvalid > 0) {
@@ -306,6 +307,37 @@ __device__ __forceinline__ void op_tile_grad(const GemmParams &p, uint32_t taddr
     }
 }
 
+// (m, s) <- the merge of two (max, sum of exp(z - max)) statistics; an empty
+// one (max = -inf) leaves the other unchanged.
+__device__ __forceinline__ void op_merge2(float &m, float &s, float m2, float s2)
+{
+    if (m2 == -CUDART_INF_F)
+        return;
+    const float nm = fmaxf(m, m2);
+    s = s * op_ex2((m - nm) * LOG2E) + s2 * op_ex2((m2 - nm) * LOG2E);
+    m = nm;
+}
+
+// Gradient of this warpgroup's half of the tile processed in order i, then
+// an arrive on that tile's TMEM-empty barrier in the leader CTA.
+__device__ __forceinline__ void op_grad_release(const GemmParams &p, const OpWork &w, int h, int i,
+                                                const float (&cmi)[OP_HCH], float m, float ls, uint32_t tlane,
+                                                int row0, int lab, uint8_t *stg, uint32_t tempty_bar)
+{
+    const int t = w.swap ? w.ntile - 1 - i : i;
+    const int col0 = (w.nb0 + t) * BN + h * OP_HALF;
+    float scale[OP_HCH];
+#pragma unroll
+    for (int c = 0; c < OP_HCH; ++c)
+        scale[c] = op_ex2(((cmi[c] - m) - ls) * LOG2E);
+    if (col0 < p.N)
+        op_half_grad(p, tlane + static_cast<uint32_t>(t * BN), row0, col0, lab, scale, stg);
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        mbar_arrive_cluster(mapa_shared(tempty_bar, 0u));
+}
+
 // Bounded wait until *flag >= target (acquire).
 __device__ __noinline__ bool wait_flag64(const unsigned long long *flag, unsigned long long target,
                                          volatile int *abort_flag, const GemmParams &p, uint32_t peer_abort)
@@ -338,11 +370,14 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
     const uint32_t bar0 = base + OP_STAGES * OP_STAGE_BYTES;
     const uint32_t drain_bar = bar0 + 8u * (2 * OP_STAGES + 4);
     const uint32_t pub_bar = drain_bar + 8u;  // warpgroup 0 wrote the pair's merged partials
-    const uint32_t xch_bar = pub_bar + 8u;    // warpgroup 1 handed over its tile's statistics
+    const uint32_t xch_bar = pub_bar + 8u;    // warpgroup 1 handed over its half-tile statistics
+    const uint32_t mrg_bar = xch_bar + 8u;    // both warpgroups stored their half of the row merge
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *xch_mx = reinterpret_cast<float *>(gbase + OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8 + 16);
-    float *xch_se = xch_mx + BM;
+    float *xch_se = xch_mx + 2 * BM;  // [order i][row]
+    float *mrg_mx = xch_se + 2 * BM;  // [warpgroup][row]
+    float *mrg_se = mrg_mx + 2 * BM;
 #define FULL_BAR(s) (bar0 + 8u * (s))
 #define EMPTY_BAR(s) (bar0 + 8u * (OP_STAGES + (s)))
 #define TFULL_BAR(t) (bar0 + 8u * (2 * OP_STAGES + (t)))
@@ -361,11 +396,12 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(TFULL_BAR(t), 1);
-            mbar_init(TEMPTY_BAR(t), 2 * OP_EPI_WARPS);
+            mbar_init(TEMPTY_BAR(t), 4 * OP_EPI_WARPS);  // both warpgroups of both CTAs
         }
         mbar_init(drain_bar, 1);
         mbar_init(pub_bar, OP_EPI_WARPS);
         mbar_init(xch_bar, OP_EPI_WARPS);
+        mbar_init(mrg_bar, 2 * OP_EPI_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -476,72 +512,90 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (both CTAs)
-        // warpgroup t (warps 2..5: t = 0, warps 6..9: t = 1) owns tile t; warp
-        // w reads TMEM lanes 32 * (w % 4) .., one row per thread.
-        const int t = (warp - 2) >> 2;
+        // Both warpgroups work on every tile: warpgroup h (warps 2..5: h = 0,
+        // warps 6..9: h = 1) takes columns [128h, 128h + 128) of each tile;
+        // warp w reads TMEM lanes 32 * (w % 4) .., one row per thread.
+        const int h = (warp - 2) >> 2;
         const int q = warp & 3;
         uint8_t *stg = gbase + OP_STG_OFF + (warp - 2) * OP_STG_WARP_BYTES;
         const int rloc = q * 32 + lane;
-        uint32_t eph = 0;
-        uint32_t pub_phase = 0;
+        uint32_t eph_bits = 0;  // TFULL phase of tile t in bit t
+        uint32_t pub_phase = 0, xch_phase = 0, mrg_phase = 0;
         const unsigned long long epoch_hi = static_cast<unsigned long long>(p.epoch) << 32;
-        const uint32_t taddr = tmem_base + static_cast<uint32_t>(t * BN) + (static_cast<uint32_t>(q * 32) << 16);
-        uint32_t xch_phase = 0;
+        const uint32_t tlane =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * OP_HALF);
         OpWork w;
-        for (int r = 0; r < p.op_rounds && op_work(p, pair, r, w); ++r) {
+        bool alive = true;
+        for (int r = 0; alive && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
             const int row0 = w.mb * OP_M + static_cast<int>(rank) * BM + q * 32;  // lane 0's row
             const int row = row0 + lane;
             const bool row_ok = row < p.M;
-            const bool mine = t < w.ntile;  // the pair's last tile may be missing (odd tile count)
-            const int nb = w.nb0 + t;
             const int qi = pair % p.op_Q;
-            // 1. statistics of this warpgroup's tile for its 128 rows; the tile
-            //    is left in TMEM as e = exp(z - tile max) for the gradient
             const int lab = row_ok ? p.labels[row] : -1;
-            float mx = -CUDART_INF_F, se = 0.f;
-            float cm[OP_CHUNKS];
-            if (mine) {
-                const bool got = wait_bar(TFULL_BAR(t), eph, abort_flag, p, ERR_EPI, peer_abort);
+            // 1. statistics of this half of each tile, in the order the MMAs
+            //    finish them (order i = 0, 1; tile t_i); the half is left in
+            //    TMEM as e = exp(z - running max) for the gradient
+            float tm[2] = {-CUDART_INF_F, -CUDART_INF_F}, ts[2] = {0.f, 0.f};
+            float cm[2][OP_HCH];
+#pragma unroll 1
+            for (int i = 0; i < w.ntile && alive; ++i) {
+                const int t = w.swap ? w.ntile - 1 - i : i;
+                const bool got = wait_bar(TFULL_BAR(t), (eph_bits >> t) & 1u, abort_flag, p, ERR_EPI, peer_abort);
+                alive = __all_sync(0xffffffffu, got);
+                if (alive) {
+                    eph_bits ^= 1u << t;
+                    tc_fence_after();
+                    const int col0 = (w.nb0 + t) * BN + h * OP_HALF;
+                    float zl = 0.f, cmt[OP_HCH], tmt = -CUDART_INF_F, tst = 0.f;
+                    bool have = false;
+                    if (col0 + OP_HALF <= p.N)
+                        op_half_stats<true>(p, tlane + static_cast<uint32_t>(t * BN), col0, lab, cmt, tmt, tst, zl,
+                                            have);
+                    else if (col0 < p.N)
+                        op_half_stats<false>(p, tlane + static_cast<uint32_t>(t * BN), col0, lab, cmt, tmt, tst, zl,
+                                             have);
+                    if (row_ok && have && lab < p.N)
+                        p.label_logit[row] = zl;
+                    // keep the results in registers named by the order index
+#pragma unroll
+                    for (int c = 0; c < OP_HCH; ++c) {
+                        cm[0][c] = i == 0 ? cmt[c] : cm[0][c];
+                        cm[1][c] = i == 0 ? cm[1][c] : cmt[c];
+                    }
+                    tm[0] = i == 0 ? tmt : tm[0];
+                    tm[1] = i == 0 ? tm[1] : tmt;
+                    ts[0] = i == 0 ? tst : ts[0];
+                    ts[1] = i == 0 ? ts[1] : tst;
+                }
+            }
+            if (!alive)
+                break;
+            // 2. warpgroup 1 hands its half statistics to warpgroup 0, which
+            //    merges the pair's (tile, half) statistics per row, stores the
+            //    partial in slot [qi][row] and publishes the CTA's flag (the
+            //    mbarrier orders the lanes' stores before the one release)
+            if (h == 1) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    xch_mx[i * BM + rloc] = tm[i];
+                    xch_se[i * BM + rloc] = ts[i];
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(xch_bar);
+            } else {
+                const bool got = wait_bar(xch_bar, xch_phase, abort_flag, p, ERR_SK_SLOT, peer_abort);
                 if (!__all_sync(0xffffffffu, got))
                     break;
-                eph ^= 1u;
-                tc_fence_after();
-                float zl = 0.f;
-                bool have;
-                if ((nb + 1) * BN <= p.N)
-                    op_tile_stats<true>(p, taddr, nb, lab, cm, mx, se, zl, have);
-                else
-                    op_tile_stats<false>(p, taddr, nb, lab, cm, mx, se, zl, have);
-                if (row_ok && have && lab < p.N)
-                    p.label_logit[row] = zl;
-            }
-            // 2. warpgroup 1 hands its statistics to warpgroup 0, which merges
-            //    the pair's two tiles per row, stores the partial in slot
-            //    [row, qi] and publishes the CTA's flag for the group
-            if (t == 1) {
-                if (mine) {
-                    xch_mx[rloc] = mx;
-                    xch_se[rloc] = se;
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(xch_bar);
-                }
-            } else {
-                if (w.ntile == 2) {
-                    const bool got = wait_bar(xch_bar, xch_phase, abort_flag, p, ERR_SK_SLOT, peer_abort);
-                    if (!__all_sync(0xffffffffu, got))
-                        break;
-                    xch_phase ^= 1u;
-                    const float m1 = xch_mx[rloc], s1 = xch_se[rloc];
-                    const float nm = fmaxf(mx, m1);
-                    se = se * op_ex2((mx - nm) * LOG2E) + s1 * op_ex2((m1 - nm) * LOG2E);
-                    mx = nm;
-                }
+                xch_phase ^= 1u;
+                float mx = tm[0], se = ts[0];
+                op_merge2(mx, se, tm[1], ts[1]);
+                op_merge2(mx, se, xch_mx[rloc], xch_se[rloc]);
+                op_merge2(mx, se, xch_mx[BM + rloc], xch_se[BM + rloc]);
                 if (row_ok) {  // partial-major: slot [qi][row]
                     p.part_max[static_cast<size_t>(qi) * p.M + row] = mx;
                     p.part_sum[static_cast<size_t>(qi) * p.M + row] = se;
                 }
-                __threadfence();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(pub_bar);
@@ -553,9 +607,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                 pub_phase ^= 1u;
             }
             // 3. wait for the group's pairs (same CTA rank holds the same rows);
-            //    the lanes poll the flags in parallel.  A warpgroup without a
-            //    tile waits too: the flags include its own pair's, so it cannot
-            //    arrive on the publish barrier for the next round early.
+            //    the lanes poll the flags in parallel
             bool got = true;
             {
                 const int first = (pair / p.op_Q) * p.op_Q;
@@ -566,27 +618,39 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             if (!__all_sync(0xffffffffu, got))
                 break;
             __syncwarp();
-            if (!mine)
-                continue;
-            // 4. merge the row's op_Q pair partials
+            // 4. merge the row's op_Q pair partials: warpgroup h takes half of
+            //    them, the two halves are exchanged through shared memory
             float m = -CUDART_INF_F, s = 0.f;
-            if (row_ok)
-                merge_row_partials(p.part_max + row, p.part_sum + row, static_cast<size_t>(p.M), p.op_Q, m, s);
-            const float ls = logf(s);
-            if (row_ok && nb == 0) {
-                const int lab = p.labels[row];
-                p.loss[row] = (lab >= 0 && lab < p.N) ? (m - __ldcg(p.label_logit + row)) + ls : CUDART_NAN_F;
+            {
+                const int qh = (p.op_Q + 1) >> 1;
+                const int j0 = h * qh;
+                const int n = min(p.op_Q, j0 + qh) - j0;
+                if (row_ok && n > 0)
+                    merge_row_partials(p.part_max + static_cast<size_t>(j0) * p.M + row,
+                                       p.part_sum + static_cast<size_t>(j0) * p.M + row, static_cast<size_t>(p.M), n,
+                                       m, s);
+                mrg_mx[h * BM + rloc] = m;
+                mrg_se[h * BM + rloc] = s;
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(mrg_bar);
+                const bool gm = wait_bar(mrg_bar, mrg_phase, abort_flag, p, ERR_SK_SLOT, peer_abort);
+                if (!__all_sync(0xffffffffu, gm))
+                    break;
+                mrg_phase ^= 1u;
+                op_merge2(m, s, mrg_mx[(1 - h) * BM + rloc], mrg_se[(1 - h) * BM + rloc]);
             }
-            // 5. gradient of this tile straight from TMEM, then free the accumulator
-            float scale[OP_CHUNKS];
-#pragma unroll
-            for (int c = 0; c < OP_CHUNKS; ++c)
-                scale[c] = op_ex2(((cm[c] - m) - ls) * LOG2E);
-            op_tile_grad(p, taddr, row0, nb, lab, scale, stg);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_cluster(mapa_shared(TEMPTY_BAR(t), 0u));
+            const float ls = logf(s);
+            if (row_ok && h == 0 && qi == 0) {
+                const int lb = p.labels[row];
+                p.loss[row] = (lb >= 0 && lb < p.N) ? (m - __ldcg(p.label_logit + row)) + ls : CUDART_NAN_F;
+            }
+            // 5. gradient straight from TMEM, the tile the next round's MMAs
+            //    need first (this round's last) first; each tile's accumulator
+            //    is released as soon as both warpgroups of both CTAs are done
+            if (w.ntile == 2)
+                op_grad_release(p, w, h, 1, cm[1], m, ls, tlane, row0, lab, stg, TEMPTY_BAR(w.swap ? 0 : 1));
+            op_grad_release(p, w, h, 0, cm[0], m, ls, tlane, row0, lab, stg, TEMPTY_BAR(w.swap ? w.ntile - 1 : 0));
         }
     }
 #undef FULL_BAR
