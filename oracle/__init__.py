@@ -64,6 +64,7 @@ def _load():
             "oracle_set_num_threads": [ctypes.c_int],
             "oracle_fp8_cast_dual": [P, I64, I64, ctypes.c_float, P, P],
             "oracle_rope_cos_sin": [P, P, I64, I64, P, P],
+            "oracle_gemm_layout": [P, ctypes.c_int, P, ctypes.c_int, I64, I64, I64, P, I64, P],
         }
         for name, argtypes in sig.items():
             fn = getattr(lib, name)
@@ -159,6 +160,28 @@ def gemm_nn(x, wt) -> np.ndarray:
     assert K == K2
     out = np.empty((M, N), dtype=np.float64)
     _load().oracle_gemm_nn(_p(x), _p(wt), M, N, K, _p(out))
+    return out
+
+
+def gemm_layout(x, x_mn: bool, w, w_mn: bool, rows=None) -> np.ndarray:
+    """out[m,n] = sum_k X(m,k) W(n,k) in fp64 with X stored [M,K] (x_mn False)
+    or [K,M] (x_mn True) and W stored [N,K] (w_mn False) or [K,N] (w_mn True);
+    `rows` restricts the result to those rows m."""
+    x, w = _bits(x), _bits(w)
+    if x_mn:
+        K, M = x.shape
+    else:
+        M, K = x.shape
+    if w_mn:
+        K2, N = w.shape
+    else:
+        N, K2 = w.shape
+    assert K == K2
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    R = M if r is None else r.shape[0]
+    out = np.empty((R, N), dtype=np.float64)
+    _load().oracle_gemm_layout(_p(x), int(bool(x_mn)), _p(w), int(bool(w_mn)), M, N, K, _p(r),
+                               0 if r is None else R, _p(out))
     return out
 
 

@@ -137,6 +137,35 @@ void oracle_gemm_nn(const uint16_t *x, const uint16_t *wt, int64_t M, int64_t N,
 }
 
 /*
+ * The contraction with either operand in either stored layout [P1, Feature:
+ * the transposed weight folded into the GEMM; P4, the matmul scheduler's
+ * canonicalisation of operand layouts to one (M, N, K) contraction]:
+ *   out[m,n] = sum_k X(m,k) * W(n,k)
+ *   X(m,k) = x[m*K + k] (x_mn == 0: X stored [M,K]) or x[k*M + m] (x_mn == 1: stored [K,M])
+ *   W(n,k) = w[n*K + k] (w_mn == 0: W stored [N,K]) or w[k*N + n] (w_mn == 1: stored [K,N])
+ * fp64, k summed in order.  `rows` (may be NULL) restricts it to R listed
+ * rows m: out is then [R, N].
+ */
+void oracle_gemm_layout(const uint16_t *x, int x_mn, const uint16_t *w, int w_mn, int64_t M, int64_t N,
+                        int64_t K, const int64_t *rows, int64_t R, double *out)
+{
+    const int64_t nrows = rows ? R : M;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t m = rows ? rows[r] : r;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const uint16_t xv = x_mn ? x[k * M + m] : x[m * K + k];
+                const uint16_t wv = w_mn ? w[k * N + n] : w[n * K + k];
+                acc += bf16_to_f64(xv) * bf16_to_f64(wv);
+            }
+            out[r * N + n] = acc;
+        }
+    }
+}
+
+/*
  * Row-wise cross-entropy over logits z [M,N] (fp64) [P4, fusion example]:
  *   mx   = max_n z[m,n]                      ("allreduce log sum exp in N")
  *   e    = exp(z - mx),  sumexp = sum_n e

@@ -473,3 +473,65 @@ def test_rope_mutants_fail_pins():
 
     for m in (swapped, no_cat, reversed_freqs, no_freq, off_by_one, sin_negated):
         assert rope_pin_failures(m), m.__name__
+
+
+# ------------------------------------------------------- operand layouts
+# "Strength reduction: fold transpose into a subsequent GEMM call": the
+# product must not depend on which stored layout an operand arrives in.
+
+def layout_pin_failures(gemm_layout):
+    failed = []
+    x = _bf16((37, 72), 1.0, 21)
+    w = _bf16((45, 72), 1.0, 22)
+    ref = oracle.gemm_nt(x, w)                      # pinned on its own above
+    xt = oracle.transpose_bf16(x)                   # [K, M]
+    wt = oracle.transpose_bf16(w)                   # [K, N]
+    for x_mn, w_mn in ((False, False), (True, False), (False, True), (True, True)):
+        got = gemm_layout(xt if x_mn else x, x_mn, wt if w_mn else w, w_mn)
+        if got.shape != ref.shape or not np.array_equal(got, ref):
+            failed.append("transpose identity %d%d" % (x_mn, w_mn))
+    # one-hot rows of X stored M-major select columns of W stored N-major, exactly
+    K, M, N = 40, 16, 24
+    xo = np.zeros((K, M), dtype=np.float32)
+    for m in range(M):
+        xo[(3 * m) % K, m] = 1.0
+    xo = torch.from_numpy(xo).to(torch.bfloat16)
+    wn = _bf16((K, N), 1.0, 23)
+    got = gemm_layout(xo, True, wn, True)
+    want = np.stack([_f64(wn)[(3 * m) % K] for m in range(M)])
+    if not np.array_equal(got, want):
+        failed.append("one-hot")
+    # row subset equals the full rows
+    full = gemm_layout(xt, True, w, False)
+    sub = gemm_layout(xt, True, w, False, rows=[0, 5, 36])
+    if not np.array_equal(sub, full[[0, 5, 36]]):
+        failed.append("rows")
+    return failed
+
+
+def test_gemm_layout_pins():
+    assert layout_pin_failures(oracle.gemm_layout) == []
+
+
+def test_gemm_layout_mutants_fail_pins():
+    def ignores_x_layout(x, x_mn, w, w_mn, rows=None):     # reads X as if K-major
+        xb = oracle._bits(x)
+        xb = xb.reshape(xb.shape[1], xb.shape[0]) if x_mn else xb
+        return oracle.gemm_layout(xb, False, w, w_mn, rows)
+
+    def transposed_w(x, x_mn, w, w_mn, rows=None):          # flips W's layout flag
+        wb = oracle._bits(w)
+        return oracle.gemm_layout(x, x_mn, wb.reshape(wb.shape[1], wb.shape[0]), not w_mn, rows)
+
+    def dropped_last_k(x, x_mn, w, w_mn, rows=None):
+        out = oracle.gemm_layout(x, x_mn, w, w_mn, rows)
+        xb, wb = oracle._bits(x), oracle._bits(w)
+        xl = oracle.bf16_bits_to_f64(xb[-1] if x_mn else xb[:, -1])
+        wl = oracle.bf16_bits_to_f64(wb[-1] if w_mn else wb[:, -1])
+        if rows is not None:
+            xl = xl[list(rows)]
+        return out - np.outer(xl, wl)
+
+    for m in (ignores_x_layout, transposed_w, dropped_last_k):
+        assert layout_pin_failures(m), m.__name__
+
