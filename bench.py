@@ -357,6 +357,31 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
                       "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes}
         del ad, bd, out
     torch.cuda.empty_cache()
+    # other operand layouts at the headline shape: W stored [K,N] (the trace's
+    # transposed copy, read as is), X stored [K,M], both
+    if "layouts" in want:
+        wl = synthetic.WORKLOADS["nt_projection"]
+        inp = synthetic.make_workload("nt_projection")
+        x = inp["x"].reshape(wl.M, wl.K)
+        w = inp["w"]
+        flops = 2.0 * wl.M * wl.N * wl.K
+        out = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+        for label, x_mn, w_mn in (("layout_nn", False, True), ("layout_tn", True, False), ("layout_tt", True, True)):
+            xs = (x.t().contiguous() if x_mn else x).to("cuda")
+            ws = (w.t().contiguous() if w_mn else w).to("cuda")
+
+            def step():
+                lf.gemm_layout(xs, ws, x_mn=x_mn, w_mn=w_mn, out=out, stream=stream)
+            times = timer.run(step, max(steps, 10), 3)
+            ms = statistics.median(times)
+            res[label] = {"M": wl.M, "N": wl.N, "K": wl.K, "x_stored": "[K,M]" if x_mn else "[M,K]",
+                          "w_stored": "[K,N]" if w_mn else "[N,K]", "ms": round(ms, 5),
+                          "tflops": round(flops / ms / 1e9, 1),
+                          "pct_of_peak": round(100 * flops / ms / 1e9 / peaks["bf16_tflops"], 1),
+                          "peak_kind": "bf16 burst (%s)" % peaks["source"]}
+            del xs, ws
+        del out, inp
+        torch.cuda.empty_cache()
     # RoPE segment (K=1 matmul + permute + cat + cos/sin -> bf16): the page's 4096
     # positions, and 2^20 positions (32 sequences of 32768) for bandwidth
     for label, (S, maxp) in ((("rope_page", (4096, 0)), ("rope_scaled", (1 << 20, 32768))) if "rope" in want else ()):
@@ -475,8 +500,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true", help="skip every secondary path")
-    ap.add_argument("--paths", default="xent,k1,rope,fp8",
-                    help="secondary paths to time after the headline (comma list of xent, k1, rope, fp8)")
+    ap.add_argument("--paths", default="xent,k1,layouts,rope,fp8",
+                    help="secondary paths to time after the headline (comma list of xent, k1, layouts, rope, fp8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     args = ap.parse_args(argv)

@@ -114,6 +114,41 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels,
 lf_status matmul_k1(const float *a, const float *b, float *out,
                     int64_t M, int64_t N, cudaStream_t stream);
 
+/* Stored layout of a GEMM operand (gemm_layout). */
+typedef enum {
+    LF_K_MAJOR = 0,  /* K contiguous: X stored [M,K], W stored [N,K] */
+    LF_MN_MAJOR = 1  /* M (resp. N) contiguous: X stored [K,M], W stored [K,N] */
+} lf_layout;
+
+/*
+ * gemm_layout -- out = X . W^T with either operand in either stored layout,
+ * no operand ever transposed in memory.
+ *
+ * Source: "Strength reduction: fold transpose into a subsequent GEMM call"
+ * (lightning-thunder issue 1252), Feature and the remark that one of the
+ * transposed layouts is served by the GEMM directly; "Allow reductions in
+ * matmul epilogues" (NVIDIA/Fuser issue 2213), whose matmul scheduler maps
+ * any operand layout onto one canonical (M, N, K) contraction.  Here the
+ * tensor core reads an MN-major operand from shared memory as readily as a
+ * K-major one, so all four combinations are one kernel, one launch.
+ *
+ *   x : bf16, device, 16-byte aligned; LF_K_MAJOR: [M,K] row-major
+ *       (X[m,k] = x[m*K + k]); LF_MN_MAJOR: [K,M] row-major (X[m,k] = x[k*M + m],
+ *       i.e. the storage of X^T, or of an [M,K] tensor with strides (1, M)).
+ *   w : bf16, device, 16-byte aligned; LF_K_MAJOR: [N,K] (W[n,k] = w[n*K + k],
+ *       the gemm_nt case); LF_MN_MAJOR: [K,N] (W[n,k] = w[k*N + n], the plain
+ *       x @ w of a [K,N] weight).
+ *   out: bf16 [M,N] row-major, out[m,n] = bf16_rn(sum_k X[m,k] * W[n,k]),
+ *       fp32 accumulation (tolerance as gemm_nt).
+ *   Row pitches must be multiples of 16 bytes: K % 8 == 0 for a K-major
+ *   operand (K > 1), M % 8 == 0 for an MN-major X, N % 8 == 0 always.
+ *   K = 1 is the broadcast product of gemm_nt (either layout is a vector).
+ *   An invalid layout value returns LF_ERR_SHAPE; other errors as gemm_nt.
+ *   Both K-major is exactly gemm_nt.
+ */
+lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, void *out,
+                      int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
 /*
  * rope_cos_sin -- the RoPE segment around the K=1 matmul, in one kernel.
  *

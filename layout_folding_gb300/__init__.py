@@ -11,6 +11,8 @@ Entry points (same names as the C ABI):
   matmul_k1(a, b, out=None)                     -> out = a * b     (fp32, K=1)
   fp8_cast_dual(x, scale)                       -> (out e4m3 [M,K], out_t e4m3 [M,K] column-major)
   rope_cos_sin(inv_freq, positions)             -> (cos bf16 [S,2H], sin bf16 [S,2H])
+  gemm_layout(x, w, x_mn, w_mn)                 -> out = X . W^T, X/W stored K-major or MN-major
+  matmul(a, b)                                  -> a @ b for contiguous or transposed-view operands
 """
 from __future__ import annotations
 
@@ -59,6 +61,8 @@ def lib():
         L.fp8_cast_dual.restype = I32
         L.rope_cos_sin.argtypes = [P, P, P, P, I64, I64, P]
         L.rope_cos_sin.restype = I32
+        L.gemm_layout.argtypes = [P, I32, P, I32, P, I64, I64, I64, P]
+        L.gemm_layout.restype = I32
         L.lf_status_string.argtypes = [I32]
         L.lf_status_string.restype = ctypes.c_char_p
         L.lf_check_device_error.argtypes = [P]
@@ -218,6 +222,50 @@ def rope_cos_sin(inv_freq, positions, cos_out=None, sin_out=None, want_sin=True,
                               None if sin_out is None else sin_out.data_ptr(), H, S, _stream(stream)),
            "rope_cos_sin")
     return cos_out, sin_out
+
+
+LF_K_MAJOR, LF_MN_MAJOR = 0, 1
+
+
+def gemm_layout(x, w, x_mn=False, w_mn=False, out=None, stream=None):
+    """out[m, n] = sum_k X[m, k] W[n, k] (bf16 out, fp32 accumulation) with
+    x stored [M, K] (x_mn False) or [K, M] (x_mn True) and w stored [N, K]
+    (w_mn False) or [K, N] (w_mn True); x and w contiguous bf16."""
+    import torch
+    _require(x, torch.bfloat16, "x")
+    _require(w, torch.bfloat16, "w")
+    if x.dim() != 2 or w.dim() != 2:
+        raise ValueError("x and w must be 2-D")
+    K, M = x.shape if x_mn else (x.shape[1], x.shape[0])
+    Kw, N = w.shape if w_mn else (w.shape[1], w.shape[0])
+    if K != Kw:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, Kw))
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _require(out, torch.bfloat16, "out")
+    if out.numel() != M * N:
+        raise ValueError("out must be [M, N]")
+    _check(lib().gemm_layout(x.data_ptr(), LF_MN_MAJOR if x_mn else LF_K_MAJOR, w.data_ptr(),
+                             LF_MN_MAJOR if w_mn else LF_K_MAJOR, out.data_ptr(), M, N, K, _stream(stream)),
+           "gemm_layout")
+    return out
+
+
+def matmul(a, b, out=None, stream=None):
+    """a @ b for 2-D bf16 a [M, K] and b [K, N], each either contiguous or the
+    transpose of a contiguous tensor (a.t(), b.t() views): the transpose is
+    folded into the GEMM's operand layout, never materialised."""
+    def storage(t):
+        if t.is_contiguous():
+            return t, False
+        if t.t().is_contiguous():
+            return t.t(), True
+        raise ValueError("operand must be contiguous or a transposed contiguous tensor")
+    if a.dim() != 2 or b.dim() != 2:
+        raise ValueError("a and b must be 2-D")
+    xa, a_t = storage(a)      # a_t: a is a transposed view -> X stored [K, M]
+    bb, b_t = storage(b)      # b_t: b is a transposed view of a [N, K] tensor -> W K-major
+    return gemm_layout(xa, bb, x_mn=a_t, w_mn=not b_t, out=out, stream=stream)
 
 
 def check_device_error(stream=None):

@@ -181,9 +181,26 @@ bool make_tmap(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, uint32_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor stored [K, rows] (rows contiguous: an MN-major operand),
+// box = 64 rows x 64 K, 128-byte swizzle; out-of-range elements read as zero.
+bool make_tmap_mn(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(rows) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(lf::BK)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Everything one GEMM launch needs: variant, tensor maps, parameters, grid.
 struct GemmPlan {
     bool pair = false;
+    int layout = 0;  // bit 0: X stored [K,M]; bit 1: W stored [K,N] (pair kernel only)
     DeviceState *dev = nullptr;
     CUtensorMap ta, tb;
     lf::GemmParams p;
@@ -191,13 +208,20 @@ struct GemmPlan {
 };
 
 lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int64_t N, int64_t K,
-                    GemmPlan *g)
+                    GemmPlan *g, int layout = 0)
 {
     const int variant = g_variant.load();
     g->dev = d;
-    g->pair = d->pair_clusters > 0 && (variant >= 2 || (variant < 0 && M > lf::BM));
+    g->layout = layout;
+    // the MN-major operand paths exist in the pair kernel only
+    g->pair = d->pair_clusters > 0 && (layout != 0 || variant >= 2 || (variant < 0 && M > lf::BM));
+    if (layout != 0 && !g->pair)
+        return LF_ERR_LAUNCH;
     const int tile_m = g->pair ? 2 * lf::BM : lf::BM;
-    if (!make_tmap(&g->ta, x, M, K, lf::BM) || !make_tmap(&g->tb, w, N, K, g->pair ? lf::BN / 2 : lf::BN))
+    const bool ok_a = (layout & 1) ? make_tmap_mn(&g->ta, x, M, K) : make_tmap(&g->ta, x, M, K, lf::BM);
+    const bool ok_b =
+        (layout & 2) ? make_tmap_mn(&g->tb, w, N, K) : make_tmap(&g->tb, w, N, K, g->pair ? lf::BN / 2 : lf::BN);
+    if (!ok_a || !ok_b)
         return LF_ERR_LAUNCH;
     lf::GemmParams &p = g->p;
     std::memset(&p, 0, sizeof p);
@@ -251,7 +275,7 @@ cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
 {
     if (g.p.streamk)
         g.p.epoch = next_epoch(g.dev);  // each launch's flags are distinct from every earlier one
-    return g.pair ? lf::launch_gemm_nt_pair(epi, g.ta, g.tb, g.p, g.grid, stream)
+    return g.pair ? lf::launch_gemm_nt_pair(epi, g.layout, g.ta, g.tb, g.p, g.grid, stream)
                   : lf::launch_gemm_nt(epi, g.ta, g.tb, g.p, g.grid, stream);
 }
 
@@ -293,6 +317,34 @@ lf_status gemm_nt(const void *x, const void *w, void *out, int64_t M, int64_t N,
         return launched(lf::launch_matmul_k1_bf16(x, w, out, M, N, d->num_sms, stream), 1);
     GemmPlan g;
     if ((st = plan_gemm(d, x, w, M, N, K, &g)) != LF_OK)
+        return st;
+    g.p.out = out;
+    return launched(run_gemm(lf::EPI_STORE, g, stream), 1);
+}
+
+lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, void *out, int64_t M, int64_t N,
+                      int64_t K, cudaStream_t stream)
+{
+    if (!x || !w || !out)
+        return LF_ERR_NULL;
+    if ((x_layout != LF_K_MAJOR && x_layout != LF_MN_MAJOR) || (w_layout != LF_K_MAJOR && w_layout != LF_MN_MAJOR))
+        return LF_ERR_SHAPE;
+    lf_status st = check_gemm_shape(M, N, K);
+    if (st != LF_OK)
+        return st;
+    // row pitches must be multiples of 16 bytes: K for a K-major operand, M
+    // (resp. N) for an MN-major one; out's pitch is N
+    const bool x_mn = x_layout == LF_MN_MAJOR, w_mn = w_layout == LF_MN_MAJOR;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || N % 8 != 0 || (x_mn && M % 8 != 0) ||
+        (K != 1 && ((!x_mn && K % 8 != 0) || (!w_mn && K % 8 != 0))))
+        return LF_ERR_ALIGN;
+    DeviceState *d = nullptr;
+    if ((st = current_device(&d)) != LF_OK)
+        return st;
+    if (K == 1)  // a [M,1] / [1,M] operand is the same vector either way
+        return launched(lf::launch_matmul_k1_bf16(x, w, out, M, N, d->num_sms, stream), 1);
+    GemmPlan g;
+    if ((st = plan_gemm(d, x, w, M, N, K, &g, (x_mn ? 1 : 0) | (w_mn ? 2 : 0))) != LF_OK)
         return st;
     g.p.out = out;
     return launched(run_gemm(lf::EPI_STORE, g, stream), 1);

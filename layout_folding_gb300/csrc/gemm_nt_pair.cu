@@ -7,6 +7,11 @@
 // transposed copy.  "Allow reductions in matmul epilogues" (NVIDIA/Fuser issue
 // 2213): the cross-entropy epilogues run on the finished accumulator.
 //
+// Other operand layouts ("fold any transpose"): X stored [K,M] and/or W
+// stored [K,N] are read MN-major by the same MMAs -- the tensor core reads
+// either major order from shared memory, so no operand is ever transposed in
+// memory; only the TMA boxes and the shared-memory descriptors change.
+//
 // Why a pair: each CTA stages only its half of the tile's operands (128 rows
 // of X and 128 rows of W per 64-wide K slice = 32 KiB), yet the pair's MMA
 // computes a 256x256 product, so the bytes each SM must pull per FLOP drop by
@@ -44,7 +49,16 @@ constexpr int PAIR_THREADS = 192;
 constexpr int PAIR_EPI_WARPS = 4;
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 3;
 constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + PAIR_NUM_BARS * 8 + 16;
-constexpr uint32_t PAIR_IDESC = idesc_bf16_f32(PAIR_M, BN);
+// Operand layouts (LAYOUT bit 0: X stored [K,M], M-major; bit 1: W stored
+// [K,N], N-major).  An MN-major operand arrives as two 64 x 64 boxes per K
+// slice (64 rows each, the second 8 KiB after the first) and is read through
+// an MN-major descriptor; each K=16 step advances two 1024-byte atoms.
+constexpr uint32_t PAIR_MN_HALF = PAIR_A_BYTES / 2;  // = PAIR_B_BYTES / 2
+constexpr uint32_t PAIR_MN_KSTEP = 2 * 1024;
+// The layout variants allocate 8 KiB of unused shared memory past the ring, so
+// that every address the MMA's descriptors can reach lies inside the
+// allocation even for the last stage.
+constexpr int PAIR_SMEM_BYTES_MN = PAIR_SMEM_BYTES + 8192;
 constexpr uint64_t ABORT_SETTLE_NS = 100000;  // after an abort: let copies in flight land
 
 // A run of K blocks [kb0, kb1) of one output tile.
@@ -118,7 +132,7 @@ __device__ __forceinline__ int sk_contributors(const GemmParams &p, int pair, in
     return n;
 }
 
-template <int EPI>
+template <int EPI, int LAYOUT>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     k_gemm_nt_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p)
@@ -208,8 +222,20 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                             mbar_arrive_expect_tx(FULL_BAR(stage), 2 * PAIR_STAGE_BYTES);
                             ++armed[stage];
                         }
-                        tma_load_2d_pair(sA + stage * PAIR_A_BYTES, &tmA, kb * BK, arow, full_leader);
-                        tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tmB, kb * BK, brow, full_leader);
+                        if (LAYOUT & 1) {
+                            tma_load_2d_pair(sA + stage * PAIR_A_BYTES, &tmA, arow, kb * BK, full_leader);
+                            tma_load_2d_pair(sA + stage * PAIR_A_BYTES + PAIR_MN_HALF, &tmA, arow + 64, kb * BK,
+                                             full_leader);
+                        } else {
+                            tma_load_2d_pair(sA + stage * PAIR_A_BYTES, &tmA, kb * BK, arow, full_leader);
+                        }
+                        if (LAYOUT & 2) {
+                            tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tmB, brow, kb * BK, full_leader);
+                            tma_load_2d_pair(sB + stage * PAIR_B_BYTES + PAIR_MN_HALF, &tmB, brow + 64, kb * BK,
+                                             full_leader);
+                        } else {
+                            tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tmB, kb * BK, brow, full_leader);
+                        }
                     }
                     if (++stage == PAIR_STAGES) {
                         stage = 0;
@@ -243,11 +269,15 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                     tc_fence_after();
                     const uint32_t a0 = sA + stage * PAIR_A_BYTES;
                     const uint32_t b0 = sB + stage * PAIR_B_BYTES;
+                    constexpr uint32_t idesc = idesc_bf16_f32_major(PAIR_M, BN, (LAYOUT & 1) != 0, (LAYOUT & 2) != 0);
 #pragma unroll
-                    for (int k = 0; k < BK / PAIR_UMMA_K; ++k)
-                        umma_f16_pair(d_tmem, smem_desc_k128(a0 + k * PAIR_UMMA_K * 2),
-                                      smem_desc_k128(b0 + k * PAIR_UMMA_K * 2), PAIR_IDESC,
-                                      (kb != g.kb0 || k != 0) ? 1u : 0u);
+                    for (int k = 0; k < BK / PAIR_UMMA_K; ++k) {
+                        const uint64_t da = (LAYOUT & 1) ? smem_desc_mn128(a0 + k * PAIR_MN_KSTEP, PAIR_MN_HALF)
+                                                         : smem_desc_k128(a0 + k * PAIR_UMMA_K * 2);
+                        const uint64_t db = (LAYOUT & 2) ? smem_desc_mn128(b0 + k * PAIR_MN_KSTEP, PAIR_MN_HALF)
+                                                         : smem_desc_k128(b0 + k * PAIR_UMMA_K * 2);
+                        umma_f16_pair(d_tmem, da, db, idesc, (kb != g.kb0 || k != 0) ? 1u : 0u);
+                    }
                     umma_commit_pair_mc(EMPTY_BAR(stage), 0x3);  // both CTAs may refill this slot
                     if (++stage == PAIR_STAGES) {
                         stage = 0;
@@ -387,7 +417,7 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t s, cudaLaunchAttribute *at
 
 // The dynamic shared-memory opt-in is a per-device function attribute: set it
 // once per device and kernel instead of on every launch.
-template <int EPI>
+template <int EPI, int LAYOUT>
 cudaError_t set_smem_attr_once()
 {
     static std::atomic<unsigned long long> done{0};
@@ -398,22 +428,25 @@ cudaError_t set_smem_attr_once()
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load() & bit)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(k_gemm_nt_pair<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_BYTES);
+    e = cudaFuncSetAttribute(k_gemm_nt_pair<EPI, LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             LAYOUT ? PAIR_SMEM_BYTES_MN : PAIR_SMEM_BYTES);
     if (e == cudaSuccess)
         done.fetch_or(bit);
     return e;
 }
 
-template <int EPI>
+template <int EPI, int LAYOUT>
 cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid,
                           cudaStream_t s)
 {
-    cudaError_t e = set_smem_attr_once<EPI>();
+    cudaError_t e = set_smem_attr_once<EPI, LAYOUT>();
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pair_config(grid, s, attr);
-    return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI>, ta, tb, p);
+    if (LAYOUT)
+        cfg.dynamicSmemBytes = PAIR_SMEM_BYTES_MN;
+    return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI, LAYOUT>, ta, tb, p);
 }
 
 }  // namespace
@@ -423,7 +456,7 @@ int gemm_pair_smem_bytes() { return PAIR_SMEM_BYTES; }
 // Number of CTA pairs of the pair kernel that fit on the device at once.
 int gemm_pair_max_active_clusters()
 {
-    if (cudaFuncSetAttribute(k_gemm_nt_pair<EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_gemm_nt_pair<EPI_STORE, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              PAIR_SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -431,23 +464,37 @@ int gemm_pair_max_active_clusters()
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pair_config(2, 0, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_nt_pair<EPI_STORE>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_nt_pair<EPI_STORE, 0>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-cudaError_t launch_gemm_nt_pair(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
-                                int grid, cudaStream_t s)
+cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, const CUtensorMap &tb,
+                                const GemmParams &p, int grid, cudaStream_t s)
 {
+    if (layout != 0) {  // other operand layouts: plain store epilogue only
+        if (epi != EPI_STORE)
+            return cudaErrorInvalidValue;
+        switch (layout) {
+        case 1:
+            return launch_pair_t<EPI_STORE, 1>(ta, tb, p, grid, s);
+        case 2:
+            return launch_pair_t<EPI_STORE, 2>(ta, tb, p, grid, s);
+        case 3:
+            return launch_pair_t<EPI_STORE, 3>(ta, tb, p, grid, s);
+        default:
+            return cudaErrorInvalidValue;
+        }
+    }
     switch (epi) {
     case EPI_STORE:
-        return launch_pair_t<EPI_STORE>(ta, tb, p, grid, s);
+        return launch_pair_t<EPI_STORE, 0>(ta, tb, p, grid, s);
     case EPI_XENT_PARTIAL:
-        return launch_pair_t<EPI_XENT_PARTIAL>(ta, tb, p, grid, s);
+        return launch_pair_t<EPI_XENT_PARTIAL, 0>(ta, tb, p, grid, s);
     case EPI_XENT_GRAD:
-        return launch_pair_t<EPI_XENT_GRAD>(ta, tb, p, grid, s);
+        return launch_pair_t<EPI_XENT_GRAD, 0>(ta, tb, p, grid, s);
     default:
         return cudaErrorInvalidValue;
     }

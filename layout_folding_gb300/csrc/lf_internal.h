@@ -58,9 +58,12 @@ cudaError_t launch_gemm_nt(int epi, const CUtensorMap &ta, const CUtensorMap &tb
 int gemm_smem_bytes();
 
 // CTA-pair variant (cta_group::2, 256x256 tiles; p.num_m_blocks counts
-// 256-row blocks; X and W tensor maps both use 128-row boxes; grid even).
-cudaError_t launch_gemm_nt_pair(int epi, const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
-                                int grid, cudaStream_t s);
+// 256-row blocks; grid even).  layout bit 0: X stored [K,M] (tensor map over
+// [K rows, M columns], 64x64 boxes), else [M,K] (64-column x 128-row boxes);
+// bit 1: W stored [K,N] likewise, else [N,K].  Layouts other than 0 support
+// the EPI_STORE epilogue only.
+cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, const CUtensorMap &tb,
+                                const GemmParams &p, int grid, cudaStream_t s);
 int gemm_pair_smem_bytes();
 int gemm_pair_max_active_clusters();
 

@@ -282,6 +282,23 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile with the
+// 128-byte swizzle, laid out by TMA loads of 64 (MN) x 64 (K) boxes with
+// CU_TENSOR_MAP_SWIZZLE_128B: a 128-byte row holds 64 MN elements of one k,
+// 8 consecutive k rows form a 1024-byte swizzle atom, so atoms along K are
+// 1024 bytes apart (stride-dim offset) and the next 64 MN elements -- the
+// next box -- are `lbo` bytes away (leading-dim offset).
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t lbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, shape M x N.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
@@ -289,6 +306,12 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr)
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// The same with A and/or B read MN-major (bits 15 / 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(uint32_t M, uint32_t N, bool a_mn, bool b_mn)
+{
+    return idesc_bf16_f32(M, N) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
 }
 
 }  // namespace lf

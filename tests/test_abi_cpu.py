@@ -12,7 +12,7 @@ from layout_folding_gb300 import build as lfbuild
 
 EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
             "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
-            "fp8_cast_dual", "rope_cos_sin"}
+            "fp8_cast_dual", "rope_cos_sin", "gemm_layout"}
 
 
 @pytest.fixture(scope="module")
@@ -100,6 +100,18 @@ def test_rope_cos_sin_rejects_on_host(L):
     assert L.rope_cos_sin(P(A16), P(A16 + 4), P(A16), None, 64, 16, None) == 3
     assert L.rope_cos_sin(P(A16 + 1), P(A16), P(A16), None, 64, 16, None) == 3
     assert L.rope_cos_sin(P(A16), P(A16), P(A16), P(A16 + 1), 64, 16, None) == 3
+
+
+def test_gemm_layout_rejects_on_host(L):
+    L.gemm_layout.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P] + [ctypes.c_int64] * 3 + [P]
+    assert L.gemm_layout(None, 0, P(A16), 0, P(A16), 8, 8, 8, None) == 1
+    assert L.gemm_layout(P(A16), 2, P(A16), 0, P(A16), 8, 8, 8, None) == 2     # no such layout
+    assert L.gemm_layout(P(A16), 0, P(A16), -1, P(A16), 8, 8, 8, None) == 2
+    assert L.gemm_layout(P(A16), 1, P(A16), 0, P(A16), 12, 8, 8, None) == 3    # X [K,M] pitch M*2 not 16-aligned
+    assert L.gemm_layout(P(A16), 0, P(A16), 1, P(A16), 8, 8, 12, None) == 3    # X [M,K] pitch K*2 not 16-aligned
+    assert L.gemm_layout(P(A16), 1, P(A16), 1, P(A16), 8, 12, 8, None) == 3    # N % 8
+    assert L.gemm_layout(P(A16 + 8), 1, P(A16), 1, P(A16), 8, 8, 8, None) == 3
+    assert L.gemm_layout(P(A16), 1, P(A16), 1, P(A16), 0, 8, 8, None) == 2
 
 
 def test_matmul_k1_rejects_on_host(L):
