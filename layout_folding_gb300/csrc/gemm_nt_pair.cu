@@ -45,9 +45,10 @@ constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;    // 16 KiB: this CTA's 128 row
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_ACC_BUFS = 2;
 constexpr int PAIR_TMEM_COLS = PAIR_ACC_BUFS * BN;  // 512
-constexpr int PAIR_THREADS = 192;
+constexpr int PAIR_THREADS = 192;  // producer, MMA, 4 epilogue warps
 constexpr int PAIR_EPI_WARPS = 4;
-constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 3;
+constexpr int PAIR_SKC_CHUNKS = BN / 32;  // a contributor's partial arrives in 8 chunks of 32 columns
+constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2 + PAIR_SKC_CHUNKS;
 constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + PAIR_NUM_BARS * 8 + 16;
 // Operand layouts (LAYOUT bit 0: X stored [K,M], M-major; bit 1: W stored
 // [K,N], N-major).  An MN-major operand arrives as two 64 x 64 boxes per K
@@ -132,6 +133,39 @@ __device__ __forceinline__ int sk_contributors(const GemmParams &p, int pair, in
     return n;
 }
 
+// out = bf16_rn(acc + partials) for this thread's row of the tile.  When
+// contributor 0's slot is being copied into shared memory (pa.smem0 set),
+// chunk c first waits for its own copy (barrier skc0 + 8 * c/32).  Returns
+// false if such a wait gave up.
+__device__ __forceinline__ bool pair_store(const GemmParams &p, uint32_t taddr, int row, int nb, const PartialAdd &pa,
+                                           uint32_t skc0, volatile int *abort_flag, uint32_t peer_abort)
+{
+    const bool row_ok = row < p.M;
+    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(row) * p.N;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        if (pa.smem0) {
+            const bool got = wait_bar(skc0 + 8u * static_cast<uint32_t>(c / 32), 0u, abort_flag, p, ERR_SK_COPY,
+                                      peer_abort);
+            if (!__all_sync(0xffffffffu, got))
+                return false;
+        }
+        uint32_t v[32];
+        load_chunk(taddr, c, pa, v);
+        if (row_ok) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                f[i] = __uint_as_float(v[i]);
+            store_row32_bf16(orow + col, f, p.N - col);
+        }
+    }
+    return true;
+}
+
 template <int EPI, int LAYOUT>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     k_gemm_nt_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -145,8 +179,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const uint32_t sB = base + PAIR_STAGES * PAIR_A_BYTES;
     const uint32_t bar0 = base + PAIR_STAGES * PAIR_STAGE_BYTES;
     const uint32_t drain_bar = bar0 + 8u * (2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS);
-    const uint32_t skw_bar = drain_bar + 8u;  // the 4 epilogue warps finished writing a partial
-    const uint32_t skc_bar = skw_bar + 8u;    // a contributor's partial landed in shared memory
+    const uint32_t skw_bar = drain_bar + 8u;  // the epilogue warps finished writing a partial
+    const uint32_t skc_bar = skw_bar + 8u;    // chunk c of a contributor's partial landed: skc_bar + 8c
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 #define FULL_BAR(s) (bar0 + 8u * (s))
@@ -172,7 +206,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         }
         mbar_init(drain_bar, 1);
         mbar_init(skw_bar, PAIR_EPI_WARPS);
-        mbar_init(skc_bar, 1);
+        for (int c = 0; c < PAIR_SKC_CHUNKS; ++c)
+            mbar_init(skc_bar + 8u * c, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -298,6 +333,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (both CTAs)
+        // warp w reads TMEM lanes 32 * (w % 4) .., one row per thread
         const int q = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -306,13 +342,33 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         for (Seg g; it.next(g);) {
             const int mb = g.tile % p.num_m_blocks;
             const int nb = g.tile / p.num_m_blocks;
+            const int rloc = q * 32 + lane;
+            const int row = mb * PAIR_M + static_cast<int>(rank) * BM + rloc;
+            const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
+            PartialAdd pa = {nullptr, 0, 0, rloc};
+            const bool owner_split = g.kb0 == 0 && g.kb1 < p.num_k_blocks;
+            const int MB = p.num_m_blocks;
+            const int first = (pair / MB + 1) * MB + pair % MB;  // first contributor pair
+            if (owner_split) {
+                // The tile's first K blocks, the rest held by the next pairs:
+                // acquire their flags while this pair's MMAs still run.
+                const int n = sk_contributors(p, pair, num_pairs, g.tile);
+                bool got = true;
+                if (lane == 0)
+                    for (int e = 0; e < n && got; ++e)
+                        got = wait_flag(p.sk_flags + (first + e * MB) * 2 + rank, p.epoch, abort_flag, p,
+                                        peer_abort);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!got)
+                    break;
+                pa.slot = p.sk_partials + static_cast<size_t>(first * 2 + rank) * SK_SLOT_FLOATS;
+                pa.stride = static_cast<size_t>(MB) * 2 * SK_SLOT_FLOATS;
+                pa.count = n;
+            }
             const bool ok = wait_bar(TFULL_BAR(acc), acc_phase, abort_flag, p, ERR_EPI, peer_abort);
             if (!__all_sync(0xffffffffu, ok))
                 break;
             tc_fence_after();
-            const int rloc = q * 32 + lane;
-            const int row = mb * PAIR_M + static_cast<int>(rank) * BM + rloc;
-            const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
             if (g.kb0 != 0) {
                 // Not the tile's first K blocks: hand the partial sum to the
                 // pair that owns the tile's start.
@@ -328,45 +384,45 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 }
                 skw_phase ^= 1u;
             } else {
-                PartialAdd pa = {nullptr, 0, 0, rloc};
-                if (g.kb1 < p.num_k_blocks) {
-                    // The tile's first K blocks, the rest held by the next pairs:
-                    // wait for their partials, then finish the tile.
-                    const int n = sk_contributors(p, pair, num_pairs, g.tile);
-                    bool got = true;
-                    const int MB = p.num_m_blocks;
-                    const int first = (pair / MB + 1) * MB + pair % MB;  // first contributor pair
-                    if (lane == 0)
-                        for (int e = 0; e < n && got; ++e)
-                            got = wait_flag(p.sk_flags + (first + e * MB) * 2 + rank, p.epoch, abort_flag, p,
-                                            peer_abort);
-                    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-                    if (!got)
-                        break;
-                    pa.slot = p.sk_partials + static_cast<size_t>(first * 2 + rank) * SK_SLOT_FLOATS;
-                    pa.stride = static_cast<size_t>(MB) * 2 * SK_SLOT_FLOATS;
-                    pa.count = n;
-                    if (n > 0) {
-                        // This is the pair's last segment, so its MMAs are done and
-                        // the operand ring is idle: pull the first contributor's
-                        // 128 KiB slot into it with one bulk copy instead of eight
-                        // dependent L2 round trips during the epilogue.
-                        if (warp == 2 && lane == 0) {
-                            mbar_arrive_expect_tx(skc_bar, SK_SLOT_FLOATS * 4);
-                            bulk_load_g2s(sA, pa.slot, SK_SLOT_FLOATS * 4, skc_bar);
+                // chunks of 32 columns that lie inside the matrix: only those
+                // are copied, and each copy is waited for by the warps that
+                // read it (none is left in flight at exit)
+                const int nch = min(PAIR_SKC_CHUNKS, (p.N - nb * BN + 31) / 32);
+                if (owner_split && pa.count > 0) {
+                    // This is the pair's last segment, so its MMAs are done and
+                    // the operand ring is idle: pull the first contributor's
+                    // 128 KiB slot into it as 8 bulk copies of 32 columns, each
+                    // on its own barrier, so the epilogue starts on the first
+                    // chunk while the rest are in flight.
+                    if (warp == 2 && lane == 0) {
+#pragma unroll 1
+                        for (int c = 0; c < nch; ++c) {
+                            constexpr int CH = SK_SLOT_FLOATS / PAIR_SKC_CHUNKS;  // floats per chunk
+                            mbar_arrive_expect_tx(skc_bar + 8u * c, CH * 4);
+                            bulk_load_g2s(sA + static_cast<uint32_t>(c * CH * 4), pa.slot + static_cast<size_t>(c) * CH,
+                                          CH * 4, skc_bar + 8u * c);
                         }
-                        const bool landed = wait_bar(skc_bar, 0u, abort_flag, p, ERR_SK_COPY, peer_abort);
-                        if (!__all_sync(0xffffffffu, landed))
-                            break;
-                        pa.smem0 = reinterpret_cast<const float4 *>(gbase);
+                    }
+                    pa.smem0 = reinterpret_cast<const float4 *>(gbase);
+                }
+                bool done = true;
+                if (EPI == EPI_STORE)
+                    done = pair_store(p, taddr, row, nb, pa, skc_bar, abort_flag, peer_abort);
+                else {
+                    if (pa.smem0) {
+                        for (int c = 0; c < nch && done; ++c)
+                            done = wait_bar(skc_bar + 8u * c, 0u, abort_flag, p, ERR_SK_COPY, peer_abort);
+                        done = __all_sync(0xffffffffu, done);
+                    }
+                    if (done) {
+                        if (EPI == EPI_XENT_PARTIAL)
+                            epi_xent_partial(p, taddr, row, nb, pa);
+                        else
+                            epi_xent_grad(p, taddr, row, nb, pa);
                     }
                 }
-                if (EPI == EPI_STORE)
-                    epi_store(p, taddr, row, nb, pa);
-                else if (EPI == EPI_XENT_PARTIAL)
-                    epi_xent_partial(p, taddr, row, nb, pa);
-                else
-                    epi_xent_grad(p, taddr, row, nb, pa);
+                if (!done)
+                    break;
             }
             tc_fence_before();
             __syncwarp();
