@@ -32,7 +32,10 @@ __device__ __forceinline__ float scaled_clamped(float v, float scale)
     return v < -448.f ? -448.f : v;
 }
 
-// Two floats -> two E4M3 codes (x in the low byte), round to nearest even.
+// Two floats -> two E4M3 codes (x in the low byte), round to nearest even,
+// saturating: anything beyond +-448 (infinities included) becomes +-448 and a
+// NaN stays NaN -- exactly what the clamp to +-448 followed by the rounding
+// gives, so the vector kernel skips the separate clamp.
 __device__ __forceinline__ uint32_t e4m3x2(float a, float b)
 {
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
@@ -80,10 +83,10 @@ __global__ void __launch_bounds__(THREADS) k_fp8_cast_dual_v16(const __nv_bfloat
                 const uint32_t w[8] = {lo[j].x, lo[j].y, lo[j].z, lo[j].w, hi[j].x, hi[j].y, hi[j].z, hi[j].w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float a = scaled_clamped(__uint_as_float(w[2 * i] << 16), scale);
-                    const float b = scaled_clamped(__uint_as_float(w[2 * i] & 0xffff0000u), scale);
-                    const float cc = scaled_clamped(__uint_as_float(w[2 * i + 1] << 16), scale);
-                    const float d = scaled_clamped(__uint_as_float(w[2 * i + 1] & 0xffff0000u), scale);
+                    const float a = __uint_as_float(w[2 * i] << 16) * scale;
+                    const float b = __uint_as_float(w[2 * i] & 0xffff0000u) * scale;
+                    const float cc = __uint_as_float(w[2 * i + 1] << 16) * scale;
+                    const float d = __uint_as_float(w[2 * i + 1] & 0xffff0000u) * scale;
                     q[i] = e4m3x2(a, b) | (e4m3x2(cc, d) << 16);
                 }
                 *reinterpret_cast<uint4 *>(out + (m0 + j * T + r) * K + k) = make_uint4(q[0], q[1], q[2], q[3]);

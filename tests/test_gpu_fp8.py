@@ -42,7 +42,8 @@ def check_full(x_cpu, scale, **kw):
     return out, out_t
 
 
-@pytest.mark.parametrize("M,K", [(64, 64), (128, 4096), (48, 80), (16, 16), (80, 1040), (1040, 48)])
+@pytest.mark.parametrize("M,K", [(64, 64), (128, 4096), (48, 80), (16, 16), (80, 1040), (1040, 48), (4, 4),
+                                 (20, 36), (68, 132), (1028, 260)])
 def test_vector_path_tiles_and_ragged_tails(M, K):
     x = synthetic.bf16_normal((M, K), 1.0, 11)
     check_full(x, 10.0)
@@ -72,6 +73,25 @@ def test_unaligned_pointers_take_the_scalar_path():
     # nothing outside the two views was written
     assert int(raw[:3].count_nonzero()) == 0 and int(raw[3 + M * K:].count_nonzero()) == 0
     assert int(raw_t[:5].count_nonzero()) == 0 and int(raw_t[5 + M * K:].count_nonzero()) == 0
+
+
+def test_eight_byte_aligned_input():
+    M, K = 64, 128
+    big = synthetic.bf16_normal((M * K + 8,), 1.0, 18)
+    x_cpu = big[4:4 + M * K].view(M, K)          # 8-byte aligned, not 16
+    x = big.to(DEV)[4:4 + M * K].view(M, K)
+    s = torch.tensor([10.0], device=DEV)
+    raw = torch.zeros(M * K + 16, dtype=torch.uint8, device=DEV)
+    raw_t = torch.zeros(M * K + 16, dtype=torch.uint8, device=DEV)
+    out = raw[4:4 + M * K].view(M, K)
+    out_t = raw_t[8:8 + M * K].view(K, M)
+    lf.fp8_cast_dual(x, s, out=out, out_t=out_t)
+    torch.cuda.synchronize()
+    ref, ref_t = oracle.fp8_cast_dual(x_cpu, 10.0)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref)
+    np.testing.assert_array_equal(out_t.cpu().numpy(), ref_t)
+    assert int(raw[:4].count_nonzero()) == 0 and int(raw[4 + M * K:].count_nonzero()) == 0
+    assert int(raw_t[:8].count_nonzero()) == 0 and int(raw_t[8 + M * K:].count_nonzero()) == 0
 
 
 @pytest.mark.parametrize("scale", [1.0, 10.0, 2.0 ** -20, 1e30])
