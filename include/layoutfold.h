@@ -281,6 +281,15 @@ lf_status lf_device_query(int *num_sms, int *pair_clusters);
 void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant);
 
 /*
+ * N-tile width of the one-pass cross-entropy-with-gradient kernel, applied to
+ * later gemm_nt_xent calls with a gradient: 128, 160, 192, 224 or 256; any
+ * other value restores the automatic choice (the width that minimises
+ * rounds x width with one group of pairs resident).  A forced width whose
+ * group does not fit the resident pairs falls back to the two-pass path.
+ */
+void lf_set_onepass_tile(int width);
+
+/*
  * Test hooks (not for production use).  inject_stall = 1 makes the next
  * tensor-core GEMM launches skip the first operand load of CTA 0, so that
  * CTA's MMA wait never completes: the bounded wait then gives up after

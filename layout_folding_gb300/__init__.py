@@ -73,6 +73,8 @@ def lib():
         L.lf_device_query.restype = I32
         L.lf_set_tuning.argtypes = [I32, I32]
         L.lf_set_tuning.restype = None
+        L.lf_set_onepass_tile.argtypes = [I32]
+        L.lf_set_onepass_tile.restype = None
         L.lf_set_test_hooks.argtypes = [I32, ctypes.c_uint64]
         L.lf_set_test_hooks.restype = None
         _lib = L
@@ -286,8 +288,15 @@ def device_query():
 
 def set_tuning(l2_prefetch_kblocks: int = -1, gemm_variant: int = -1):
     """L2-prefetch distance in K blocks (-1 = default, off) and GEMM tile
-    variant (1 = single CTA, 2 = CTA pair, -1 = automatic)."""
+    variant (1 = single CTA, 2 = CTA pair, 3 = CTA pair + stream-K, -1 =
+    automatic)."""
     lib().lf_set_tuning(int(l2_prefetch_kblocks), int(gemm_variant))
+
+
+def set_onepass_tile(width: int = 0):
+    """N-tile width of the one-pass cross-entropy kernel (128..256, multiple
+    of 32); 0 = automatic."""
+    lib().lf_set_onepass_tile(int(width))
 
 
 def set_test_hooks(inject_stall: bool, wait_timeout_ns: int = 0):

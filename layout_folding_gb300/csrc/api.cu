@@ -35,6 +35,7 @@ std::atomic<int> g_inject{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_l2_prefetch{-1};  // -1: per-shape default
 std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA, 2 CTA-pair whole tiles, 3 CTA-pair stream-K
+std::atomic<int> g_op_tile{0};       // one-pass cross-entropy N-tile width; 0 = automatic
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -385,12 +386,38 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
     p.labels = labels;
     // With a gradient on CTA pairs: one pass, when a whole 256-row block of
     // tiles (two per pair) fits on the resident pairs -- no recompute GEMM and
-    // no combine kernel.
-    if (grad_or_null && g.pair && (p.num_n_blocks + 1) / 2 <= d->pair_clusters) {
+    // no combine kernel.  The N-tile width is the one (of 256, 224, ..., 128)
+    // that minimises rounds x width, i.e. the MMA time per call: at N = 32768
+    // on 76 pairs, 224 (74 pairs busy) beats 256 (64 busy) by 12.5 %.
+    int op_tile = 0;
+    long long best = 0;
+    const int forced = g_op_tile.load();
+    for (int wdt = 256; wdt >= 128 && grad_or_null && g.pair; wdt -= 32) {
+        if (forced && wdt != forced)
+            continue;
+        const int nt = static_cast<int>((N + wdt - 1) / wdt);
+        const int q = (nt + 1) / 2;
+        if (q > d->pair_clusters)
+            continue;
+        int k = d->pair_clusters / q;
+        if (k > p.num_m_blocks)
+            k = p.num_m_blocks;
+        const long long cost = static_cast<long long>((p.num_m_blocks + k - 1) / k) * wdt;
+        if (op_tile == 0 || cost < best) {
+            op_tile = wdt;
+            best = cost;
+        }
+    }
+    if (op_tile > 0) {
         if ((st = ensure_onepass_flags(d)) != LF_OK)
             return st;
+        CUtensorMap tb_op;  // W in boxes of op_tile / 2 rows (each CTA's half of a tile)
+        if (!make_tmap(&tb_op, w, N, K, static_cast<uint32_t>(op_tile / 2)))
+            return LF_ERR_LAUNCH;
         p.streamk = 0;
-        p.op_Q = (p.num_n_blocks + 1) / 2;
+        p.op_tile = op_tile;
+        p.op_ntiles = static_cast<int>((N + op_tile - 1) / op_tile);
+        p.op_Q = (p.op_ntiles + 1) / 2;
         p.op_k = d->pair_clusters / p.op_Q;
         if (p.op_k > p.num_m_blocks)
             p.op_k = p.num_m_blocks;
@@ -399,7 +426,7 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
         p.loss = loss;
         p.out = grad_or_null;
         p.epoch = next_epoch(d);
-        return launched(lf::launch_xent_onepass(g.ta, g.tb, p, 2 * p.op_k * p.op_Q, stream), 1);
+        return launched(lf::launch_xent_onepass(g.ta, tb_op, p, 2 * p.op_k * p.op_Q, stream), 1);
     }
     if ((st = launched(run_gemm(lf::EPI_XENT_PARTIAL, g, stream), 1)) != LF_OK)
         return st;
@@ -526,7 +553,12 @@ lf_status lf_device_query(int *num_sms, int *pair_clusters)
 void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant)
 {
     g_l2_prefetch.store(l2_prefetch_kblocks < 0 ? -1 : l2_prefetch_kblocks);
-    g_variant.store(gemm_variant == 1 || gemm_variant == 2 ? gemm_variant : -1);
+    g_variant.store(gemm_variant >= 1 && gemm_variant <= 3 ? gemm_variant : -1);
+}
+
+void lf_set_onepass_tile(int width)
+{
+    g_op_tile.store(width >= 128 && width <= 256 && width % 32 == 0 ? width : 0);
 }
 
 void lf_set_test_hooks(int inject_stall, uint64_t wait_timeout_ns)

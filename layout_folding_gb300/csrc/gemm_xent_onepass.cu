@@ -10,10 +10,11 @@
 // a row of tiles has to be resident at once so the result can be broadcast
 // back.  That is what this kernel does, one 256-row block of rows at a time.
 //
-// Schedule: CTA pairs (tcgen05 cta_group::2, M=256 x N=256 MMAs) form groups
-// of Q = ceil(N_tiles / 2) pairs; pair qi of a group owns N tiles 2qi and
-// 2qi+1 of the group's M block and keeps both 256-column accumulators in TMEM
-// (all 512 columns).  k = floor(pairs / Q) groups run side by side, so a round
+// Schedule: CTA pairs (tcgen05 cta_group::2, M=256 x N=op_tile MMAs, op_tile
+// 128..256 chosen by the host so that one group uses as many of the resident
+// pairs as possible) form groups of Q = ceil(N_tiles / 2) pairs; pair qi of a
+// group owns N tiles 2qi and 2qi+1 of the group's M block and keeps both
+// accumulators in TMEM (columns [0, op_tile) and [256, 256 + op_tile)).  k = floor(pairs / Q) groups run side by side, so a round
 // covers k M blocks; round r of group g is M block r*k + g.  Per round:
 //   1. mainloop of the pair's one or two tiles (same TMA/MMA machinery as the
 //      pair GEMM kernel);
@@ -52,9 +53,9 @@ constexpr int OP_M = 2 * BM;  // 256 rows per pair
 constexpr int OP_UMMA_K = 16;
 constexpr int OP_STAGES = 6;
 constexpr int OP_A_BYTES = BM * BK * 2;        // this CTA's 128 rows of X
-constexpr int OP_B_BYTES = (BN / 2) * BK * 2;  // this CTA's 128 rows of W
+constexpr int OP_B_BYTES = (BN / 2) * BK * 2;  // room for this CTA's op_tile / 2 (<= 128) rows of W
 constexpr int OP_STAGE_BYTES = OP_A_BYTES + OP_B_BYTES;
-constexpr int OP_TMEM_COLS = 2 * BN;  // tile A: columns [0, 256), tile B: [256, 512)
+constexpr int OP_TMEM_COLS = 2 * BN;  // tile 0: columns [0, op_tile), tile 1: [256, 256 + op_tile)
 constexpr int OP_THREADS = 320;     // producer, MMA, and one epilogue warpgroup per tile
 constexpr int OP_EPI_WARPS = 4;    // per warpgroup (= per tile)
 constexpr int OP_NUM_BARS = 2 * OP_STAGES + 2 + 2 + 4;  // ring, tfull[2], tempty[2], drain, publish, exchange, merge
@@ -65,7 +66,6 @@ constexpr int OP_STG_WARP_BYTES = 32 * 32 * 2;            // a warp's 32 rows x 
 constexpr int OP_STG_OFF =
     ((OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8 + 16 + OP_XCH_BYTES + 127) / 128) * 128;
 constexpr int OP_SMEM_BYTES = 1024 + OP_STG_OFF + 2 * OP_EPI_WARPS * OP_STG_WARP_BYTES;
-constexpr uint32_t OP_IDESC = idesc_bf16_f32(OP_M, BN);
 constexpr uint64_t OP_ABORT_SETTLE_NS = 100000;
 constexpr int ERR_OP_FLAG = 0x108;  // a group member never published its partials
 
@@ -82,8 +82,8 @@ __device__ __forceinline__ bool op_work(const GemmParams &p, int pair, int r, Op
     w.mb = r * p.op_k + grp;
     if (w.mb >= p.num_m_blocks)
         return false;
-    w.nb0 = 2 * qi;  // < num_n_blocks because op_Q = ceil(num_n_blocks / 2)
-    w.ntile = (w.nb0 + 1 < p.num_n_blocks) ? 2 : 1;
+    w.nb0 = 2 * qi;  // < op_ntiles because op_Q = ceil(op_ntiles / 2)
+    w.ntile = (w.nb0 + 1 < p.op_ntiles) ? 2 : 1;
     // Alternate the order of the two tiles every round: the W rows of the tile
     // processed last are what L2 still holds, so the next round starts there.
     w.swap = (r & 1) && w.ntile == 2;
@@ -200,8 +200,9 @@ __device__ __forceinline__ void op_regs_after_wait(uint32_t (&v)[32])
                    "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
 }
 
-// Statistics of this thread's row of one half tile (128 columns from col0)
-// in a single pass over TMEM
+// Statistics of this thread's row of one half tile (columns [col0, lim):
+// at most 128, fewer in the second half of a narrower tile or past N) in a
+// single pass over TMEM
 // ("Allow reductions in matmul epilogues", fusion example: row max, exp(z -
 // max) and its sum, the label logit).  Chunk c is taken relative to the
 // running max m_c (the max over chunks 0..c): e = exp(z - m_c) is written
@@ -209,10 +210,10 @@ __device__ __forceinline__ void op_regs_after_wait(uint32_t (&v)[32])
 // is read once.  Returns the tile's max and sum of exp(z - max); cm[c] = m_c,
 // from which the gradient rescales chunk c.  The next chunk's TMEM load is in
 // flight while the current one is processed; max and sum are tree reductions.
-// FULL: every column of the half is < N (all but a ragged last tile).
+// FULL: all 128 columns of the half are in [col0, lim).
 template <bool FULL>
-__device__ __forceinline__ void op_half_stats(const GemmParams &p, uint32_t taddr, int col0, int lab,
-                                              float (&cm)[OP_HCH], float &mx, float &se, float &zl, bool &have)
+__device__ __forceinline__ void op_half_stats(int lim, uint32_t taddr, int col0, int lab, float (&cm)[OP_HCH],
+                                              float &mx, float &se, float &zl, bool &have)
 {
     const int lab_local = lab - col0;
     mx = -CUDART_INF_F;
@@ -222,7 +223,7 @@ __device__ __forceinline__ void op_half_stats(const GemmParams &p, uint32_t tadd
     tmem_ld_32x32b_x32(taddr, v[0]);
 #pragma unroll
     for (int c = 0; c < OP_HCH; ++c) {
-        const int nvalid = FULL ? 32 * (OP_HCH - c) : p.N - (col0 + c * 32);  // <= 0 past the last column
+        const int nvalid = FULL ? 32 * (OP_HCH - c) : lim - (col0 + c * 32);  // <= 0 past the half's last column
         tmem_wait_ld();
         if (c + 1 < OP_HCH && nvalid > 32)
             tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>((c + 1) * 32), v[(c + 1) & 1]);
@@ -259,8 +260,8 @@ __device__ __forceinline__ void op_half_stats(const GemmParams &p, uint32_t tadd
 // stored 8 rows x 64 bytes per instruction instead of 32 rows x 16 bytes.
 // (Double-buffering these TMEM loads spilled registers: 168 is the limit at
 // 10 warps per CTA.)
-__device__ __forceinline__ void op_half_grad(const GemmParams &p, uint32_t taddr, int row0, int col0, int lab,
-                                             const float (&scale)[OP_HCH], uint8_t *stg)
+__device__ __forceinline__ void op_half_grad(const GemmParams &p, int lim, uint32_t taddr, int row0, int col0,
+                                             int lab, const float (&scale)[OP_HCH], uint8_t *stg)
 {
     const int lane = threadIdx.x & 31;
     const int lab_local = lab - col0;
@@ -268,7 +269,7 @@ __device__ __forceinline__ void op_half_grad(const GemmParams &p, uint32_t taddr
 #pragma unroll
     for (int c = 0; c < OP_HCH; ++c) {
         const int col = col0 + c * 32;
-        const int nvalid = p.N - col;  // warp-uniform
+        const int nvalid = lim - col;  // warp-uniform
         if (nvalid > 0) {
             uint32_t u[32];
             tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), u);
@@ -298,8 +299,8 @@ __device__ __forceinline__ void op_half_grad(const GemmParams &p, uint32_t taddr
                 const int pc = lane & 3;            // 8-column piece
                 const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((pc ^ ((r >> 1) & 3)) << 4));
                 const int grow = row0 + r;
-                const int gcol = col + pc * 8;  // N % 8 == 0: a piece is all in or all out
-                if (grow < p.M && gcol < p.N)
+                const int gcol = col + pc * 8;  // lim % 8 == 0: a piece is all in or all out
+                if (grow < p.M && gcol < lim)
                     *reinterpret_cast<uint4 *>(out + static_cast<size_t>(grow) * p.N + gcol) = val;
             }
             __syncwarp();
@@ -325,13 +326,14 @@ __device__ __forceinline__ void op_grad_release(const GemmParams &p, const OpWor
                                                 int row0, int lab, uint8_t *stg, uint32_t tempty_bar)
 {
     const int t = w.swap ? w.ntile - 1 - i : i;
-    const int col0 = (w.nb0 + t) * BN + h * OP_HALF;
+    const int col0 = (w.nb0 + t) * p.op_tile + h * OP_HALF;
+    const int lim = min(p.N, (w.nb0 + t) * p.op_tile + min(p.op_tile, (h + 1) * OP_HALF));
     float scale[OP_HCH];
 #pragma unroll
     for (int c = 0; c < OP_HCH; ++c)
         scale[c] = op_ex2(((cmi[c] - m) - ls) * LOG2E);
-    if (col0 < p.N)
-        op_half_grad(p, tlane + static_cast<uint32_t>(t * BN), row0, col0, lab, scale, stg);
+    if (col0 < lim)
+        op_half_grad(p, lim, tlane + static_cast<uint32_t>(t * BN), row0, col0, lab, scale, stg);
     tc_fence_before();
     __syncwarp();
     if ((threadIdx.x & 31) == 0)
@@ -430,12 +432,14 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             for (int s = 0; s < OP_STAGES; ++s)
                 armed[s] = 0;
             bool ok = true, first = true;
+            // both CTAs' A (128 rows) and B (op_tile / 2 rows) boxes of a K slice
+            const uint32_t stage_tx = 2u * (OP_A_BYTES + static_cast<uint32_t>(p.op_tile / 2) * BK * 2u);
             OpWork w;
             for (int r = 0; ok && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
                 const int arow = w.mb * OP_M + static_cast<int>(rank) * BM;
                 for (int i = 0; ok && i < w.ntile; ++i) {
                     const int t = w.swap ? w.ntile - 1 - i : i;
-                    const int brow = (w.nb0 + t) * BN + static_cast<int>(rank) * (BN / 2);
+                    const int brow = (w.nb0 + t) * p.op_tile + static_cast<int>(rank) * (p.op_tile / 2);
                     for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                         if (!wait_bar(EMPTY_BAR(stage), phase ^ 1u, abort_flag, p, ERR_PRODUCER, peer_abort)) {
                             ok = false;
@@ -446,7 +450,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                         first = false;
                         if (!skip) {
                             if (leader) {
-                                mbar_arrive_expect_tx(FULL_BAR(stage), 2 * OP_STAGE_BYTES);
+                                mbar_arrive_expect_tx(FULL_BAR(stage), stage_tx);
                                 ++armed[stage];
                             }
                             tma_load_2d_pair(sA + stage * OP_A_BYTES, &tmA, kb * BK, arow, full_leader);
@@ -471,6 +475,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t tph[2] = {0u, 0u};
+            const uint32_t idesc = idesc_bf16_f32(OP_M, static_cast<uint32_t>(p.op_tile));
             bool ok = true;
             OpWork w;
             for (int r = 0; ok && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
@@ -493,7 +498,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
 #pragma unroll
                         for (int k = 0; k < BK / OP_UMMA_K; ++k)
                             umma_f16_pair(d_tmem, smem_desc_k128(a0 + k * OP_UMMA_K * 2),
-                                          smem_desc_k128(b0 + k * OP_UMMA_K * 2), OP_IDESC, (kb | k) != 0 ? 1u : 0u);
+                                          smem_desc_k128(b0 + k * OP_UMMA_K * 2), idesc, (kb | k) != 0 ? 1u : 0u);
                         umma_commit_pair_mc(EMPTY_BAR(stage), 0x3);
                         if (++stage == OP_STAGES) {
                             stage = 0;
@@ -545,15 +550,17 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                 if (alive) {
                     eph_bits ^= 1u << t;
                     tc_fence_after();
-                    const int col0 = (w.nb0 + t) * BN + h * OP_HALF;
+                    const int col0 = (w.nb0 + t) * p.op_tile + h * OP_HALF;
+                    // this half's columns end at the tile's width or at N
+                    const int lim = min(p.N, (w.nb0 + t) * p.op_tile + min(p.op_tile, (h + 1) * OP_HALF));
                     float zl = 0.f, cmt[OP_HCH], tmt = -CUDART_INF_F, tst = 0.f;
                     bool have = false;
-                    if (col0 + OP_HALF <= p.N)
-                        op_half_stats<true>(p, tlane + static_cast<uint32_t>(t * BN), col0, lab, cmt, tmt, tst, zl,
+                    if (col0 + OP_HALF <= lim)
+                        op_half_stats<true>(lim, tlane + static_cast<uint32_t>(t * BN), col0, lab, cmt, tmt, tst, zl,
                                             have);
-                    else if (col0 < p.N)
-                        op_half_stats<false>(p, tlane + static_cast<uint32_t>(t * BN), col0, lab, cmt, tmt, tst, zl,
-                                             have);
+                    else if (col0 < lim)
+                        op_half_stats<false>(lim, tlane + static_cast<uint32_t>(t * BN), col0, lab, cmt, tmt, tst,
+                                             zl, have);
                     if (row_ok && have && lab < p.N)
                         p.label_logit[row] = zl;
                     // keep the results in registers named by the order index

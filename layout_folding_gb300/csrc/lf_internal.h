@@ -42,10 +42,11 @@ struct GemmParams {
     float *sk_partials;         // [2 * pairs][128 * 256] fp32 partial accumulators
     unsigned *sk_flags;         // [2 * pairs] = epoch once the slot is written
     // one-pass cross-entropy with gradient (pair kernel): groups of op_Q pairs
-    // each hold one 256-row M block (two 256-column tiles per pair) per round.
+    // each hold one 256-row M block (two op_tile-column tiles per pair) per round.
     float *loss;                      // [M]
     unsigned long long *round_flags;  // [2 * pairs]: (epoch << 32) | rounds published
     int op_Q, op_k, op_rounds;        // pairs per M block, M blocks per round, rounds
+    int op_tile, op_ntiles;           // N-tile width (128..256, multiple of 32) and ceil(N / op_tile)
 };
 
 // One stream-K partial slot: a CTA's 128 rows x 256 columns of fp32,

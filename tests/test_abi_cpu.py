@@ -12,7 +12,7 @@ from layout_folding_gb300 import build as lfbuild
 
 EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
             "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
-            "fp8_cast_dual", "rope_cos_sin", "gemm_layout"}
+            "fp8_cast_dual", "rope_cos_sin", "gemm_layout", "lf_set_onepass_tile"}
 
 
 @pytest.fixture(scope="module")

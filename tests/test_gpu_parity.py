@@ -294,3 +294,27 @@ def test_matmul_k1_shapes_bitexact(M, N, offset):
     out = lf.matmul_k1(a.to(DEV).reshape(M, 1), bd.reshape(1, N)).cpu()
     want = oracle.matmul_k1(a.numpy(), b.numpy()[offset:])
     assert np.array_equal(out.numpy().view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("width", [128, 160, 192, 224, 256])
+def test_xent_onepass_every_tile_width(width):
+    """The one-pass kernel at each N-tile width it can choose, on a shape whose
+    last tile is ragged in a different way for each (N = 1032: 136 columns at
+    224, 72 at 160, ...), every row against the oracle."""
+    M, N, K = 600, 1032, 264
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N, seed=11)
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    lf.set_onepass_tile(width)
+    try:
+        b0 = lf.launch_count()
+        loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        b1 = lf.launch_count()
+        lf.check_device_error()
+    finally:
+        lf.set_onepass_tile(0)
+    assert b1 - b0 == 1
+    rows = list(range(M))
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    assert_loss_close(f64(loss), rloss, "width %d" % width)
+    assert_grad_close(f64(grad), rgrad, "width %d" % width)
