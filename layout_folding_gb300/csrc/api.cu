@@ -386,9 +386,12 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
     p.labels = labels;
     // With a gradient on CTA pairs: one pass, when a whole 256-row block of
     // tiles (two per pair) fits on the resident pairs -- no recompute GEMM and
-    // no combine kernel.  The N-tile width is the one (of 256, 224, ..., 128)
-    // that minimises rounds x width, i.e. the MMA time per call: at N = 32768
-    // on 76 pairs, 224 (74 pairs busy) beats 256 (64 busy) by 12.5 %.
+    // no combine kernel.  N-tile width: 256, unless the whole problem takes a
+    // single round, where narrower tiles (more pairs, shorter MMA chains)
+    // shorten that round.  With several rounds narrower tiles measured slower
+    // even when they keep more pairs busy (4096 x 32768 x 4096: 1.011 ms at
+    // 256 with 64 pairs, 1.038 ms at 224 with 74): every pair re-reads its M
+    // block of X per tile, and the extra operand traffic outweighs the MMAs.
     int op_tile = 0;
     long long best = 0;
     const int forced = g_op_tile.load();
@@ -402,7 +405,10 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
         int k = d->pair_clusters / q;
         if (k > p.num_m_blocks)
             k = p.num_m_blocks;
-        const long long cost = static_cast<long long>((p.num_m_blocks + k - 1) / k) * wdt;
+        const int rounds = (p.num_m_blocks + k - 1) / k;
+        if (wdt < 256 && rounds > 1 && !forced)
+            continue;
+        const long long cost = static_cast<long long>(rounds) * wdt;
         if (op_tile == 0 || cost < best) {
             op_tile = wdt;
             best = cost;

@@ -10,9 +10,8 @@
 // a row of tiles has to be resident at once so the result can be broadcast
 // back.  That is what this kernel does, one 256-row block of rows at a time.
 //
-// Schedule: CTA pairs (tcgen05 cta_group::2, M=256 x N=op_tile MMAs, op_tile
-// 128..256 chosen by the host so that one group uses as many of the resident
-// pairs as possible) form groups of Q = ceil(N_tiles / 2) pairs; pair qi of a
+// Schedule: CTA pairs (tcgen05 cta_group::2, M=256 x N=op_tile MMAs; op_tile
+// is 256, or 128..224 for problems that fit one round of pairs) form groups of Q = ceil(N_tiles / 2) pairs; pair qi of a
 // group owns N tiles 2qi and 2qi+1 of the group's M block and keeps both
 // accumulators in TMEM (columns [0, op_tile) and [256, 256 + op_tile)).  k = floor(pairs / Q) groups run side by side, so a round
 // covers k M blocks; round r of group g is M block r*k + g.  Per round:
