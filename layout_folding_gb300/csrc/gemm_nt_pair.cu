@@ -49,7 +49,10 @@ constexpr int PAIR_THREADS = 192;  // producer, MMA, 4 epilogue warps
 constexpr int PAIR_EPI_WARPS = 4;
 constexpr int PAIR_SKC_CHUNKS = BN / 32;  // a contributor's partial arrives in 8 chunks of 32 columns
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2 + PAIR_SKC_CHUNKS;
-constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + PAIR_NUM_BARS * 8 + 16;
+// per epilogue warp: 32 rows x 32 bf16 columns of output staged for row-contiguous stores
+constexpr int PAIR_STG_WARP_BYTES = 32 * 32 * 2;
+constexpr int PAIR_STG_OFF = ((PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16 + 127) / 128) * 128;
+constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STG_OFF + PAIR_EPI_WARPS * PAIR_STG_WARP_BYTES;
 // Operand layouts (LAYOUT bit 0: X stored [K,M], M-major; bit 1: W stored
 // [K,N], N-major).  An MN-major operand arrives as two 64 x 64 boxes per K
 // slice (64 rows each, the second 8 KiB after the first) and is read through
@@ -133,15 +136,19 @@ __device__ __forceinline__ int sk_contributors(const GemmParams &p, int pair, in
     return n;
 }
 
-// out = bf16_rn(acc + partials) for this thread's row of the tile.  When
-// contributor 0's slot is being copied into shared memory (pa.smem0 set),
-// chunk c first waits for its own copy (barrier skc0 + 8 * c/32).  Returns
-// false if such a wait gave up.
-__device__ __forceinline__ bool pair_store(const GemmParams &p, uint32_t taddr, int row, int nb, const PartialAdd &pa,
-                                           uint32_t skc0, volatile int *abort_flag, uint32_t peer_abort)
+// out = bf16_rn(acc + partials) for the warp's 32 rows of the tile (thread
+// `lane` owns row row0 + lane).  When contributor 0's slot is being copied
+// into shared memory (pa.smem0 set), chunk c first waits for its own copy
+// (barrier skc0 + 8 * c/32).  Each 32-column chunk is staged in the warp's
+// 2 KiB of shared memory (16-byte pieces XOR-swizzled by row pair, so writes
+// and reads are conflict-free) and stored 8 rows x 64 bytes per instruction
+// instead of 32 rows x 16 bytes.  Returns false if a copy wait gave up.
+__device__ __forceinline__ bool pair_store(const GemmParams &p, uint32_t taddr, int row0, int nb, const PartialAdd &pa,
+                                           uint32_t skc0, uint8_t *stg, volatile int *abort_flag,
+                                           uint32_t peer_abort)
 {
-    const bool row_ok = row < p.M;
-    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(row) * p.N;
+    const int lane = threadIdx.x & 31;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
         const int col = nb * BN + c;
@@ -155,13 +162,25 @@ __device__ __forceinline__ bool pair_store(const GemmParams &p, uint32_t taddr, 
         }
         uint32_t v[32];
         load_chunk(taddr, c, pa, v);
-        if (row_ok) {
-            float f[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                f[i] = __uint_as_float(v[i]);
-            store_row32_bf16(orow + col, f, p.N - col);
+        for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(pack_bf16(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                           pack_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                           pack_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                           pack_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 8 * i + (lane >> 2);  // row of the warp's 32
+            const int pc = lane & 3;            // 8-column piece
+            const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((pc ^ ((r >> 1) & 3)) << 4));
+            const int grow = row0 + r;
+            const int gcol = col + pc * 8;  // N % 8 == 0: a piece is all in or all out
+            if (grow < p.M && gcol < p.N)
+                *reinterpret_cast<uint4 *>(out + static_cast<size_t>(grow) * p.N + gcol) = val;
         }
+        __syncwarp();
     }
     return true;
 }
@@ -407,7 +426,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 }
                 bool done = true;
                 if (EPI == EPI_STORE)
-                    done = pair_store(p, taddr, row, nb, pa, skc_bar, abort_flag, peer_abort);
+                    done = pair_store(p, taddr, row - lane, nb, pa, skc_bar,
+                                      gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES, abort_flag, peer_abort);
                 else {
                     if (pa.smem0) {
                         for (int c = 0; c < nch && done; ++c)
