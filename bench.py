@@ -329,7 +329,10 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
         lf.check_device_error(stream)
         ms = statistics.mean(times)
         flops = 2.0 * wl.M * wl.N * wl.K
-        executed = flops * (2 if want_grad else 1)
+        # the two-pass gradient (partials, combine, recompute) runs the GEMM
+        # twice; the one-pass kernel (one launch) runs it once
+        one_pass = want_grad and launches == steps
+        executed = flops * (2 if want_grad and not one_pass else 1)
         peak = peaks["bf16_tflops_sustained"]
         res[name] = {"M": wl.M, "N": wl.N, "K": wl.K, "grad": want_grad, "ms": round(ms, 4),
                      "tflops_algorithmic": round(flops / ms / 1e9, 1),
@@ -337,7 +340,25 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
                      "pct_of_peak_algorithmic": round(100 * flops / ms / 1e9 / peak, 1),
                      "pct_of_peak_executed": round(100 * executed / ms / 1e9 / peak, 1),
                      "peak": peak, "peak_kind": "bf16 sustained (%s)" % peaks["source"],
-                     "launches_per_step": launches / steps}
+                     "launches_per_step": launches / steps, "one_pass": bool(one_pass)}
+        if not want_grad:
+            # The unfused comparison of the loss-only fusion ("the IO saving"): this
+            # library's GEMM writing the bf16 logits to HBM, then PyTorch's
+            # cross-entropy reading them back.  A measured comparison, not a target.
+            logits = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+            lab64 = lab.long()
+
+            def unfused():
+                lf.gemm_nt(x, w, logits, stream=stream)
+                with torch.cuda.stream(stream):
+                    torch.nn.functional.cross_entropy(logits, lab64, reduction="none")
+            times = timer.run(unfused, steps, 3)
+            ms_u = statistics.mean(times)
+            res["xent_loss_unfused"] = {"M": wl.M, "N": wl.N, "K": wl.K, "ms": round(ms_u, 4),
+                                        "what": "gemm_nt to bf16 logits + torch cross_entropy(reduction='none')",
+                                        "logits_bytes": wl.M * wl.N * 2,
+                                        "fused_speedup": round(ms_u / ms, 3)}
+            del logits, lab64
         del x, w, lab, loss, grad, inp
         torch.cuda.empty_cache()
     # K=1: the page's [64,1]x[1,4096] (latency regime) and a scaled column count for bandwidth
