@@ -65,6 +65,7 @@ def _load():
             "oracle_fp8_cast_dual": [P, I64, I64, ctypes.c_float, P, P],
             "oracle_rope_cos_sin": [P, P, I64, I64, P, P],
             "oracle_gemm_layout": [P, ctypes.c_int, P, ctypes.c_int, I64, I64, I64, P, I64, P],
+            "oracle_gemm_batched": [P, ctypes.c_int, I64, I64, P, ctypes.c_int, I64, I64, I64, I64, I64, I64, P],
         }
         for name, argtypes in sig.items():
             fn = getattr(lib, name)
@@ -182,6 +183,21 @@ def gemm_layout(x, x_mn: bool, w, w_mn: bool, rows=None) -> np.ndarray:
     out = np.empty((R, N), dtype=np.float64)
     _load().oracle_gemm_layout(_p(x), int(bool(x_mn)), _p(w), int(bool(w_mn)), M, N, K, _p(r),
                                0 if r is None else R, _p(out))
+    return out
+
+
+def gemm_batched(x, x_mn: bool, ldx: int, sx: int, w, w_mn: bool, ldw: int, sw: int,
+                 batch: int, M: int, N: int, K: int) -> np.ndarray:
+    """out[b, m, n] = sum_k X_b(m, k) W_b(n, k) in fp64 over flat bf16 storage:
+    X_b(m, k) = x[b*sx + m*ldx + k] (x_mn False) or x[b*sx + k*ldx + m] (True),
+    W_b(n, k) = w[b*sw + n*ldw + k] (w_mn False) or w[b*sw + k*ldw + n] (True)."""
+    xb, wb = _bits(x).ravel(), _bits(w).ravel()
+    need_x = (batch - 1) * sx + ((K - 1) * ldx + M if x_mn else (M - 1) * ldx + K)
+    need_w = (batch - 1) * sw + ((K - 1) * ldw + N if w_mn else (N - 1) * ldw + K)
+    assert xb.size >= need_x and wb.size >= need_w, "storage too small for the views"
+    out = np.empty((batch, M, N), dtype=np.float64)
+    _load().oracle_gemm_batched(_p(np.ascontiguousarray(xb)), int(bool(x_mn)), ldx, sx,
+                                _p(np.ascontiguousarray(wb)), int(bool(w_mn)), ldw, sw, batch, M, N, K, _p(out))
     return out
 
 

@@ -166,6 +166,35 @@ void oracle_gemm_layout(const uint16_t *x, int x_mn, const uint16_t *w, int w_mn
 }
 
 /*
+ * The same contraction over a batch of strided views [P1: the projection's
+ * input is itself a view of a larger tensor; the matmul page's operands are
+ * batched and permuted views]: for b < batch,
+ *   out[b][m][n] = sum_k X_b(m,k) * W_b(n,k)
+ *   X_b(m,k) = x[b*sx + m*ldx + k] (x_mn == 0) or x[b*sx + k*ldx + m] (x_mn == 1)
+ *   W_b(n,k) = w[b*sw + n*ldw + k] (w_mn == 0) or w[b*sw + k*ldw + n] (w_mn == 1)
+ * (sw == 0: one W for every batch).  fp64, k in order; out is [batch, M, N].
+ */
+void oracle_gemm_batched(const uint16_t *x, int x_mn, int64_t ldx, int64_t sx, const uint16_t *w, int w_mn,
+                         int64_t ldw, int64_t sw, int64_t batch, int64_t M, int64_t N, int64_t K, double *out)
+{
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t m = 0; m < M; ++m) {
+            const uint16_t *xb = x + b * sx;
+            const uint16_t *wb = w + b * sw;
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    const uint16_t xv = x_mn ? xb[k * ldx + m] : xb[m * ldx + k];
+                    const uint16_t wv = w_mn ? wb[k * ldw + n] : wb[n * ldw + k];
+                    acc += bf16_to_f64(xv) * bf16_to_f64(wv);
+                }
+                out[(b * M + m) * N + n] = acc;
+            }
+        }
+}
+
+/*
  * Row-wise cross-entropy over logits z [M,N] (fp64) [P4, fusion example]:
  *   mx   = max_n z[m,n]                      ("allreduce log sum exp in N")
  *   e    = exp(z - mx),  sumexp = sum_n e

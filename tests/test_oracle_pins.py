@@ -535,3 +535,48 @@ def test_gemm_layout_mutants_fail_pins():
     for m in (ignores_x_layout, transposed_w, dropped_last_k):
         assert layout_pin_failures(m), m.__name__
 
+
+
+# ------------------------------------------------ batched, strided views
+
+def batched_pin_failures(gemm_batched):
+    failed = []
+    B, M, N, K = 3, 20, 24, 40
+    ldx, ldw = 56, 48                               # padded rows: views of wider tensors
+    xs = _bf16((B, M, ldx), 1.0, 41)
+    ws = _bf16((B, N, ldw), 1.0, 42)
+    got = gemm_batched(xs, False, ldx, M * ldx, ws, False, ldw, N * ldw, B, M, N, K)
+    for b in range(B):                              # each batch is the 2-D product of its slices
+        ref = oracle.gemm_nt(xs[b, :, :K].contiguous(), ws[b, :, :K].contiguous())
+        if not np.array_equal(got[b], ref):
+            failed.append("slice %d" % b)
+    # MN-major views: the transposed storage of the same operands
+    xt = torch.stack([xs[b, :, :K].t().contiguous() for b in range(B)])       # [B, K, M]
+    wt = torch.stack([ws[b, :, :K].t().contiguous() for b in range(B)])       # [B, K, N]
+    got_t = gemm_batched(xt, True, M, K * M, wt, True, N, K * N, B, M, N, K)
+    if not np.array_equal(got_t, got):
+        failed.append("layouts")
+    # one W for every batch (batch stride 0)
+    got_bc = gemm_batched(xs, False, ldx, M * ldx, ws[0], False, ldw, 0, B, M, N, K)
+    for b in range(B):
+        if not np.array_equal(got_bc[b], oracle.gemm_nt(xs[b, :, :K].contiguous(), ws[0, :, :K].contiguous())):
+            failed.append("broadcast %d" % b)
+    return failed
+
+
+def test_gemm_batched_pins():
+    assert batched_pin_failures(oracle.gemm_batched) == []
+
+
+def test_gemm_batched_mutants_fail_pins():
+    def ignores_ld(x, x_mn, ldx, sx, w, w_mn, ldw, sw, B, M, N, K):      # assumes dense rows
+        return oracle.gemm_batched(x, x_mn, K if not x_mn else M, sx, w, w_mn, ldw, sw, B, M, N, K)
+
+    def first_batch_only(x, x_mn, ldx, sx, w, w_mn, ldw, sw, B, M, N, K):
+        return oracle.gemm_batched(x, x_mn, ldx, 0, w, w_mn, ldw, sw, B, M, N, K)
+
+    def w_batch_ignored(x, x_mn, ldx, sx, w, w_mn, ldw, sw, B, M, N, K):
+        return oracle.gemm_batched(x, x_mn, ldx, sx, w, w_mn, ldw, 0, B, M, N, K)
+
+    for m in (ignores_ld, first_batch_only, w_batch_ignored):
+        assert batched_pin_failures(m), m.__name__
