@@ -150,6 +150,34 @@ lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, 
                       int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
+ * gemm_batched -- gemm_layout over a batch of strided views: for b < batch,
+ *   out_b[m,n] = bf16_rn(sum_k X_b[m,k] * W_b[n,k])
+ * where, with all offsets in elements,
+ *   X_b[m,k] = x[b*stride_x + m*ldx + k]    (LF_K_MAJOR)   or x[b*stride_x + k*ldx + m] (LF_MN_MAJOR)
+ *   W_b[n,k] = w[b*stride_w + n*ldw + k]    (LF_K_MAJOR)   or w[b*stride_w + k*ldw + n] (LF_MN_MAJOR)
+ *   out_b[m,n] = out[b*stride_o + m*ldo + n]
+ * stride_x = 0 (stride_w = 0) uses one X (one W) for every batch.
+ *
+ * Source: "Strength reduction: fold transpose into a subsequent GEMM call"
+ * (lightning-thunder issue 1252) -- the projection's input is a view of a
+ * larger tensor -- and the batched, permuted operands of the Mistral listing
+ * of "Feature request: Schedule a small matmul op as a reduction (or
+ * pointwise) op" (NVIDIA/Fuser issue 3646): slices, transposes and batch
+ * dimensions are all folded into the operand tensor maps (one launch, no copy).
+ *
+ *   Row pitches: ldx >= K (K-major X) or M (MN-major X); ldw >= K or N; ldo >= N.
+ *   ldx, ldw, ldo, stride_x, stride_w, stride_o and N multiples of 8 (16
+ *   bytes); x, w, out 16-byte aligned (else LF_ERR_ALIGN).  batch >= 1; for
+ *   batch > 1 the out matrices must not overlap (stride_o >= (M-1)*ldo + N),
+ *   else LF_ERR_SHAPE.  Inputs may overlap.  Accumulation and tolerance as
+ *   gemm_nt; other errors as gemm_layout.
+ */
+lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_x,
+                       const void *w, int w_layout, int64_t ldw, int64_t stride_w,
+                       void *out, int64_t ldo, int64_t stride_o,
+                       int64_t batch, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * rope_cos_sin -- the RoPE segment around the K=1 matmul, in one kernel.
  *
  * Source: "Feature request: Schedule a small matmul op as a reduction (or

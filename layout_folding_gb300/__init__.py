@@ -13,6 +13,7 @@ Entry points (same names as the C ABI):
   rope_cos_sin(inv_freq, positions)             -> (cos bf16 [S,2H], sin bf16 [S,2H])
   gemm_layout(x, w, x_mn, w_mn)                 -> out = X . W^T, X/W stored K-major or MN-major
   matmul(a, b)                                  -> a @ b for contiguous or transposed-view operands
+  gemm_batched(...) / bmm(a, b)                 -> batched a @ b over strided views (pitches, batch strides)
 """
 from __future__ import annotations
 
@@ -63,6 +64,8 @@ def lib():
         L.rope_cos_sin.restype = I32
         L.gemm_layout.argtypes = [P, I32, P, I32, P, I64, I64, I64, P]
         L.gemm_layout.restype = I32
+        L.gemm_batched.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I64, I64, I64, I64, I64, I64, P]
+        L.gemm_batched.restype = I32
         L.lf_status_string.argtypes = [I32]
         L.lf_status_string.restype = ctypes.c_char_p
         L.lf_check_device_error.argtypes = [P]
@@ -268,6 +271,67 @@ def matmul(a, b, out=None, stream=None):
     xa, a_t = storage(a)      # a_t: a is a transposed view -> X stored [K, M]
     bb, b_t = storage(b)      # b_t: b is a transposed view of a [N, K] tensor -> W K-major
     return gemm_layout(xa, bb, x_mn=a_t, w_mn=not b_t, out=out, stream=stream)
+
+
+def gemm_batched(x, x_mn, ldx, stride_x, w, w_mn, ldw, stride_w, out, ldo, stride_o, batch, M, N, K,
+                 stream=None):
+    """The raw batched entry point on bf16 CUDA tensors used as flat storage
+    (element offsets; see gemm_batched in include/layoutfold.h)."""
+    import torch
+    for t, name in ((x, "x"), (w, "w"), (out, "out")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError("%s must be a bf16 CUDA tensor" % name)
+    _check(lib().gemm_batched(x.data_ptr(), LF_MN_MAJOR if x_mn else LF_K_MAJOR, ldx, stride_x, w.data_ptr(),
+                              LF_MN_MAJOR if w_mn else LF_K_MAJOR, ldw, stride_w, out.data_ptr(), ldo, stride_o,
+                              batch, M, N, K, _stream(stream)), "gemm_batched")
+    return out
+
+
+def _strided_view(t, rows_are_k):
+    """(mn_major, ld) of the last two dims of t: unit column stride -> rows of
+    length t.shape[-1] with pitch stride(-2); unit row stride -> the transposed
+    storage with pitch stride(-1).  `rows_are_k`: the view's rows index K (the
+    [K, N] right operand), so a row-major view of it is the N-major W."""
+    s_r, s_c = t.stride(-2), t.stride(-1)
+    if s_c == 1:
+        return (rows_are_k, s_r)
+    if s_r == 1:
+        return (not rows_are_k, s_c)
+    raise ValueError("each matrix must have unit stride along one of its two dimensions")
+
+
+def bmm(a, b, out=None, stream=None):
+    """a @ b over batches of strided views: a [M, K] or [B, M, K], b [K, N] or
+    [B, K, N] (a 2-D operand is shared by every batch), bf16, each matrix with a
+    unit stride in one dimension (slices, transposes and batch strides are
+    folded into the kernel's tensor maps, never copied).  Returns [B, M, N]
+    (or [M, N] when both are 2-D)."""
+    import torch
+    if a.dim() not in (2, 3) or b.dim() not in (2, 3):
+        raise ValueError("a and b must be 2-D or 3-D")
+    M, K = a.shape[-2], a.shape[-1]
+    K2, N = b.shape[-2], b.shape[-1]
+    if K != K2:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    B = max(a.shape[0] if a.dim() == 3 else 1, b.shape[0] if b.dim() == 3 else 1)
+    for t in (a, b):
+        if t.dim() == 3 and t.shape[0] not in (1, B):
+            raise ValueError("batch sizes differ")
+    x_mn, ldx = _strided_view(a, rows_are_k=False)
+    w_mn, ldw = _strided_view(b, rows_are_k=True)
+    sx = a.stride(0) if a.dim() == 3 and a.shape[0] == B and B > 1 else 0
+    sw = b.stride(0) if b.dim() == 3 and b.shape[0] == B and B > 1 else 0
+    if out is None:
+        out = torch.empty(B, M, N, dtype=torch.bfloat16, device=a.device)
+    if out.dim() == 2:
+        out3 = out.unsqueeze(0)
+    else:
+        out3 = out
+    if tuple(out3.shape) != (B, M, N) or out3.stride(-1) != 1:
+        raise ValueError("out must be [B, M, N] with unit column stride")
+    gemm_batched(a, x_mn, ldx, sx, b, w_mn, ldw, sw, out3, out3.stride(-2), out3.stride(0) if B > 1 else 0,
+                 B, M, N, K, stream=stream)
+    return out3[0] if a.dim() == 2 and b.dim() == 2 and out.dim() == 3 else out
 
 
 def check_device_error(stream=None):

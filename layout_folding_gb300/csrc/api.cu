@@ -198,6 +198,31 @@ bool make_tmap_mn(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor: `batch` matrices `stride` elements apart, each `outer`
+// rows of `inner` contiguous elements with a row pitch of `ld` elements; box
+// = 64 inner x box_outer rows x 1 batch, 128-byte swizzle, zero fill.
+bool make_tmap3(CUtensorMap *m, const void *ptr, int64_t inner, int64_t outer, int64_t ld, int64_t batch,
+                int64_t stride, uint32_t box_outer)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
+                                static_cast<cuuint64_t>(batch)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(stride) * 2};
+    const cuuint32_t box[3] = {64, box_outer, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A batch of strided views (gemm_batched): row pitches and batch strides in
+// elements; sw == 0 means one W for every batch.
+struct BatchSpec {
+    int64_t batch, ldx, sx, ldw, sw, ldo, so;
+};
+
 // Everything one GEMM launch needs: variant, tensor maps, parameters, grid.
 struct GemmPlan {
     bool pair = false;
@@ -209,19 +234,35 @@ struct GemmPlan {
 };
 
 lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int64_t N, int64_t K,
-                    GemmPlan *g, int layout = 0)
+                    GemmPlan *g, int layout = 0, const BatchSpec *bs = nullptr)
 {
     const int variant = g_variant.load();
     g->dev = d;
+    if (bs)
+        layout |= 4;
     g->layout = layout;
     // the MN-major operand paths exist in the pair kernel only
     g->pair = d->pair_clusters > 0 && (layout != 0 || variant >= 2 || (variant < 0 && M > lf::BM));
     if (layout != 0 && !g->pair)
         return LF_ERR_LAUNCH;
     const int tile_m = g->pair ? 2 * lf::BM : lf::BM;
-    const bool ok_a = (layout & 1) ? make_tmap_mn(&g->ta, x, M, K) : make_tmap(&g->ta, x, M, K, lf::BM);
-    const bool ok_b =
-        (layout & 2) ? make_tmap_mn(&g->tb, w, N, K) : make_tmap(&g->tb, w, N, K, g->pair ? lf::BN / 2 : lf::BN);
+    bool ok_a, ok_b;
+    if (bs) {
+        // an operand with batch stride 0 (or a batch of 1) is one matrix: a map
+        // whose batch extent is 1, read at batch coordinate 0
+        const bool xb = bs->sx != 0 && bs->batch > 1, wbat = bs->sw != 0 && bs->batch > 1;
+        const int64_t sx = xb ? bs->sx : ((layout & 1) ? K * bs->ldx : M * bs->ldx);
+        const int64_t wb = wbat ? bs->batch : 1;
+        const int64_t sw = wbat ? bs->sw : ((layout & 2) ? K * bs->ldw : N * bs->ldw);
+        ok_a = (layout & 1) ? make_tmap3(&g->ta, x, M, K, bs->ldx, xb ? bs->batch : 1, sx, 64)
+                            : make_tmap3(&g->ta, x, K, M, bs->ldx, xb ? bs->batch : 1, sx, lf::BM);
+        ok_b = (layout & 2) ? make_tmap3(&g->tb, w, N, K, bs->ldw, wb, sw, 64)
+                            : make_tmap3(&g->tb, w, K, N, bs->ldw, wb, sw, lf::BN / 2);
+    } else {
+        ok_a = (layout & 1) ? make_tmap_mn(&g->ta, x, M, K) : make_tmap(&g->ta, x, M, K, lf::BM);
+        ok_b = (layout & 2) ? make_tmap_mn(&g->tb, w, N, K)
+                            : make_tmap(&g->tb, w, N, K, g->pair ? lf::BN / 2 : lf::BN);
+    }
     if (!ok_a || !ok_b)
         return LF_ERR_LAUNCH;
     lf::GemmParams &p = g->p;
@@ -232,7 +273,15 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
     p.num_m_blocks = static_cast<int>((M + tile_m - 1) / tile_m);
     p.num_n_blocks = static_cast<int>((N + lf::BN - 1) / lf::BN);
     p.num_k_blocks = static_cast<int>((K + lf::BK - 1) / lf::BK);
-    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    const int64_t batch = bs ? bs->batch : 1;
+    p.batch = static_cast<int>(batch);
+    p.x_batched = bs && bs->sx && batch > 1 ? 1 : 0;
+    p.w_batched = bs && bs->sw && batch > 1 ? 1 : 0;
+    p.ldo = bs ? bs->ldo : N;
+    p.stride_o = bs ? bs->so : 0;
+    if (static_cast<int64_t>(p.num_m_blocks) * p.num_n_blocks * batch > MAX_DIM)
+        return LF_ERR_SHAPE;
+    p.num_tiles = static_cast<int>(p.num_m_blocks * p.num_n_blocks * batch);
     p.err = d->err_word;
     p.timeout_ns = g_timeout_ns.load();
     p.inject = g_inject.load();
@@ -247,7 +296,7 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
         // Stream-K groups: G groups of MB pairs (one per M block), G <= V so
         // that no pair gets an empty share -- a tile's owner waits on every
         // later group's partial, so each must write one.
-        const long long V = static_cast<long long>(p.num_n_blocks) * p.num_k_blocks;
+        const long long V = static_cast<long long>(p.num_n_blocks) * batch * p.num_k_blocks;
         long long G = p.num_m_blocks <= P ? P / p.num_m_blocks : 0;
         if (G > V)
             G = V;
@@ -346,6 +395,37 @@ lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, 
         return launched(lf::launch_matmul_k1_bf16(x, w, out, M, N, d->num_sms, stream), 1);
     GemmPlan g;
     if ((st = plan_gemm(d, x, w, M, N, K, &g, (x_mn ? 1 : 0) | (w_mn ? 2 : 0))) != LF_OK)
+        return st;
+    g.p.out = out;
+    return launched(run_gemm(lf::EPI_STORE, g, stream), 1);
+}
+
+lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_x, const void *w, int w_layout,
+                       int64_t ldw, int64_t stride_w, void *out, int64_t ldo, int64_t stride_o, int64_t batch,
+                       int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    if (!x || !w || !out)
+        return LF_ERR_NULL;
+    if ((x_layout != LF_K_MAJOR && x_layout != LF_MN_MAJOR) || (w_layout != LF_K_MAJOR && w_layout != LF_MN_MAJOR))
+        return LF_ERR_SHAPE;
+    lf_status st = check_gemm_shape(M, N, K);
+    if (st != LF_OK)
+        return st;
+    const bool x_mn = x_layout == LF_MN_MAJOR, w_mn = w_layout == LF_MN_MAJOR;
+    // every view lies inside its row pitch; batches of out do not overlap
+    if (batch < 1 || batch > MAX_DIM || ldx < (x_mn ? M : K) || ldw < (w_mn ? N : K) || ldo < N ||
+        stride_x < 0 || stride_w < 0 || (batch > 1 && stride_o < (M - 1) * ldo + N))
+        return LF_ERR_SHAPE;
+    // TMA and the 16-byte stores: 16-byte bases, row pitches and batch strides
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || ldx % 8 || ldw % 8 || ldo % 8 || N % 8 ||
+        stride_x % 8 || stride_w % 8 || stride_o % 8)
+        return LF_ERR_ALIGN;
+    DeviceState *d = nullptr;
+    if ((st = current_device(&d)) != LF_OK)
+        return st;
+    const BatchSpec bs = {batch, ldx, stride_x, ldw, stride_w, ldo, stride_o};
+    GemmPlan g;
+    if ((st = plan_gemm(d, x, w, M, N, K, &g, (x_mn ? 1 : 0) | (w_mn ? 2 : 0), &bs)) != LF_OK)
         return st;
     g.p.out = out;
     return launched(run_gemm(lf::EPI_STORE, g, stream), 1);

@@ -54,7 +54,8 @@ constexpr int PAIR_STG_WARP_BYTES = 32 * 32 * 2;
 constexpr int PAIR_STG_OFF = ((PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16 + 127) / 128) * 128;
 constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STG_OFF + PAIR_EPI_WARPS * PAIR_STG_WARP_BYTES;
 // Operand layouts (LAYOUT bit 0: X stored [K,M], M-major; bit 1: W stored
-// [K,N], N-major).  An MN-major operand arrives as two 64 x 64 boxes per K
+// [K,N], N-major; bit 2: batched, 3-D tensor maps with the batch as their
+// outermost coordinate).  An MN-major operand arrives as two 64 x 64 boxes per K
 // slice (64 rows each, the second 8 KiB after the first) and is read through
 // an MN-major descriptor; each K=16 step advances two 1024-byte atoms.
 constexpr uint32_t PAIR_MN_HALF = PAIR_A_BYTES / 2;  // = PAIR_B_BYTES / 2
@@ -94,7 +95,7 @@ struct WorkIter {
         const int G = num_pairs / MB;
         const int g = pair / MB;
         m = pair % MB;
-        const long long V = static_cast<long long>(p.num_n_blocks) * KB;
+        const long long V = static_cast<long long>(p.num_n_blocks) * (p.batch > 1 ? p.batch : 1) * KB;
         v = V * g / G;
         v_end = V * (g + 1) / G;
     }
@@ -128,7 +129,7 @@ __device__ __forceinline__ int sk_contributors(const GemmParams &p, int pair, in
 {
     const int MB = p.num_m_blocks;
     const int G = num_pairs / MB;
-    const long long V = static_cast<long long>(p.num_n_blocks) * p.num_k_blocks;
+    const long long V = static_cast<long long>(p.num_n_blocks) * (p.batch > 1 ? p.batch : 1) * p.num_k_blocks;
     const long long tile_end = static_cast<long long>(tile / MB + 1) * p.num_k_blocks;
     int n = 0;
     for (int g = pair / MB + 1; g < G && V * g / G < tile_end; ++g)
@@ -137,18 +138,18 @@ __device__ __forceinline__ int sk_contributors(const GemmParams &p, int pair, in
 }
 
 // out = bf16_rn(acc + partials) for the warp's 32 rows of the tile (thread
-// `lane` owns row row0 + lane).  When contributor 0's slot is being copied
+// `lane` owns row row0 + lane; `out` is this batch's matrix, rows p.ldo
+// elements apart).  When contributor 0's slot is being copied
 // into shared memory (pa.smem0 set), chunk c first waits for its own copy
 // (barrier skc0 + 8 * c/32).  Each 32-column chunk is staged in the warp's
 // 2 KiB of shared memory (16-byte pieces XOR-swizzled by row pair, so writes
 // and reads are conflict-free) and stored 8 rows x 64 bytes per instruction
 // instead of 32 rows x 16 bytes.  Returns false if a copy wait gave up.
-__device__ __forceinline__ bool pair_store(const GemmParams &p, uint32_t taddr, int row0, int nb, const PartialAdd &pa,
-                                           uint32_t skc0, uint8_t *stg, volatile int *abort_flag,
-                                           uint32_t peer_abort)
+__device__ __forceinline__ bool pair_store(const GemmParams &p, __nv_bfloat16 *out, uint32_t taddr, int row0, int nb,
+                                           const PartialAdd &pa, uint32_t skc0, uint8_t *stg,
+                                           volatile int *abort_flag, uint32_t peer_abort)
 {
     const int lane = threadIdx.x & 31;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
         const int col = nb * BN + c;
@@ -178,7 +179,7 @@ __device__ __forceinline__ bool pair_store(const GemmParams &p, uint32_t taddr, 
             const int grow = row0 + r;
             const int gcol = col + pc * 8;  // N % 8 == 0: a piece is all in or all out
             if (grow < p.M && gcol < p.N)
-                *reinterpret_cast<uint4 *>(out + static_cast<size_t>(grow) * p.N + gcol) = val;
+                *reinterpret_cast<uint4 *>(out + static_cast<size_t>(grow) * p.ldo + gcol) = val;
         }
         __syncwarp();
     }
@@ -258,7 +259,11 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             WorkIter it(p, pair, num_pairs);
             for (Seg g; ok && it.next(g);) {
                 const int mb = g.tile % p.num_m_blocks;
-                const int nb = g.tile / p.num_m_blocks;
+                const int nbt = g.tile / p.num_m_blocks;  // batch-major N block
+                const int bz = nbt / p.num_n_blocks;       // batch (0 unless batched)
+                const int nb = nbt % p.num_n_blocks;
+                const int xz = p.x_batched ? bz : 0;
+                const int wz = p.w_batched ? bz : 0;
                 const int arow = mb * PAIR_M + static_cast<int>(rank) * BM;
                 const int brow = nb * BN + static_cast<int>(rank) * (BN / 2);
                 for (int kb = g.kb0; kb < g.kb1; ++kb) {
@@ -276,19 +281,33 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                             mbar_arrive_expect_tx(FULL_BAR(stage), 2 * PAIR_STAGE_BYTES);
                             ++armed[stage];
                         }
-                        if (LAYOUT & 1) {
-                            tma_load_2d_pair(sA + stage * PAIR_A_BYTES, &tmA, arow, kb * BK, full_leader);
-                            tma_load_2d_pair(sA + stage * PAIR_A_BYTES + PAIR_MN_HALF, &tmA, arow + 64, kb * BK,
-                                             full_leader);
+                        const uint32_t a_dst = sA + stage * PAIR_A_BYTES, b_dst = sB + stage * PAIR_B_BYTES;
+                        if (LAYOUT & 4) {  // batched: the batch is the maps' third coordinate
+                            if (LAYOUT & 1) {
+                                tma_load_3d_pair(a_dst, &tmA, arow, kb * BK, xz, full_leader);
+                                tma_load_3d_pair(a_dst + PAIR_MN_HALF, &tmA, arow + 64, kb * BK, xz, full_leader);
+                            } else {
+                                tma_load_3d_pair(a_dst, &tmA, kb * BK, arow, xz, full_leader);
+                            }
+                            if (LAYOUT & 2) {
+                                tma_load_3d_pair(b_dst, &tmB, brow, kb * BK, wz, full_leader);
+                                tma_load_3d_pair(b_dst + PAIR_MN_HALF, &tmB, brow + 64, kb * BK, wz, full_leader);
+                            } else {
+                                tma_load_3d_pair(b_dst, &tmB, kb * BK, brow, wz, full_leader);
+                            }
                         } else {
-                            tma_load_2d_pair(sA + stage * PAIR_A_BYTES, &tmA, kb * BK, arow, full_leader);
-                        }
-                        if (LAYOUT & 2) {
-                            tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tmB, brow, kb * BK, full_leader);
-                            tma_load_2d_pair(sB + stage * PAIR_B_BYTES + PAIR_MN_HALF, &tmB, brow + 64, kb * BK,
-                                             full_leader);
-                        } else {
-                            tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tmB, kb * BK, brow, full_leader);
+                            if (LAYOUT & 1) {
+                                tma_load_2d_pair(a_dst, &tmA, arow, kb * BK, full_leader);
+                                tma_load_2d_pair(a_dst + PAIR_MN_HALF, &tmA, arow + 64, kb * BK, full_leader);
+                            } else {
+                                tma_load_2d_pair(a_dst, &tmA, kb * BK, arow, full_leader);
+                            }
+                            if (LAYOUT & 2) {
+                                tma_load_2d_pair(b_dst, &tmB, brow, kb * BK, full_leader);
+                                tma_load_2d_pair(b_dst + PAIR_MN_HALF, &tmB, brow + 64, kb * BK, full_leader);
+                            } else {
+                                tma_load_2d_pair(b_dst, &tmB, kb * BK, brow, full_leader);
+                            }
                         }
                     }
                     if (++stage == PAIR_STAGES) {
@@ -360,7 +379,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         WorkIter it(p, pair, num_pairs);
         for (Seg g; it.next(g);) {
             const int mb = g.tile % p.num_m_blocks;
-            const int nb = g.tile / p.num_m_blocks;
+            const int nbt = g.tile / p.num_m_blocks;  // batch-major N block
+            const int nb = nbt % p.num_n_blocks;
+            const int bz = nbt / p.num_n_blocks;
             const int rloc = q * 32 + lane;
             const int row = mb * PAIR_M + static_cast<int>(rank) * BM + rloc;
             const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
@@ -426,7 +447,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 }
                 bool done = true;
                 if (EPI == EPI_STORE)
-                    done = pair_store(p, taddr, row - lane, nb, pa, skc_bar,
+                    done = pair_store(p, static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(bz) * p.stride_o, taddr,
+                                      row - lane, nb, pa, skc_bar,
                                       gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES, abort_flag, peer_abort);
                 else {
                     if (pa.smem0) {
@@ -560,6 +582,14 @@ cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, cons
             return launch_pair_t<EPI_STORE, 2>(ta, tb, p, grid, s);
         case 3:
             return launch_pair_t<EPI_STORE, 3>(ta, tb, p, grid, s);
+        case 4:
+            return launch_pair_t<EPI_STORE, 4>(ta, tb, p, grid, s);
+        case 5:
+            return launch_pair_t<EPI_STORE, 5>(ta, tb, p, grid, s);
+        case 6:
+            return launch_pair_t<EPI_STORE, 6>(ta, tb, p, grid, s);
+        case 7:
+            return launch_pair_t<EPI_STORE, 7>(ta, tb, p, grid, s);
         default:
             return cudaErrorInvalidValue;
         }

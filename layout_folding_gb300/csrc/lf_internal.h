@@ -47,6 +47,12 @@ struct GemmParams {
     unsigned long long *round_flags;  // [2 * pairs]: (epoch << 32) | rounds published
     int op_Q, op_k, op_rounds;        // pairs per M block, M blocks per round, rounds
     int op_tile, op_ntiles;           // N-tile width (128..256, multiple of 32) and ceil(N / op_tile)
+    // batches of strided views (pair kernel, plain store epilogue): tile
+    // index = (batch, N block, M block), M block fastest
+    int batch;                        // number of batches (0 or 1: not batched)
+    int x_batched, w_batched;         // 0: one X (resp. W) for every batch
+    long long ldo;                    // row pitch of out in elements (N when not strided)
+    long long stride_o;               // batch stride of out in elements
 };
 
 // One stream-K partial slot: a CTA's 128 rows x 256 columns of fp32,
@@ -61,8 +67,9 @@ int gemm_smem_bytes();
 // CTA-pair variant (cta_group::2, 256x256 tiles; p.num_m_blocks counts
 // 256-row blocks; grid even).  layout bit 0: X stored [K,M] (tensor map over
 // [K rows, M columns], 64x64 boxes), else [M,K] (64-column x 128-row boxes);
-// bit 1: W stored [K,N] likewise, else [N,K].  Layouts other than 0 support
-// the EPI_STORE epilogue only.
+// bit 1: W stored [K,N] likewise, else [N,K]; bit 2: batched (3-D tensor
+// maps, batch outermost; p.batch, p.w_batched, p.ldo, p.stride_o).  Layouts
+// other than 0 support the EPI_STORE epilogue only.
 cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, const CUtensorMap &tb,
                                 const GemmParams &p, int grid, cudaStream_t s);
 int gemm_pair_smem_bytes();

@@ -12,7 +12,7 @@ from layout_folding_gb300 import build as lfbuild
 
 EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
             "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
-            "fp8_cast_dual", "rope_cos_sin", "gemm_layout", "lf_set_onepass_tile"}
+            "fp8_cast_dual", "rope_cos_sin", "gemm_layout", "lf_set_onepass_tile", "gemm_batched"}
 
 
 @pytest.fixture(scope="module")
@@ -112,6 +112,27 @@ def test_gemm_layout_rejects_on_host(L):
     assert L.gemm_layout(P(A16), 1, P(A16), 1, P(A16), 8, 12, 8, None) == 3    # N % 8
     assert L.gemm_layout(P(A16 + 8), 1, P(A16), 1, P(A16), 8, 8, 8, None) == 3
     assert L.gemm_layout(P(A16), 1, P(A16), 1, P(A16), 0, 8, 8, None) == 2
+
+
+def test_gemm_batched_rejects_on_host(L):
+    I = ctypes.c_int64
+    L.gemm_batched.argtypes = [P, ctypes.c_int, I, I, P, ctypes.c_int, I, I, P, I, I, I, I, I, I, P]
+    ok = dict(x=P(A16), xl=0, ldx=64, sx=64 * 64, w=P(A16), wl=0, ldw=64, sw=64 * 64, o=P(A16), ldo=64, so=64 * 64,
+              b=2, M=64, N=64, K=64)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.gemm_batched(a["x"], a["xl"], a["ldx"], a["sx"], a["w"], a["wl"], a["ldw"], a["sw"], a["o"],
+                              a["ldo"], a["so"], a["b"], a["M"], a["N"], a["K"], None)
+    assert call(x=None) == 1
+    assert call(xl=2) == 2
+    assert call(b=0) == 2
+    assert call(ldx=32) == 2          # K-major X rows shorter than K
+    assert call(ldo=56) == 2          # out rows shorter than N
+    assert call(so=64) == 2           # overlapping out matrices
+    assert call(ldx=72 + 4) == 3      # pitch not a multiple of 8 elements
+    assert call(sx=64 * 64 + 4) == 3
+    assert call(o=P(A16 + 8)) == 3
 
 
 def test_matmul_k1_rejects_on_host(L):
