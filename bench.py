@@ -401,6 +401,27 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
                           "pct_of_peak": round(100 * flops / ms / 1e9 / peaks["bf16_tflops"], 1),
                           "peak_kind": "bf16 burst (%s)" % peaks["source"]}
             del xs, ws
+        # batched strided views: the same FLOPs as 4 batches of N/4 columns (one
+        # shared X, W sliced by a batch stride), and X read through a view with
+        # padded rows (row pitch 16384 instead of 13824)
+        xd, wd = x.to("cuda"), w.to("cuda")
+        B, Nb = 4, wl.N // 4
+        outb = torch.empty(B, wl.M, Nb, dtype=torch.bfloat16, device="cuda")
+        xpad = torch.zeros(wl.M, 16384, dtype=torch.bfloat16, device="cuda")
+        xpad[:, :wl.K] = xd
+        cases = (("batched_4x", lambda: lf.gemm_batched(xd, False, wl.K, 0, wd, False, wl.K, Nb * wl.K, outb, Nb,
+                                                         wl.M * Nb, B, wl.M, Nb, wl.K, stream=stream),
+                  "4 batches of [768 x 1280], X shared (stride 0), W batch stride 1280*13824"),
+                 ("strided_x", lambda: lf.bmm(xpad[:, :wl.K], wd.t(), out=out, stream=stream),
+                  "X a [768, 13824] view of [768, 16384] rows"))
+        for label, fn, what in cases:
+            times = timer.run(fn, max(steps, 10), 3)
+            ms = statistics.median(times)
+            res[label] = {"M": wl.M, "N": wl.N, "K": wl.K, "what": what, "ms": round(ms, 5),
+                          "tflops": round(flops / ms / 1e9, 1),
+                          "pct_of_peak": round(100 * flops / ms / 1e9 / peaks["bf16_tflops"], 1),
+                          "peak_kind": "bf16 burst (%s)" % peaks["source"]}
+        del xd, wd, outb, xpad
         del out, inp
         torch.cuda.empty_cache()
     # RoPE segment (K=1 matmul + permute + cat + cos/sin -> bf16): the page's 4096
