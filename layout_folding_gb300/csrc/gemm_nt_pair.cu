@@ -186,6 +186,59 @@ __device__ __forceinline__ bool pair_store(const GemmParams &p, __nv_bfloat16 *o
     return true;
 }
 
+// Gradient pass of the two-pass cross-entropy ("Allow reductions in matmul
+// epilogues", the softmax-minus-onehot output) for the warp's 32 rows:
+// grad = bf16_rn(exp(z - row_max - row_logsum) - [n == label]) with the
+// exponent as one FFMA (z * log2 e - (max + logsum) * log2 e) and ex2.approx,
+// staged and stored like pair_store.  Row statistics come from the combine
+// kernel; this thread owns row row0 + lane.
+__device__ __forceinline__ void pair_xent_grad(const GemmParams &p, uint32_t taddr, int row0, int nb,
+                                               const PartialAdd &pa, uint8_t *stg)
+{
+    const int lane = threadIdx.x & 31;
+    const int row = row0 + lane;
+    const bool row_ok = row < p.M;
+    const int lab = row_ok ? p.labels[row] : -1;
+    const float off = row_ok ? (p.row_max[row] + p.row_logsum[row]) * LOG2E : 0.f;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        uint32_t v[32];
+        load_chunk(taddr, c, pa, v);
+        const int li = lab - col;
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float g0 = ex2_approx(fmaf(__uint_as_float(v[2 * i]), LOG2E, -off));
+            float g1 = ex2_approx(fmaf(__uint_as_float(v[2 * i + 1]), LOG2E, -off));
+            if (2 * i == li)
+                g0 -= 1.f;
+            if (2 * i + 1 == li)
+                g1 -= 1.f;
+            pk[i] = pack_bf16(g0, g1);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 8 * i + (lane >> 2);
+            const int pc = lane & 3;
+            const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((pc ^ ((r >> 1) & 3)) << 4));
+            const int grow = row0 + r;
+            const int gcol = col + pc * 8;
+            if (grow < p.M && gcol < p.N)
+                *reinterpret_cast<uint4 *>(out + static_cast<size_t>(grow) * p.N + gcol) = val;
+        }
+        __syncwarp();
+    }
+}
+
 template <int EPI, int LAYOUT>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     k_gemm_nt_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -460,7 +513,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                         if (EPI == EPI_XENT_PARTIAL)
                             epi_xent_partial(p, taddr, row, nb, pa);
                         else
-                            epi_xent_grad(p, taddr, row, nb, pa);
+                            pair_xent_grad(p, taddr, row - lane, nb, pa,
+                                           gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES);
                     }
                 }
                 if (!done)

@@ -89,15 +89,6 @@ __device__ __forceinline__ bool op_work(const GemmParams &p, int pair, int r, Op
     return true;
 }
 
-// 2^x with the PTX approximation (relative error about 2^-22; results below
-// 2^-126 flush to zero, which no sum or gradient here can see).
-__device__ __forceinline__ float op_ex2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Tree max / sum of the first `n` (all when FULL) of 32 values held as bits.
 template <bool FULL>
 __device__ __forceinline__ float op_tree_max_bits(const uint32_t (&u)[32], int n)
@@ -178,10 +169,10 @@ __device__ __forceinline__ void merge_row_partials(const float *pm, const float 
         }
         const float nm = fmaxf(m, op_tree_max16(a));
         const float nml = nm * LOG2E;
-        s *= op_ex2((m - nm) * LOG2E);
+        s *= ex2_approx((m - nm) * LOG2E);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            b[i] *= op_ex2(fmaf(a[i], LOG2E, -nml));
+            b[i] *= ex2_approx(fmaf(a[i], LOG2E, -nml));
         s += op_tree_sum16(b);
         m = nm;
     }
@@ -242,8 +233,8 @@ __device__ __forceinline__ void op_half_stats(int lim, uint32_t taddr, int col0,
             const float mcl = m_c * LOG2E;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-                u[i] = __float_as_uint((FULL || i < nvalid) ? op_ex2(fmaf(__uint_as_float(u[i]), LOG2E, -mcl)) : 0.f);
-            se = se * op_ex2((mx - m_c) * LOG2E) + op_tree_sum_bits(u);
+                u[i] = __float_as_uint((FULL || i < nvalid) ? ex2_approx(fmaf(__uint_as_float(u[i]), LOG2E, -mcl)) : 0.f);
+            se = se * ex2_approx((mx - m_c) * LOG2E) + op_tree_sum_bits(u);
             mx = m_c;
             cm[c] = m_c;
             tmem_st_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), u);
@@ -314,7 +305,7 @@ __device__ __forceinline__ void op_merge2(float &m, float &s, float m2, float s2
     if (m2 == -CUDART_INF_F)
         return;
     const float nm = fmaxf(m, m2);
-    s = s * op_ex2((m - nm) * LOG2E) + s2 * op_ex2((m2 - nm) * LOG2E);
+    s = s * ex2_approx((m - nm) * LOG2E) + s2 * ex2_approx((m2 - nm) * LOG2E);
     m = nm;
 }
 
@@ -330,7 +321,7 @@ __device__ __forceinline__ void op_grad_release(const GemmParams &p, const OpWor
     float scale[OP_HCH];
 #pragma unroll
     for (int c = 0; c < OP_HCH; ++c)
-        scale[c] = op_ex2(((cmi[c] - m) - ls) * LOG2E);
+        scale[c] = ex2_approx(((cmi[c] - m) - ls) * LOG2E);
     if (col0 < lim)
         op_half_grad(p, lim, tlane + static_cast<uint32_t>(t * BN), row0, col0, lab, scale, stg);
     tc_fence_before();

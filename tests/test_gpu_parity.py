@@ -318,3 +318,31 @@ def test_xent_onepass_every_tile_width(width):
     _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
     assert_loss_close(f64(loss), rloss, "width %d" % width)
     assert_grad_close(f64(grad), rgrad, "width %d" % width)
+
+
+@pytest.mark.parametrize("variant", [2, 3])
+def test_xent_two_pass_gradient_on_pairs(variant):
+    """A vocabulary too wide for one pass (N = 40992: 161 tiles, more than two
+    per resident pair; the last tile 32 columns wide) takes the two-pass form
+    on CTA pairs: partials, combine, and the recompute pass writing the
+    gradient.  Sampled rows, every column, against the oracle."""
+    M, N, K = 512, 40992, 256
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N, seed=12)
+    lab[5] = N - 1
+    lab[6] = 0
+    lab[7] = 256 * 160                      # first column of the ragged last tile
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    lf.set_tuning(-1, variant)
+    try:
+        b0 = lf.launch_count()
+        loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        b1 = lf.launch_count()
+        lf.check_device_error()
+    finally:
+        lf.set_tuning(-1, -1)
+    assert b1 - b0 == 3                     # partials GEMM, combine, gradient GEMM
+    rows = sample_rows(M, k=12, seed=13, extra=(5, 6, 7))
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    assert_loss_close(f64(loss)[rows], rloss, "two-pass")
+    assert_grad_close(f64(grad)[rows], rgrad, "two-pass")

@@ -72,3 +72,34 @@ def test_stalled_wait_in_onepass_cross_entropy_times_out():
     _, rloss, _, _ = oracle.xent(x, w, lab.numpy(), want_grad=False)
     got = loss.double().cpu().numpy()
     assert np.max(np.abs(got - rloss) / np.abs(rloss)) <= 1e-3
+
+
+@pytest.mark.parametrize("kind", ["layout_tt", "batched"])
+def test_stalled_wait_times_out_in_layout_and_batched_variants(kind):
+    # the MN-major operand and batched (3-D tensor map) variants of the pair
+    # kernel share the bounded waits: same error, same clean unwind
+    torch.cuda.set_device(0)
+    M, N, K = 256, 1024, 512
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    xd, wd = x.to(DEV), w.to(DEV)
+    xt, wt = xd.t().contiguous(), wd.t().contiguous()
+
+    def call():
+        if kind == "layout_tt":
+            return lf.gemm_layout(xt, wt, x_mn=True, w_mn=True)
+        return lf.bmm(xd.view(2, M // 2, K), wd.t())
+
+    lf.check_device_error()
+    lf.set_test_hooks(True, 200_000_000)
+    try:
+        call()
+        with pytest.raises(lf.LayoutFoldError) as info:
+            lf.check_device_error()
+        assert info.value.status == 6
+    finally:
+        lf.set_test_hooks(False, 0)
+    out = call()
+    lf.check_device_error()
+    ref = oracle.gemm_nt(x, w)
+    got = out.reshape(M, N).float().cpu().double().numpy()
+    assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
