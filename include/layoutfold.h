@@ -144,7 +144,9 @@ typedef enum {
  *   operand (K > 1), M % 8 == 0 for an MN-major X, N % 8 == 0 always.
  *   K = 1 is the broadcast product of gemm_nt (either layout is a vector).
  *   An invalid layout value returns LF_ERR_SHAPE; other errors as gemm_nt.
- *   Both K-major is exactly gemm_nt.
+ *   Both K-major is exactly gemm_nt.  Like gemm_nt it may use the stream-K
+ *   split and its per-device workspace: such calls on one device must not
+ *   run concurrently on different streams.
  */
 lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, void *out,
                       int64_t M, int64_t N, int64_t K, cudaStream_t stream);
@@ -170,7 +172,7 @@ lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, 
  *   bytes); x, w, out 16-byte aligned (else LF_ERR_ALIGN).  batch >= 1; for
  *   batch > 1 the out matrices must not overlap (stride_o >= (M-1)*ldo + N),
  *   else LF_ERR_SHAPE.  Inputs may overlap.  Accumulation and tolerance as
- *   gemm_nt; other errors as gemm_layout.
+ *   gemm_nt; other errors, and the rule on concurrent calls, as gemm_layout.
  */
 lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_x,
                        const void *w, int w_layout, int64_t ldw, int64_t stride_w,
