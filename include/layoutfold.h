@@ -58,7 +58,9 @@ typedef enum {
  *         as "Feature request: Schedule a small matmul op as a reduction (or
  *         pointwise) op" (NVIDIA/Fuser issue 3646) proposes; N % 8 == 0 is still required.
  *   x, w, out must be 16-byte aligned.  out must not overlap x or w.
- * One kernel launch per call.  When the output has too few 256x256 tiles to
+ * One kernel launch per call.  A skinny X (M <= 128) with few output tiles is
+ * computed with the operands swapped (out^T = W . X^T on the tensor cores,
+ * stored transposed).  When the output has too few 256x256 tiles to
  * keep every SM busy, the launch splits the K loop across SMs (stream-K) and
  * uses a library-owned per-device workspace (about 20 MB, allocated on first
  * such call); calls on one device must then not run concurrently on
@@ -304,9 +306,12 @@ lf_status lf_device_query(int *num_sms, int *pair_clusters);
  *     L2; 0 disables it, a negative value restores the default (off).
  *   gemm_variant: 1 = single-CTA 128x256 tiles, 2 = CTA-pair 256x256 tiles
  *     (tcgen05 cta_group::2) by whole tiles, 3 = CTA-pair tiles with the K
- *     iterations split evenly over all pairs (stream-K), anything else =
- *     automatic (pairs when M > 128; stream-K when whole tiles would leave
- *     more than 15% of the pairs idle in the last wave).
+ *     iterations split evenly over all pairs (stream-K), 4 = gemm_nt with the
+ *     operands swapped (M <= 128; whole tiles or stream-K chosen
+ *     automatically), anything else = automatic (swapped operands when M <=
+ *     128 and N has fewer 256-column tiles than half the SMs; pairs when M >
+ *     128 or a long K would leave most SMs idle; stream-K when whole tiles
+ *     would leave more than 15% of the pairs idle in the last wave).
  */
 void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant);
 

@@ -34,7 +34,8 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_inject{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_l2_prefetch{-1};  // -1: per-shape default
-std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA, 2 CTA-pair whole tiles, 3 CTA-pair stream-K
+std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA, 2 CTA-pair whole tiles, 3 CTA-pair stream-K,
+                                     // 4 swapped operands (skinny M)
 std::atomic<int> g_op_tile{0};       // one-pass cross-entropy N-tile width; 0 = automatic
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -234,9 +235,12 @@ struct GemmPlan {
 };
 
 lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int64_t N, int64_t K,
-                    GemmPlan *g, int layout = 0, const BatchSpec *bs = nullptr)
+                    GemmPlan *g, int layout = 0, const BatchSpec *bs = nullptr, int tile_n = 0)
 {
-    const int variant = g_variant.load();
+    // the swapped path (tile_n > 0) always runs on the pair kernel; it keeps an
+    // explicit whole-tile (2) or stream-K (3) choice, else decides automatically
+    const int gv = g_variant.load();
+    const int variant = tile_n ? ((gv == 2 || gv == 3) ? gv : -1) : gv;
     g->dev = d;
     if (bs)
         layout |= 4;
@@ -248,7 +252,7 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
     const int64_t tiles1 = ((M + lf::BM - 1) / lf::BM) * ((N + lf::BN - 1) / lf::BN);
     const bool skinny_split = tiles1 * 4 <= d->num_sms && (K + lf::BK - 1) / lf::BK >= 128;
     g->pair = d->pair_clusters > 0 &&
-              (layout != 0 || variant >= 2 || (variant < 0 && (M > lf::BM || skinny_split)));
+              (tile_n > 0 || layout != 0 || variant >= 2 || (variant < 0 && (M > lf::BM || skinny_split)));
     if (layout != 0 && !g->pair)
         return LF_ERR_LAUNCH;
     const int tile_m = g->pair ? 2 * lf::BM : lf::BM;
@@ -266,8 +270,8 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
                             : make_tmap3(&g->tb, w, K, N, bs->ldw, wb, sw, lf::BN / 2);
     } else {
         ok_a = (layout & 1) ? make_tmap_mn(&g->ta, x, M, K) : make_tmap(&g->ta, x, M, K, lf::BM);
-        ok_b = (layout & 2) ? make_tmap_mn(&g->tb, w, N, K)
-                            : make_tmap(&g->tb, w, N, K, g->pair ? lf::BN / 2 : lf::BN);
+        const uint32_t b_rows = tile_n ? static_cast<uint32_t>(tile_n / 2) : (g->pair ? lf::BN / 2 : lf::BN);
+        ok_b = (layout & 2) ? make_tmap_mn(&g->tb, w, N, K) : make_tmap(&g->tb, w, N, K, b_rows);
     }
     if (!ok_a || !ok_b)
         return LF_ERR_LAUNCH;
@@ -277,7 +281,8 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.num_m_blocks = static_cast<int>((M + tile_m - 1) / tile_m);
-    p.num_n_blocks = static_cast<int>((N + lf::BN - 1) / lf::BN);
+    p.tile_n = tile_n;
+    p.num_n_blocks = static_cast<int>((N + (tile_n ? tile_n : lf::BN) - 1) / (tile_n ? tile_n : lf::BN));
     p.num_k_blocks = static_cast<int>((K + lf::BK - 1) / lf::BK);
     const int64_t batch = bs ? bs->batch : 1;
     p.batch = static_cast<int>(batch);
@@ -371,7 +376,22 @@ lf_status gemm_nt(const void *x, const void *w, void *out, int64_t M, int64_t N,
         return st;
     if (K == 1)
         return launched(lf::launch_matmul_k1_bf16(x, w, out, M, N, d->num_sms, stream), 1);
+    const int variant = g_variant.load();
     GemmPlan g;
+    const int64_t tiles1 = (N + lf::BN - 1) / lf::BN;  // single-CTA tiles of a skinny X
+    if (d->pair_clusters > 0 && M <= lf::BM && (variant == 4 || (variant < 0 && tiles1 * 2 < d->num_sms))) {
+        // Skinny X with few output tiles: swap the operands so W's N rows fill
+        // the MMA's 256-row side and X's M rows (rounded up to 16) are the MMA's
+        // N -- outT = W . X^T, stored transposed -- instead of tiles whose X rows
+        // are mostly zero (64 x 5120 x 13824: 39 us against 54 us stream-K and
+        // 94 us single-CTA).  With enough tiles (64 x 32768 x 4096) the
+        // single-CTA kernel is faster (51 vs 55 us) and keeps the call.
+        if ((st = plan_gemm(d, w, x, N, M, K, &g, 0, nullptr, static_cast<int>((M + 15) / 16 * 16))) != LF_OK)
+            return st;
+        g.p.out = out;
+        g.p.ldo = N;
+        return launched(run_gemm(lf::EPI_STORE_T, g, stream), 1);
+    }
     if ((st = plan_gemm(d, x, w, M, N, K, &g)) != LF_OK)
         return st;
     g.p.out = out;
@@ -645,7 +665,7 @@ lf_status lf_device_query(int *num_sms, int *pair_clusters)
 void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant)
 {
     g_l2_prefetch.store(l2_prefetch_kblocks < 0 ? -1 : l2_prefetch_kblocks);
-    g_variant.store(gemm_variant >= 1 && gemm_variant <= 3 ? gemm_variant : -1);
+    g_variant.store(gemm_variant >= 1 && gemm_variant <= 4 ? gemm_variant : -1);
 }
 
 void lf_set_onepass_tile(int width)

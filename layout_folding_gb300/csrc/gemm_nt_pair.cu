@@ -50,7 +50,10 @@ constexpr int PAIR_EPI_WARPS = 4;
 constexpr int PAIR_SKC_CHUNKS = BN / 32;  // a contributor's partial arrives in 8 chunks of 32 columns
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2 + PAIR_SKC_CHUNKS;
 // per epilogue warp: 32 rows x 32 bf16 columns of output staged for row-contiguous stores
-constexpr int PAIR_STG_WARP_BYTES = 32 * 32 * 2;
+// (80-byte rows: the transposed store of EPI_STORE_T reads them 16 bytes at a time
+// without bank conflicts)
+constexpr int PAIR_STG_ROW = 80;
+constexpr int PAIR_STG_WARP_BYTES = 32 * PAIR_STG_ROW;
 constexpr int PAIR_STG_OFF = ((PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16 + 127) / 128) * 128;
 constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STG_OFF + PAIR_EPI_WARPS * PAIR_STG_WARP_BYTES;
 // Operand layouts (LAYOUT bit 0: X stored [K,M], M-major; bit 1: W stored
@@ -186,6 +189,50 @@ __device__ __forceinline__ bool pair_store(const GemmParams &p, __nv_bfloat16 *o
     return true;
 }
 
+// Swapped operands (skinny X): the accumulator holds acc[n][m] = sum_k W[n,k]
+// X[m,k] -- this thread's row is output column n = row0 + lane, its TMEM
+// columns are output rows m.  Each 32 x 32 chunk is written transposed into
+// the warp's staging tile (S[m][n], 80-byte rows) with 2-byte stores, then
+// thread t stores output row m = col + t: 32 consecutive n, 64 bytes.
+__device__ __forceinline__ bool pair_store_t(const GemmParams &p, __nv_bfloat16 *out, uint32_t taddr, int row0,
+                                             int nb, int tn, const PartialAdd &pa, uint32_t skc0, uint8_t *stg,
+                                             volatile int *abort_flag, uint32_t peer_abort)
+{
+    const int lane = threadIdx.x & 31;
+    const int M_out = p.N;  // the caller's M (kernel columns)
+    const int N_out = p.M;  // the caller's N (kernel rows)
+#pragma unroll 1
+    for (int c = 0; c < tn; c += 32) {
+        const int col = nb * tn + c;
+        if (col >= M_out)
+            break;  // warp-uniform
+        if (pa.smem0) {
+            const bool got = wait_bar(skc0 + 8u * static_cast<uint32_t>(c / 32), 0u, abort_flag, p, ERR_SK_COPY,
+                                      peer_abort);
+            if (!__all_sync(0xffffffffu, got))
+                return false;
+        }
+        uint32_t v[32];
+        load_chunk(taddr, c, pa, v);
+        __nv_bfloat16 *srow = reinterpret_cast<__nv_bfloat16 *>(stg);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)  // S[m = i][n = lane]
+            srow[i * (PAIR_STG_ROW / 2) + lane] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        __syncwarp();
+        const int m = col + lane;
+        if (m < M_out) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(stg + lane * PAIR_STG_ROW);
+            __nv_bfloat16 *dst = out + static_cast<size_t>(m) * p.ldo + row0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (row0 + 8 * j < N_out)  // N % 8 == 0: 8 columns are all in or all out
+                    *reinterpret_cast<uint4 *>(dst + 8 * j) = src[j];
+        }
+        __syncwarp();
+    }
+    return true;
+}
+
 // Gradient pass of the two-pass cross-entropy ("Allow reductions in matmul
 // epilogues", the softmax-minus-onehot output) for the warp's 32 rows:
 // grad = bf16_rn(exp(z - row_max - row_logsum) - [n == label]) with the
@@ -267,6 +314,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1;
     const int num_pairs = gridDim.x >> 1;
+    // the MMA's N: BN, or for the swapped-operand store the caller's M rounded up to 16
+    const int tn = (EPI == EPI_STORE_T && p.tile_n > 0) ? p.tile_n : BN;
+    // bytes both CTAs' copies of one K slice bring: A 128 rows, B tn / 2 rows each
+    const uint32_t stage_tx = 2u * (PAIR_A_BYTES + static_cast<uint32_t>(tn / 2) * BK * 2u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < PAIR_STAGES; ++s) {
@@ -318,7 +369,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 const int xz = p.x_batched ? bz : 0;
                 const int wz = p.w_batched ? bz : 0;
                 const int arow = mb * PAIR_M + static_cast<int>(rank) * BM;
-                const int brow = nb * BN + static_cast<int>(rank) * (BN / 2);
+                const int brow = nb * tn + static_cast<int>(rank) * (tn / 2);
                 for (int kb = g.kb0; kb < g.kb1; ++kb) {
                     if (!wait_bar(EMPTY_BAR(stage), phase ^ 1u, abort_flag, p, ERR_PRODUCER, peer_abort)) {
                         ok = false;
@@ -331,7 +382,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                     first = false;
                     if (!skip) {
                         if (leader) {
-                            mbar_arrive_expect_tx(FULL_BAR(stage), 2 * PAIR_STAGE_BYTES);
+                            mbar_arrive_expect_tx(FULL_BAR(stage), stage_tx);
                             ++armed[stage];
                         }
                         const uint32_t a_dst = sA + stage * PAIR_A_BYTES, b_dst = sB + stage * PAIR_B_BYTES;
@@ -395,7 +446,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                     tc_fence_after();
                     const uint32_t a0 = sA + stage * PAIR_A_BYTES;
                     const uint32_t b0 = sB + stage * PAIR_B_BYTES;
-                    constexpr uint32_t idesc = idesc_bf16_f32_major(PAIR_M, BN, (LAYOUT & 1) != 0, (LAYOUT & 2) != 0);
+                    const uint32_t idesc =
+                        idesc_bf16_f32_major(PAIR_M, static_cast<uint32_t>(tn), (LAYOUT & 1) != 0, (LAYOUT & 2) != 0);
 #pragma unroll
                     for (int k = 0; k < BK / PAIR_UMMA_K; ++k) {
                         const uint64_t da = (LAYOUT & 1) ? smem_desc_mn128(a0 + k * PAIR_MN_KSTEP, PAIR_MN_HALF)
@@ -480,7 +532,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 // chunks of 32 columns that lie inside the matrix: only those
                 // are copied, and each copy is waited for by the warps that
                 // read it (none is left in flight at exit)
-                const int nch = min(PAIR_SKC_CHUNKS, (p.N - nb * BN + 31) / 32);
+                const int nch = min((tn + 31) / 32, (p.N - nb * tn + 31) / 32);
                 if (owner_split && pa.count > 0) {
                     // This is the pair's last segment, so its MMAs are done and
                     // the operand ring is idle: pull the first contributor's
@@ -503,6 +555,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                     done = pair_store(p, static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(bz) * p.stride_o, taddr,
                                       row - lane, nb, pa, skc_bar,
                                       gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES, abort_flag, peer_abort);
+                else if (EPI == EPI_STORE_T)
+                    done = pair_store_t(p, static_cast<__nv_bfloat16 *>(p.out), taddr, row - lane, nb, tn, pa, skc_bar,
+                                        gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES, abort_flag,
+                                        peer_abort);
                 else {
                     if (pa.smem0) {
                         for (int c = 0; c < nch && done; ++c)
@@ -651,6 +707,8 @@ cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, cons
     switch (epi) {
     case EPI_STORE:
         return launch_pair_t<EPI_STORE, 0>(ta, tb, p, grid, s);
+    case EPI_STORE_T:
+        return launch_pair_t<EPI_STORE_T, 0>(ta, tb, p, grid, s);
     case EPI_XENT_PARTIAL:
         return launch_pair_t<EPI_XENT_PARTIAL, 0>(ta, tb, p, grid, s);
     case EPI_XENT_GRAD:

@@ -18,6 +18,7 @@ enum Epilogue : int {
     EPI_STORE = 0,         // out = bf16_rn(acc)
     EPI_XENT_PARTIAL = 1,  // per (row, N-tile): max, sum exp(z - max); label logit
     EPI_XENT_GRAD = 2,     // grad = bf16_rn(exp(z - lse) - onehot)
+    EPI_STORE_T = 3,       // swapped operands: acc = W . X^T, out[m][n] = bf16_rn(acc[n][m]) (pair kernel)
 };
 
 struct GemmParams {
@@ -53,6 +54,8 @@ struct GemmParams {
     int x_batched, w_batched;         // 0: one X (resp. W) for every batch
     long long ldo;                    // row pitch of out in elements (N when not strided)
     long long stride_o;               // batch stride of out in elements
+    // EPI_STORE_T: the MMA's N (the caller's M, rounded up to 16); 0 = BN
+    int tile_n;
 };
 
 // One stream-K partial slot: a CTA's 128 rows x 256 columns of fp32,

@@ -346,3 +346,42 @@ def test_xent_two_pass_gradient_on_pairs(variant):
     _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
     assert_loss_close(f64(loss)[rows], rloss, "two-pass")
     assert_grad_close(f64(grad)[rows], rgrad, "two-pass")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (8, 2056, 13824), (16, 4096, 4096), (33, 1032, 264),
+                                   (64, 5120, 13824), (100, 520, 2048), (128, 32768, 512), (64, 256, 128)])
+def test_skinny_gemm_swapped_operands(M, N, K):
+    """M <= 128 runs with the operands swapped (W's rows on the MMA's 256-row
+    side, X's rows as its N, the accumulator stored transposed), whole tiles or
+    stream-K as the planner picks; every element against the oracle."""
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    n0 = lf.launch_count()
+    out = lf.gemm_nt(x.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    assert lf.launch_count() - n0 == 1
+    lf.check_device_error()
+    ref = oracle.gemm_nt(x, w)
+    got = f64(out)
+    err = np.abs(got - ref)
+    scale = np.abs(ref).max()
+    assert err.max() <= 1e-2 * scale
+    assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-3 * scale)
+
+
+@pytest.mark.parametrize("variant", [2, 3])
+def test_skinny_gemm_swapped_whole_tiles_and_streamk(variant):
+    M, N, K = 48, 3000 - 3000 % 8, 1536
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lf.set_tuning(-1, 4)                     # force the swapped path ...
+    try:
+        out_auto = lf.gemm_nt(x.to(DEV), w.to(DEV))
+        lf.set_tuning(-1, variant)           # ... and compare with the given pair schedule
+        out_v = lf.gemm_nt(x.to(DEV), w.to(DEV))
+        torch.cuda.synchronize()
+    finally:
+        lf.set_tuning(-1, -1)
+    lf.check_device_error()
+    ref = oracle.gemm_nt(x, w)
+    for out in (out_auto, out_v):
+        err = np.abs(f64(out) - ref)
+        assert err.max() <= 1e-2 * np.abs(ref).max()
