@@ -423,7 +423,19 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
                           "tflops": round(flops / ms / 1e9, 1),
                           "pct_of_peak": round(100 * flops / ms / 1e9 / peaks["bf16_tflops"], 1),
                           "peak_kind": "bf16 burst (%s)" % peaks["source"]}
-        del xd, wd, outb, xpad
+        # skinny X (decode-like): 64 rows against the same W; HBM-bound on the
+        # 141.6 MB weight stream, computed with the operands swapped
+        xs64 = xd[:64].contiguous()
+        outs = torch.empty(64, wl.N, dtype=torch.bfloat16, device="cuda")
+        times = timer.run(lambda: lf.gemm_nt(xs64, wd, outs, stream=stream), max(steps, 10), 3)
+        ms = statistics.median(times)
+        wbytes = wl.N * wl.K * 2
+        res["skinny_m64"] = {"M": 64, "N": wl.N, "K": wl.K, "ms": round(ms, 5),
+                             "tflops": round(2.0 * 64 * wl.N * wl.K / ms / 1e9, 1),
+                             "w_stream_GB/s": round(wbytes / ms / 1e6, 1),
+                             "pct_of_hbm": round(100 * wbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
+                             "what": "W bytes / time against the HBM copy peak (swapped operands)"}
+        del xd, wd, outb, xpad, xs64, outs
         del out, inp
         torch.cuda.empty_cache()
     # RoPE segment (K=1 matmul + permute + cat + cos/sin -> bf16): the page's 4096
