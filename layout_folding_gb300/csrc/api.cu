@@ -218,6 +218,27 @@ bool make_tmap3(CUtensorMap *m, const void *ptr, int64_t inner, int64_t outer, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The output of the pair kernel's store epilogue as a bf16 tensor map: N
+// columns x M rows with a row pitch of ld elements (3-D: `batch` such matrices
+// `stride` elements apart, batch outermost); 32 x 32 boxes with the 64-byte
+// swizzle the epilogue's staging tiles use.  Returns false if the driver
+// rejects the layout (the kernel then stores without TMA).
+bool make_tmap_out(CUtensorMap *m, void *ptr, int64_t M, int64_t N, int64_t ld, int64_t batch, int64_t stride,
+                   bool three_d)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
+                                static_cast<cuuint64_t>(batch)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(stride) * 2};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, three_d ? 3 : 2, ptr, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A batch of strided views (gemm_batched): row pitches and batch strides in
 // elements; sw == 0 means one W for every batch.
 struct BatchSpec {
@@ -230,6 +251,7 @@ struct GemmPlan {
     int layout = 0;  // bit 0: X stored [K,M]; bit 1: W stored [K,N] (pair kernel only)
     DeviceState *dev = nullptr;
     CUtensorMap ta, tb;
+    CUtensorMap to;  // output map of the pair kernel's TMA-store epilogue (set by run_gemm)
     lf::GemmParams p;
     int grid = 0;
 };
@@ -336,7 +358,15 @@ cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
 {
     if (g.p.streamk)
         g.p.epoch = next_epoch(g.dev);  // each launch's flags are distinct from every earlier one
-    return g.pair ? lf::launch_gemm_nt_pair(epi, g.layout, g.ta, g.tb, g.p, g.grid, stream)
+    g.p.tma_store = 0;
+    std::memset(&g.to, 0, sizeof g.to);
+    if (g.pair && (epi == lf::EPI_STORE || epi == lf::EPI_XENT_GRAD) && g.p.out) {
+        const bool b3 = (g.layout & 4) != 0;
+        const int64_t batch = b3 ? g.p.batch : 1;
+        const int64_t stride = batch > 1 ? g.p.stride_o : static_cast<int64_t>(g.p.M) * g.p.ldo;
+        g.p.tma_store = make_tmap_out(&g.to, g.p.out, g.p.M, g.p.N, g.p.ldo, batch, stride, b3) ? 1 : 0;
+    }
+    return g.pair ? lf::launch_gemm_nt_pair(epi, g.layout, g.ta, g.tb, g.to, g.p, g.grid, stream)
                   : lf::launch_gemm_nt(epi, g.ta, g.tb, g.p, g.grid, stream);
 }
 

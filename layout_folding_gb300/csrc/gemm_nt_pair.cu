@@ -28,6 +28,9 @@
 //            with a multicast arrive to both CTAs' barriers.
 //   warps 2..5 (both CTAs): epilogue on this CTA's 128 accumulator rows; one
 //            lane per warp arrives on the leader's accumulator-free barrier.
+//            bf16 results (the plain store and the cross-entropy gradient)
+//            are packed into 32 x 32 staging tiles and leave through TMA
+//            stores, so the epilogue issues no global stores of its own.
 // Bounded waits everywhere; an abort raised in either CTA is mirrored into the
 // peer, and both meet at a final cluster barrier before TMEM is freed.
 #include <atomic>
@@ -49,12 +52,17 @@ constexpr int PAIR_THREADS = 192;  // producer, MMA, 4 epilogue warps
 constexpr int PAIR_EPI_WARPS = 4;
 constexpr int PAIR_SKC_CHUNKS = BN / 32;  // a contributor's partial arrives in 8 chunks of 32 columns
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2 + PAIR_SKC_CHUNKS;
-// per epilogue warp: 32 rows x 32 bf16 columns of output staged for row-contiguous stores
-// (80-byte rows: the transposed store of EPI_STORE_T reads them 16 bytes at a time
-// without bank conflicts)
+// Per epilogue warp: two 2 KiB slots, each 32 rows x 32 bf16 columns of output
+// (64-byte rows whose 16-byte pieces are XOR-swizzled by row pair -- the layout
+// of a TMA 64-byte swizzle), so a TMA store can read one slot while the warp
+// fills the other.  The transposed store of EPI_STORE_T uses the first 2560
+// bytes as 32 rows of 80 bytes (read 16 bytes at a time without bank conflicts).
 constexpr int PAIR_STG_ROW = 80;
-constexpr int PAIR_STG_WARP_BYTES = 32 * PAIR_STG_ROW;
-constexpr int PAIR_STG_OFF = ((PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16 + 127) / 128) * 128;
+constexpr int PAIR_STG_SLOT = 32 * 64;
+constexpr int PAIR_STG_WARP_BYTES = 2 * PAIR_STG_SLOT;
+static_assert(PAIR_STG_WARP_BYTES >= 32 * PAIR_STG_ROW, "transposed staging tile must fit");
+// 1024-byte aligned: the swizzle pattern of a TMA store follows the address bits
+constexpr int PAIR_STG_OFF = ((PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16 + 1023) / 1024) * 1024;
 constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STG_OFF + PAIR_EPI_WARPS * PAIR_STG_WARP_BYTES;
 // Operand layouts (LAYOUT bit 0: X stored [K,M], M-major; bit 1: W stored
 // [K,N], N-major; bit 2: batched, 3-D tensor maps with the batch as their
@@ -189,6 +197,81 @@ __device__ __forceinline__ bool pair_store(const GemmParams &p, __nv_bfloat16 *o
     return true;
 }
 
+// TMA-store path of the epilogues: chunk k of the warp (this thread's row of
+// 32 columns packed as 16 bf16 pairs) goes to staging slot k & 1 (64-byte
+// rows, 16-byte pieces XOR-swizzled by row pair: the output map's 64-byte
+// swizzle) and lane 0 stores the 32 x 32 box at (col, row0[, bz]); the TMA
+// unit leaves out the box's rows >= M and columns >= N.  A slot is refilled
+// only after the store issued from it two chunks earlier has read it.
+template <bool BATCHED>
+__device__ __forceinline__ void tma_store_chunk(const GemmParams &p, const CUtensorMap *tmO, uint8_t *stg,
+                                                uint32_t stg_s, int k, const uint32_t (&pk)[16], int col, int row0,
+                                                int bz)
+{
+    const int lane = threadIdx.x & 31;
+    const int slot = k & 1;
+    if (k >= 2) {
+        if (lane == 0)
+            bulk_wait_group_read<1>();
+        __syncwarp();
+    }
+    uint8_t *buf = stg + slot * PAIR_STG_SLOT;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4 *>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    fence_proxy_async_smem();  // the generic-proxy writes before the TMA unit reads them
+    __syncwarp();
+    if (lane == 0 && row0 < p.M) {
+        const uint32_t src = stg_s + static_cast<uint32_t>(slot * PAIR_STG_SLOT);
+        if (BATCHED)
+            tma_store_3d(tmO, src, col, row0, bz);
+        else
+            tma_store_2d(tmO, src, col, row0);
+        bulk_commit_group();
+    }
+}
+
+// After a tile's last chunk: every store has read its staging slot.
+__device__ __forceinline__ void tma_store_drain()
+{
+    if ((threadIdx.x & 31) == 0)
+        bulk_wait_group_read<0>();
+    __syncwarp();
+}
+
+// As pair_store, with the chunks written by TMA stores (tma_store_chunk).
+template <bool BATCHED>
+__device__ __forceinline__ bool pair_store_tma(const GemmParams &p, const CUtensorMap *tmO, uint32_t taddr, int row0,
+                                               int nb, int bz, const PartialAdd &pa, uint32_t skc0, uint8_t *stg,
+                                               uint32_t stg_s, volatile int *abort_flag, uint32_t peer_abort)
+{
+    bool ok = true;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        if (pa.smem0) {
+            const bool got = wait_bar(skc0 + 8u * static_cast<uint32_t>(c / 32), 0u, abort_flag, p, ERR_SK_COPY,
+                                      peer_abort);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+        }
+        uint32_t v[32];
+        load_chunk(taddr, c, pa, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        tma_store_chunk<BATCHED>(p, tmO, stg, stg_s, c / 32, pk, col, row0, bz);
+    }
+    tma_store_drain();
+    return ok;
+}
+
 // Swapped operands (skinny X): the accumulator holds acc[n][m] = sum_k W[n,k]
 // X[m,k] -- this thread's row is output column n = row0 + lane, its TMEM
 // columns are output rows m.  Each 32 x 32 chunk is written transposed into
@@ -239,8 +322,8 @@ __device__ __forceinline__ bool pair_store_t(const GemmParams &p, __nv_bfloat16 
 // exponent as one FFMA (z * log2 e - (max + logsum) * log2 e) and ex2.approx,
 // staged and stored like pair_store.  Row statistics come from the combine
 // kernel; this thread owns row row0 + lane.
-__device__ __forceinline__ void pair_xent_grad(const GemmParams &p, uint32_t taddr, int row0, int nb,
-                                               const PartialAdd &pa, uint8_t *stg)
+__device__ __forceinline__ void pair_xent_grad(const GemmParams &p, const CUtensorMap *tmO, uint32_t taddr, int row0,
+                                               int nb, const PartialAdd &pa, uint8_t *stg, uint32_t stg_s)
 {
     const int lane = threadIdx.x & 31;
     const int row = row0 + lane;
@@ -267,6 +350,10 @@ __device__ __forceinline__ void pair_xent_grad(const GemmParams &p, uint32_t tad
                 g1 -= 1.f;
             pk[i] = pack_bf16(g0, g1);
         }
+        if (p.tma_store) {
+            tma_store_chunk<false>(p, tmO, stg, stg_s, c / 32, pk, col, row0, 0);
+            continue;
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
@@ -284,12 +371,14 @@ __device__ __forceinline__ void pair_xent_grad(const GemmParams &p, uint32_t tad
         }
         __syncwarp();
     }
+    if (p.tma_store)
+        tma_store_drain();
 }
 
 template <int EPI, int LAYOUT>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     k_gemm_nt_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p)
+                   const __grid_constant__ CUtensorMap tmO, const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -338,6 +427,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if ((EPI == EPI_STORE || EPI == EPI_XENT_GRAD) && p.tma_store)
+            prefetch_tmap(&tmO);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_slot), PAIR_TMEM_COLS);
@@ -551,7 +642,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                     pa.smem0 = reinterpret_cast<const float4 *>(gbase);
                 }
                 bool done = true;
-                if (EPI == EPI_STORE)
+                if (EPI == EPI_STORE && p.tma_store)
+                    done = pair_store_tma<(LAYOUT & 4) != 0>(
+                        p, &tmO, taddr, row - lane, nb, bz, pa, skc_bar,
+                        gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES,
+                        base + static_cast<uint32_t>(PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES), abort_flag,
+                        peer_abort);
+                else if (EPI == EPI_STORE)
                     done = pair_store(p, static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(bz) * p.stride_o, taddr,
                                       row - lane, nb, pa, skc_bar,
                                       gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES, abort_flag, peer_abort);
@@ -569,8 +666,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                         if (EPI == EPI_XENT_PARTIAL)
                             epi_xent_partial(p, taddr, row, nb, pa);
                         else
-                            pair_xent_grad(p, taddr, row - lane, nb, pa,
-                                           gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES);
+                            pair_xent_grad(p, &tmO, taddr, row - lane, nb, pa,
+                                           gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES,
+                                           base + static_cast<uint32_t>(PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES));
                     }
                 }
                 if (!done)
@@ -644,8 +742,8 @@ cudaError_t set_smem_attr_once()
 }
 
 template <int EPI, int LAYOUT>
-cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid,
-                          cudaStream_t s)
+cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to, const GemmParams &p,
+                          int grid, cudaStream_t s)
 {
     cudaError_t e = set_smem_attr_once<EPI, LAYOUT>();
     if (e != cudaSuccess)
@@ -654,7 +752,7 @@ cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const Ge
     cudaLaunchConfig_t cfg = pair_config(grid, s, attr);
     if (LAYOUT)
         cfg.dynamicSmemBytes = PAIR_SMEM_BYTES_MN;
-    return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI, LAYOUT>, ta, tb, p);
+    return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI, LAYOUT>, ta, tb, to, p);
 }
 
 }  // namespace
@@ -680,39 +778,39 @@ int gemm_pair_max_active_clusters()
 }
 
 cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, const CUtensorMap &tb,
-                                const GemmParams &p, int grid, cudaStream_t s)
+                                const CUtensorMap &to, const GemmParams &p, int grid, cudaStream_t s)
 {
     if (layout != 0) {  // other operand layouts: plain store epilogue only
         if (epi != EPI_STORE)
             return cudaErrorInvalidValue;
         switch (layout) {
         case 1:
-            return launch_pair_t<EPI_STORE, 1>(ta, tb, p, grid, s);
+            return launch_pair_t<EPI_STORE, 1>(ta, tb, to, p, grid, s);
         case 2:
-            return launch_pair_t<EPI_STORE, 2>(ta, tb, p, grid, s);
+            return launch_pair_t<EPI_STORE, 2>(ta, tb, to, p, grid, s);
         case 3:
-            return launch_pair_t<EPI_STORE, 3>(ta, tb, p, grid, s);
+            return launch_pair_t<EPI_STORE, 3>(ta, tb, to, p, grid, s);
         case 4:
-            return launch_pair_t<EPI_STORE, 4>(ta, tb, p, grid, s);
+            return launch_pair_t<EPI_STORE, 4>(ta, tb, to, p, grid, s);
         case 5:
-            return launch_pair_t<EPI_STORE, 5>(ta, tb, p, grid, s);
+            return launch_pair_t<EPI_STORE, 5>(ta, tb, to, p, grid, s);
         case 6:
-            return launch_pair_t<EPI_STORE, 6>(ta, tb, p, grid, s);
+            return launch_pair_t<EPI_STORE, 6>(ta, tb, to, p, grid, s);
         case 7:
-            return launch_pair_t<EPI_STORE, 7>(ta, tb, p, grid, s);
+            return launch_pair_t<EPI_STORE, 7>(ta, tb, to, p, grid, s);
         default:
             return cudaErrorInvalidValue;
         }
     }
     switch (epi) {
     case EPI_STORE:
-        return launch_pair_t<EPI_STORE, 0>(ta, tb, p, grid, s);
+        return launch_pair_t<EPI_STORE, 0>(ta, tb, to, p, grid, s);
     case EPI_STORE_T:
-        return launch_pair_t<EPI_STORE_T, 0>(ta, tb, p, grid, s);
+        return launch_pair_t<EPI_STORE_T, 0>(ta, tb, to, p, grid, s);
     case EPI_XENT_PARTIAL:
-        return launch_pair_t<EPI_XENT_PARTIAL, 0>(ta, tb, p, grid, s);
+        return launch_pair_t<EPI_XENT_PARTIAL, 0>(ta, tb, to, p, grid, s);
     case EPI_XENT_GRAD:
-        return launch_pair_t<EPI_XENT_GRAD, 0>(ta, tb, p, grid, s);
+        return launch_pair_t<EPI_XENT_GRAD, 0>(ta, tb, to, p, grid, s);
     default:
         return cudaErrorInvalidValue;
     }

@@ -56,6 +56,9 @@ struct GemmParams {
     long long stride_o;               // batch stride of out in elements
     // EPI_STORE_T: the MMA's N (the caller's M, rounded up to 16); 0 = BN
     int tile_n;
+    // pair kernel, EPI_STORE and EPI_XENT_GRAD: 1 = the output tensor map is
+    // valid and the epilogue writes through TMA stores, 0 = plain stores
+    int tma_store;
 };
 
 // One stream-K partial slot: a CTA's 128 rows x 256 columns of fp32,
@@ -72,9 +75,12 @@ int gemm_smem_bytes();
 // [K rows, M columns], 64x64 boxes), else [M,K] (64-column x 128-row boxes);
 // bit 1: W stored [K,N] likewise, else [N,K]; bit 2: batched (3-D tensor
 // maps, batch outermost; p.batch, p.w_batched, p.ldo, p.stride_o).  Layouts
-// other than 0 support the EPI_STORE epilogue only.
+// other than 0 support the EPI_STORE epilogue only.  `to`: the output as a
+// bf16 tensor map (2-D [M rows, N columns], row pitch p.ldo; 3-D with the
+// batch outermost when batched), 32 x 32 boxes, 64-byte swizzle -- read only
+// when p.tma_store is set.
 cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, const CUtensorMap &tb,
-                                const GemmParams &p, int grid, cudaStream_t s);
+                                const CUtensorMap &to, const GemmParams &p, int grid, cudaStream_t s);
 int gemm_pair_smem_bytes();
 int gemm_pair_max_active_clusters();
 
