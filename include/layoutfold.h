@@ -87,12 +87,17 @@ lf_status gemm_nt(const void *x, const void *w, void *out,
  *   grad_or_null : NULL, or bf16 [M,N], device;
  *             grad[m,n] = bf16_rn(exp(z[m,n] - lse[m]) - [n == labels[m]]).
  *             When NULL nothing of size [M,N] is written anywhere.
- * Work: one GEMM pass writing per-(row, 256-column tile) partials (max,
- * sum-exp) and the label logit, one combine kernel, and -- only with grad --
- * a second GEMM pass that recomputes the logits and writes the gradient.
- * The partials live in a per-device workspace that the library allocates on
- * first use (and grows, never shrinks) and frees at unload; calls that share a
- * device must therefore not run concurrently on different streams.
+ * Work: without grad, one GEMM pass writing per-(row, 256-column tile)
+ * partials (max, sum-exp) and the label logit, then one combine kernel.  With
+ * grad, when a 256-row block of tiles fits on the co-resident CTA pairs (two
+ * N tiles per pair: N <= 512 x pairs), ONE launch computes the logits once and
+ * writes loss and gradient, the pairs of a row block exchanging their row
+ * partials through flags in global memory; otherwise the two passes above
+ * plus a GEMM pass that recomputes the logits and writes the gradient.
+ * Partials, flags and the one-pass kernel's stash (128 KiB per CTA) live in a
+ * per-device workspace that the library allocates on first use (and grows,
+ * never shrinks) and frees at unload; calls that share a device must
+ * therefore not run concurrently on different streams.
  */
 lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels,
                        float *loss, void *grad_or_null,

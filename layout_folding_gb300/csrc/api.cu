@@ -21,7 +21,8 @@ struct DeviceState {
     int num_sms = 0;
     int pair_clusters = 0;    // co-resident CTA pairs of the pair kernel
     void *sk_ws = nullptr;    // stream-K partial slots + flags (fixed size, zeroed once)
-    void *op_flags = nullptr; // one-pass cross-entropy round flags (2 per pair, zeroed once)
+    void *op_flags = nullptr; // one-pass cross-entropy: round flags (2 per pair, zeroed once), then
+                              // the per-CTA stash of a tile's exp values (128 x 256 fp32 per CTA)
     unsigned sk_epoch = 0;    // last epoch handed to a stream-K launch
     int *err_word = nullptr;  // device int[64]; [0] = first error code
     void *ws = nullptr;       // cross-entropy workspace (grow-only)
@@ -136,14 +137,23 @@ lf_status ensure_sk_workspace(DeviceState *d)
     return LF_OK;
 }
 
-// One-pass cross-entropy round flags, allocated and zeroed on first use.
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// One-pass cross-entropy workspace, allocated on first use: the round flags
+// (zeroed once; every launch's flags carry a new epoch) and the stash.
+size_t onepass_flag_bytes(const DeviceState *d)
+{
+    return round_up(static_cast<size_t>(2 * d->pair_clusters) * sizeof(unsigned long long), 256);
+}
+
 lf_status ensure_onepass_flags(DeviceState *d)
 {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (d->op_flags)
         return LF_OK;
-    const size_t bytes = static_cast<size_t>(2 * d->pair_clusters) * sizeof(unsigned long long);
-    if (cudaMalloc(&d->op_flags, bytes) != cudaSuccess || cudaMemset(d->op_flags, 0, bytes) != cudaSuccess ||
+    const size_t bytes = onepass_flag_bytes(d) + static_cast<size_t>(2 * d->pair_clusters) * lf::BM * lf::BN * 4;
+    if (cudaMalloc(&d->op_flags, bytes) != cudaSuccess ||
+        cudaMemset(d->op_flags, 0, onepass_flag_bytes(d)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         if (d->op_flags)
@@ -165,7 +175,6 @@ unsigned next_epoch(DeviceState *d)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // 2-D bf16 tensor [rows, K] (K contiguous), box = 64 columns x box_rows rows,
 // 128-byte swizzle; out-of-range rows/columns read as zero.
@@ -565,6 +574,7 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
             p.op_k = p.num_m_blocks;
         p.op_rounds = (p.num_m_blocks + p.op_k - 1) / p.op_k;
         p.round_flags = static_cast<unsigned long long *>(d->op_flags);
+        p.op_stash = reinterpret_cast<float *>(static_cast<char *>(d->op_flags) + onepass_flag_bytes(d));
         p.loss = loss;
         p.out = grad_or_null;
         p.epoch = next_epoch(d);

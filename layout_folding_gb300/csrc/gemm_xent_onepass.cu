@@ -1,6 +1,7 @@
 // gemm_xent_onepass.cu -- GEMM + row-wise cross-entropy + gradient in ONE
 // pass over the tensor cores: the logits are computed once, never written to
-// memory, and the gradient comes straight from the accumulators.
+// memory, and the gradient comes from the accumulators (one tile of each
+// pair by way of a stash in L2, so its accumulator is freed early).
 //
 // Source: "Allow reductions in matmul epilogues" (NVIDIA/Fuser issue 2213):
 // the fusion example (row max, sum-exp, log-sum-exp, label logit, and the
@@ -11,32 +12,39 @@
 // back.  That is what this kernel does, one 256-row block of rows at a time.
 //
 // Schedule: CTA pairs (tcgen05 cta_group::2, M=256 x N=op_tile MMAs; op_tile
-// is 256, or 128..224 for problems that fit one round of pairs) form groups of Q = ceil(N_tiles / 2) pairs; pair qi of a
-// group owns N tiles 2qi and 2qi+1 of the group's M block and keeps both
-// accumulators in TMEM (columns [0, op_tile) and [256, 256 + op_tile)).  k = floor(pairs / Q) groups run side by side, so a round
-// covers k M blocks; round r of group g is M block r*k + g.  Per round:
+// is 256, or 128..224 for problems that fit one round of pairs) form groups of
+// Q = ceil(N_tiles / 2) pairs; pair qi of a group owns N tiles 2qi and 2qi+1
+// of the group's M block.  k = floor(pairs / Q) groups run side by side, so a
+// round covers k M blocks; round r of group g is M block r*k + g.  The tile
+// processed first in a round (order 0) goes to accumulator 0 (TMEM columns
+// [0, op_tile)), the second to accumulator 1 ([256, 256 + op_tile)); the two
+// W tiles alternate their order every round so the next round starts on the
+// W rows L2 still holds.  Per round:
 //   1. mainloop of the pair's one or two tiles (same TMA/MMA machinery as the
 //      pair GEMM kernel);
 //   2. epilogue (8 warps; a thread owns a row, warpgroup h takes columns
 //      [128h, 128h + 128) of every tile): per-(row, half tile) statistics
 //      (max, sum exp(z - max), label logit) in one pass over TMEM with a
-//      running max, leaving exp(z - running max) in TMEM; warpgroup 1 hands
-//      its statistics to warpgroup 0 through shared memory, which merges the
-//      pair's four per row, stores one partial per row in slot [qi][row]
-//      (partial-major) and releases the CTA's flag (epoch << 32 | round+1);
-//   3. the lanes poll the flags of the group's Q pairs in parallel (acquire,
-//      bounded); each warpgroup merges half of the row's Q partials
-//      (coalesced loads, 16 per round trip), the halves are exchanged through
-//      shared memory, warpgroup 0 of the group's first pair writes loss[row];
-//   4. grad = exp(z - lse) - onehot from TMEM, staged per warp in shared
-//      memory so the stores are row-contiguous, first for the tile the next
-//      round's MMAs start with; each accumulator is released as soon as both
-//      warpgroups of both CTAs are done with it.
-// Measured per round at 4096x32768x4096 (one GB300): mainloop ~47 us; after
-// its last MMA, statistics ~1.6 us, publish ~2 us, the group's slowest pair
-// ~5 us (mainloop skew between pairs), merge ~2.7 us, gradient ~3.5 us (before
-// the column split: the split halves the statistics, merge and the wait for
-// the first freed accumulator).
+//      running max.  Tile 0's exp values go to a per-CTA stash in global
+//      memory (L2) while tile 1's MMAs run, and accumulator 0 is released at
+//      once, so the next round's first MMAs follow this round's last ones
+//      without waiting for the merge; tile 1's stay in TMEM.  Warpgroup 1
+//      hands its statistics to warpgroup 0 through shared memory, which
+//      merges the pair's four per row, stores one partial per row in slot
+//      [qi][row] (partial-major) and releases the CTA's flag (epoch << 32 |
+//      round+1) with one cumulative release store;
+//   3. one warp polls the flags of the group's Q pairs (acquire, bounded, with
+//      backoff) and hands the result to the other warps through an mbarrier;
+//      each warpgroup merges half of the row's Q partials (coalesced loads, 16
+//      per round trip), the halves are exchanged through shared memory,
+//      warpgroup 0 of the group's first pair writes loss[row];
+//   4. grad = exp(z - lse) - onehot, tile 1 from TMEM (then accumulator 1 is
+//      released), tile 0 from the stash, staged per warp in shared memory so
+//      the stores are row-contiguous.
+// Measured per round at 4096x32768x4096 (one GB300): two mainloops of ~24.5
+// us; the group's merge and the gradient of tile 1 overlap the next round's
+// first mainloop (before, with both tiles held in TMEM until the merge, ~16
+// us per round ran after the last MMA with the tensor cores idle).
 // The producer streams the next round's first K slices into the ring while
 // the epilogue runs.  Waits only go to the same round of the same group, whose
 // pairs never wait on anything later, so there is no cycle; every wait is
@@ -57,7 +65,7 @@ constexpr int OP_STAGE_BYTES = OP_A_BYTES + OP_B_BYTES;
 constexpr int OP_TMEM_COLS = 2 * BN;  // tile 0: columns [0, op_tile), tile 1: [256, 256 + op_tile)
 constexpr int OP_THREADS = 320;     // producer, MMA, and one epilogue warpgroup per tile
 constexpr int OP_EPI_WARPS = 4;    // per warpgroup (= per tile)
-constexpr int OP_NUM_BARS = 2 * OP_STAGES + 2 + 2 + 4;  // ring, tfull[2], tempty[2], drain, publish, exchange, merge
+constexpr int OP_NUM_BARS = 2 * OP_STAGES + 2 + 2 + 5;  // ring, tfull[2], tempty[2], drain, publish, exchange, merge, group
 constexpr int OP_XCH_BYTES = 8 * BM * 4;  // (max, sum) per row: 2 half-tile statistics + 2 half merges
 constexpr int OP_HALF = BN / 2;           // columns of a tile taken by one epilogue warpgroup
 constexpr int OP_HCH = OP_HALF / 32;      // 32-column chunks of a half
@@ -200,10 +208,12 @@ __device__ __forceinline__ void op_regs_after_wait(uint32_t (&v)[32])
 // is read once.  Returns the tile's max and sum of exp(z - max); cm[c] = m_c,
 // from which the gradient rescales chunk c.  The next chunk's TMEM load is in
 // flight while the current one is processed; max and sum are tree reductions.
-// FULL: all 128 columns of the half are in [col0, lim).
+// FULL: all 128 columns of the half are in [col0, lim).  With `stash` set the
+// exp values go to this thread's stash slots (float4 column j of the half at
+// stash[j * BM]) instead of back into TMEM, so the accumulator can be reused.
 template <bool FULL>
 __device__ __forceinline__ void op_half_stats(int lim, uint32_t taddr, int col0, int lab, float (&cm)[OP_HCH],
-                                              float &mx, float &se, float &zl, bool &have)
+                                              float &mx, float &se, float &zl, bool &have, float4 *stash)
 {
     const int lab_local = lab - col0;
     mx = -CUDART_INF_F;
@@ -237,21 +247,32 @@ __device__ __forceinline__ void op_half_stats(int lim, uint32_t taddr, int col0,
             se = se * ex2_approx((mx - m_c) * LOG2E) + op_tree_sum_bits(u);
             mx = m_c;
             cm[c] = m_c;
-            tmem_st_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), u);
+            if (stash) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    __stcg(stash + (c * 8 + i) * BM,
+                           make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                       __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3])));
+            } else {
+                tmem_st_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), u);
+            }
         }
     }
-    tmem_wait_st();
+    if (!stash)
+        tmem_wait_st();
 }
 
 // grad = bf16_rn(e * scale[c] - [n == label]) for this thread's row of one
-// half tile, e = exp(z - m_c) read back from TMEM, scale[c] = exp(m_c - lse).
+// half tile, e = exp(z - m_c) read back from TMEM (or from the stash when
+// `stash` is set), scale[c] = exp(m_c - lse).
 // The warp's 32 rows x 32 columns of a chunk are staged in shared memory
 // (16-byte pieces XOR-swizzled by row pair, conflict-free both ways) and
 // stored 8 rows x 64 bytes per instruction instead of 32 rows x 16 bytes.
 // (Double-buffering these TMEM loads spilled registers: 168 is the limit at
 // 10 warps per CTA.)
 __device__ __forceinline__ void op_half_grad(const GemmParams &p, int lim, uint32_t taddr, int row0, int col0,
-                                             int lab, const float (&scale)[OP_HCH], uint8_t *stg)
+                                             int lab, const float (&scale)[OP_HCH], uint8_t *stg,
+                                             const float4 *stash)
 {
     const int lane = threadIdx.x & 31;
     const int lab_local = lab - col0;
@@ -262,9 +283,20 @@ __device__ __forceinline__ void op_half_grad(const GemmParams &p, int lim, uint3
         const int nvalid = lim - col;  // warp-uniform
         if (nvalid > 0) {
             uint32_t u[32];
-            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), u);
-            tmem_wait_ld();
-            op_regs_after_wait(u);
+            if (stash) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 f = __ldcg(stash + (c * 8 + i) * BM);
+                    u[4 * i] = __float_as_uint(f.x);
+                    u[4 * i + 1] = __float_as_uint(f.y);
+                    u[4 * i + 2] = __float_as_uint(f.z);
+                    u[4 * i + 3] = __float_as_uint(f.w);
+                }
+            } else {
+                tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), u);
+                tmem_wait_ld();
+                op_regs_after_wait(u);
+            }
             const int li = lab_local - c * 32;
             uint32_t pk[16];
 #pragma unroll
@@ -310,10 +342,13 @@ __device__ __forceinline__ void op_merge2(float &m, float &s, float m2, float s2
 }
 
 // Gradient of this warpgroup's half of the tile processed in order i, then
-// an arrive on that tile's TMEM-empty barrier in the leader CTA.
+// an arrive on that tile's TMEM-empty barrier in the leader CTA -- or, for the
+// stashed tile (`stash` set: its accumulator was released after the
+// statistics), from the stash and without an arrive.
 __device__ __forceinline__ void op_grad_release(const GemmParams &p, const OpWork &w, int h, int i,
                                                 const float (&cmi)[OP_HCH], float m, float ls, uint32_t tlane,
-                                                int row0, int lab, uint8_t *stg, uint32_t tempty_bar)
+                                                int row0, int lab, uint8_t *stg, uint32_t tempty_bar,
+                                                const float4 *stash)
 {
     const int t = w.swap ? w.ntile - 1 - i : i;
     const int col0 = (w.nb0 + t) * p.op_tile + h * OP_HALF;
@@ -323,7 +358,9 @@ __device__ __forceinline__ void op_grad_release(const GemmParams &p, const OpWor
     for (int c = 0; c < OP_HCH; ++c)
         scale[c] = ex2_approx(((cmi[c] - m) - ls) * LOG2E);
     if (col0 < lim)
-        op_half_grad(p, lim, tlane + static_cast<uint32_t>(t * BN), row0, col0, lab, scale, stg);
+        op_half_grad(p, lim, tlane + static_cast<uint32_t>(i * BN), row0, col0, lab, scale, stg, stash);
+    if (stash)
+        return;
     tc_fence_before();
     __syncwarp();
     if ((threadIdx.x & 31) == 0)
@@ -338,6 +375,7 @@ __device__ __noinline__ bool wait_flag64(const unsigned long long *flag, unsigne
     for (uint32_t it = 0;; ++it) {
         if (ld_acquire_gpu_u64(flag) >= target)
             return true;
+        __nanosleep(64);
         if ((it & 15u) == 15u) {
             if (*abort_flag)
                 return false;
@@ -364,6 +402,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
     const uint32_t pub_bar = drain_bar + 8u;  // warpgroup 0 wrote the pair's merged partials
     const uint32_t xch_bar = pub_bar + 8u;    // warpgroup 1 handed over its half-tile statistics
     const uint32_t mrg_bar = xch_bar + 8u;    // both warpgroups stored their half of the row merge
+    const uint32_t grp_bar = mrg_bar + 8u;    // the polling warp saw every group member's flag
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *xch_mx = reinterpret_cast<float *>(gbase + OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8 + 16);
@@ -394,6 +433,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
         mbar_init(pub_bar, OP_EPI_WARPS);
         mbar_init(xch_bar, OP_EPI_WARPS);
         mbar_init(mrg_bar, 2 * OP_EPI_WARPS);
+        mbar_init(grp_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -470,13 +510,13 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             OpWork w;
             for (int r = 0; ok && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
                 for (int i = 0; ok && i < w.ntile; ++i) {
-                    const int t = w.swap ? w.ntile - 1 - i : i;
-                    if (!wait_bar(TEMPTY_BAR(t), tph[t] ^ 1u, abort_flag, p, ERR_MMA_ACC, peer_abort)) {
+                    // accumulator i holds the tile processed in order i
+                    if (!wait_bar(TEMPTY_BAR(i), tph[i] ^ 1u, abort_flag, p, ERR_MMA_ACC, peer_abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(t * BN);
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(i * BN);
                     for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                         if (!wait_bar(FULL_BAR(stage), phase, abort_flag, p, ERR_MMA_FULL, peer_abort)) {
                             ok = false;
@@ -497,8 +537,8 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                     }
                     if (!ok)
                         break;
-                    umma_commit_pair_mc(TFULL_BAR(t), 0x3);
-                    tph[t] ^= 1u;
+                    umma_commit_pair_mc(TFULL_BAR(i), 0x3);
+                    tph[i] ^= 1u;
                 }
             }
             umma_commit_pair_mc(drain_bar, 0x1);
@@ -515,10 +555,14 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
         uint8_t *stg = gbase + OP_STG_OFF + (warp - 2) * OP_STG_WARP_BYTES;
         const int rloc = q * 32 + lane;
         uint32_t eph_bits = 0;  // TFULL phase of tile t in bit t
-        uint32_t pub_phase = 0, xch_phase = 0, mrg_phase = 0;
+        uint32_t pub_phase = 0, xch_phase = 0, mrg_phase = 0, grp_phase = 0;
         const unsigned long long epoch_hi = static_cast<unsigned long long>(p.epoch) << 32;
         const uint32_t tlane =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * OP_HALF);
+        // this thread's stash slots: the CTA's 128 x 256 fp32 region, float4
+        // column j of half h at [(32 h + j) * BM + row]
+        float4 *stash = reinterpret_cast<float4 *>(p.op_stash) + static_cast<size_t>(blockIdx.x) * (BM * BN / 4) +
+                        static_cast<size_t>(h * 32) * BM + rloc;
         OpWork w;
         bool alive = true;
         for (int r = 0; alive && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
@@ -535,22 +579,35 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
 #pragma unroll 1
             for (int i = 0; i < w.ntile && alive; ++i) {
                 const int t = w.swap ? w.ntile - 1 - i : i;
-                const bool got = wait_bar(TFULL_BAR(t), (eph_bits >> t) & 1u, abort_flag, p, ERR_EPI, peer_abort);
+                const bool got = wait_bar(TFULL_BAR(i), (eph_bits >> i) & 1u, abort_flag, p, ERR_EPI, peer_abort);
                 alive = __all_sync(0xffffffffu, got);
                 if (alive) {
-                    eph_bits ^= 1u << t;
+                    eph_bits ^= 1u << i;
                     tc_fence_after();
                     const int col0 = (w.nb0 + t) * p.op_tile + h * OP_HALF;
                     // this half's columns end at the tile's width or at N
                     const int lim = min(p.N, (w.nb0 + t) * p.op_tile + min(p.op_tile, (h + 1) * OP_HALF));
                     float zl = 0.f, cmt[OP_HCH], tmt = -CUDART_INF_F, tst = 0.f;
                     bool have = false;
+                    // With two tiles, the first one's exp values go to the stash
+                    // while the second tile's MMAs run, and accumulator 0 is
+                    // released at once: the next round's first MMAs (into it)
+                    // follow this round's last ones without waiting for the
+                    // merge and the gradient.
+                    const bool to_stash = i == 0 && w.ntile == 2;
+                    float4 *st = to_stash ? stash : nullptr;
                     if (col0 + OP_HALF <= lim)
-                        op_half_stats<true>(lim, tlane + static_cast<uint32_t>(t * BN), col0, lab, cmt, tmt, tst, zl,
-                                            have);
+                        op_half_stats<true>(lim, tlane + static_cast<uint32_t>(i * BN), col0, lab, cmt, tmt, tst, zl,
+                                            have, st);
                     else if (col0 < lim)
-                        op_half_stats<false>(lim, tlane + static_cast<uint32_t>(t * BN), col0, lab, cmt, tmt, tst,
-                                             zl, have);
+                        op_half_stats<false>(lim, tlane + static_cast<uint32_t>(i * BN), col0, lab, cmt, tmt, tst,
+                                             zl, have, st);
+                    if (to_stash) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive_cluster(mapa_shared(TEMPTY_BAR(0), 0u));
+                    }
                     if (row_ok && have && lab < p.N)
                         p.label_logit[row] = zl;
                     // keep the results in registers named by the order index
@@ -569,8 +626,9 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                 break;
             // 2. warpgroup 1 hands its half statistics to warpgroup 0, which
             //    merges the pair's (tile, half) statistics per row, stores the
-            //    partial in slot [qi][row] and publishes the CTA's flag (the
-            //    mbarrier orders the lanes' stores before the one release)
+            //    partial in slot [qi][row] and publishes the CTA's flag: the
+            //    mbarrier orders the lanes' stores before the one release
+            //    store, which is cumulative at GPU scope (no separate fence)
             if (h == 1) {
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
@@ -598,20 +656,29 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                     mbar_arrive(pub_bar);
                 if (warp == 2 && lane == 0 &&
                     wait_bar(pub_bar, pub_phase, abort_flag, p, ERR_SK_SLOT, peer_abort)) {
-                    __threadfence();
                     st_release_gpu_u64(p.round_flags + pair * 2 + rank, epoch_hi | static_cast<unsigned>(r + 1));
                 }
                 pub_phase ^= 1u;
             }
-            // 3. wait for the group's pairs (same CTA rank holds the same rows);
-            //    the lanes poll the flags in parallel
+            // 3. wait for the group's pairs (same CTA rank holds the same rows):
+            //    one warp polls the flags (lanes in parallel, with backoff, so
+            //    the flags' cache lines are not flooded while the other CTAs
+            //    publish) and hands the result to the others through an
+            //    mbarrier (acquire by the poller, then release/acquire at CTA
+            //    scope: the partials it observed are visible to every warp)
             bool got = true;
-            {
+            if (warp == 2) {
                 const int first = (pair / p.op_Q) * p.op_Q;
                 const unsigned long long target = epoch_hi | static_cast<unsigned>(r + 1);
                 for (int j = lane; j < p.op_Q && got; j += 32)
                     got = wait_flag64(p.round_flags + (first + j) * 2 + rank, target, abort_flag, p, peer_abort);
+                got = __all_sync(0xffffffffu, got);
+                if (got && lane == 0)
+                    mbar_arrive(grp_bar);
             }
+            if (got)
+                got = wait_bar(grp_bar, grp_phase, abort_flag, p, ERR_OP_FLAG, peer_abort);
+            grp_phase ^= 1u;
             if (!__all_sync(0xffffffffu, got))
                 break;
             __syncwarp();
@@ -642,12 +709,15 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                 const int lb = p.labels[row];
                 p.loss[row] = (lb >= 0 && lb < p.N) ? (m - __ldcg(p.label_logit + row)) + ls : CUDART_NAN_F;
             }
-            // 5. gradient straight from TMEM, the tile the next round's MMAs
-            //    need first (this round's last) first; each tile's accumulator
-            //    is released as soon as both warpgroups of both CTAs are done
-            if (w.ntile == 2)
-                op_grad_release(p, w, h, 1, cm[1], m, ls, tlane, row0, lab, stg, TEMPTY_BAR(w.swap ? 0 : 1));
-            op_grad_release(p, w, h, 0, cm[0], m, ls, tlane, row0, lab, stg, TEMPTY_BAR(w.swap ? w.ntile - 1 : 0));
+            // 5. gradient: first the tile still in TMEM (its accumulator is
+            //    what the next round's second tile needs; released as soon as
+            //    both warpgroups of both CTAs are done), then the stashed one
+            if (w.ntile == 2) {
+                op_grad_release(p, w, h, 1, cm[1], m, ls, tlane, row0, lab, stg, TEMPTY_BAR(1), nullptr);
+                op_grad_release(p, w, h, 0, cm[0], m, ls, tlane, row0, lab, stg, 0u, stash);
+            } else {
+                op_grad_release(p, w, h, 0, cm[0], m, ls, tlane, row0, lab, stg, TEMPTY_BAR(0), nullptr);
+            }
         }
     }
 #undef FULL_BAR

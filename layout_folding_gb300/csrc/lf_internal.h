@@ -48,6 +48,7 @@ struct GemmParams {
     unsigned long long *round_flags;  // [2 * pairs]: (epoch << 32) | rounds published
     int op_Q, op_k, op_rounds;        // pairs per M block, M blocks per round, rounds
     int op_tile, op_ntiles;           // N-tile width (128..256, multiple of 32) and ceil(N / op_tile)
+    float *op_stash;                  // [CTAs][2 halves x 32 float4 columns][128 rows] float4: a tile's exp values
     // batches of strided views (pair kernel, plain store epilogue): tile
     // index = (batch, N block, M block), M block fastest
     int batch;                        // number of batches (0 or 1: not batched)
