@@ -578,7 +578,10 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
         p.loss = loss;
         p.out = grad_or_null;
         p.epoch = next_epoch(d);
-        return launched(lf::launch_xent_onepass(g.ta, tb_op, p, 2 * p.op_k * p.op_Q, stream), 1);
+        CUtensorMap to;  // the gradient, written by TMA stores
+        if (!make_tmap_out(&to, grad_or_null, M, N, N, 1, M * N, false))
+            return LF_ERR_LAUNCH;
+        return launched(lf::launch_xent_onepass(g.ta, tb_op, to, p, 2 * p.op_k * p.op_Q, stream), 1);
     }
     if ((st = launched(run_gemm(lf::EPI_XENT_PARTIAL, g, stream), 1)) != LF_OK)
         return st;

@@ -39,8 +39,8 @@
 //      per round trip), the halves are exchanged through shared memory,
 //      warpgroup 0 of the group's first pair writes loss[row];
 //   4. grad = exp(z - lse) - onehot, tile 1 from TMEM (then accumulator 1 is
-//      released), tile 0 from the stash, staged per warp in shared memory so
-//      the stores are row-contiguous.
+//      released), tile 0 from the stash, written by TMA stores of 32 x 32
+//      boxes staged per warp in shared memory.
 // Measured per round at 4096x32768x4096 (one GB300): two mainloops of ~24.5
 // us; the group's merge and the gradient of tile 1 overlap the next round's
 // first mainloop (before, with both tiles held in TMEM until the merge, ~16
@@ -71,10 +71,26 @@ constexpr int OP_HALF = BN / 2;           // columns of a tile taken by one epil
 constexpr int OP_HCH = OP_HALF / 32;      // 32-column chunks of a half
 constexpr int OP_STG_WARP_BYTES = 32 * 32 * 2;            // a warp's 32 rows x 32 bf16 gradient columns
 constexpr int OP_STG_OFF =
-    ((OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8 + 16 + OP_XCH_BYTES + 127) / 128) * 128;
+    ((OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8 + 16 + OP_XCH_BYTES + 1023) / 1024) * 1024;
 constexpr int OP_SMEM_BYTES = 1024 + OP_STG_OFF + 2 * OP_EPI_WARPS * OP_STG_WARP_BYTES;
 constexpr uint64_t OP_ABORT_SETTLE_NS = 100000;
 constexpr int ERR_OP_FLAG = 0x108;  // a group member never published its partials
+
+// L2 eviction policy: lines written with it are evicted after other lines.
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16-byte store with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void st_f4_hint(float4 *ptr, float4 v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(pol)
+                 : "memory");
+}
 
 struct OpWork {
     int mb, nb0, ntile;
@@ -210,7 +226,10 @@ __device__ __forceinline__ void op_regs_after_wait(uint32_t (&v)[32])
 // flight while the current one is processed; max and sum are tree reductions.
 // FULL: all 128 columns of the half are in [col0, lim).  With `stash` set the
 // exp values go to this thread's stash slots (float4 column j of the half at
-// stash[j * BM]) instead of back into TMEM, so the accumulator can be reused.
+// stash[j * BM]) instead of back into TMEM, so the accumulator can be reused;
+// they are written with an L2 evict-last policy, so the ~17 MB a round stashes
+// stay in L2 against the W stream until the gradient reads them back (without
+// it about half went to DRAM and came back: +0.5 GB of traffic per call).
 template <bool FULL>
 __device__ __forceinline__ void op_half_stats(int lim, uint32_t taddr, int col0, int lab, float (&cm)[OP_HCH],
                                               float &mx, float &se, float &zl, bool &have, float4 *stash)
@@ -248,11 +267,13 @@ __device__ __forceinline__ void op_half_stats(int lim, uint32_t taddr, int col0,
             mx = m_c;
             cm[c] = m_c;
             if (stash) {
+                const uint64_t pol = policy_evict_last();
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    __stcg(stash + (c * 8 + i) * BM,
-                           make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
-                                       __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3])));
+                    st_f4_hint(stash + (c * 8 + i) * BM,
+                               make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                           __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3])),
+                               pol);
             } else {
                 tmem_st_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), u);
             }
@@ -264,19 +285,17 @@ __device__ __forceinline__ void op_half_stats(int lim, uint32_t taddr, int col0,
 
 // grad = bf16_rn(e * scale[c] - [n == label]) for this thread's row of one
 // half tile, e = exp(z - m_c) read back from TMEM (or from the stash when
-// `stash` is set), scale[c] = exp(m_c - lse).
-// The warp's 32 rows x 32 columns of a chunk are staged in shared memory
-// (16-byte pieces XOR-swizzled by row pair, conflict-free both ways) and
-// stored 8 rows x 64 bytes per instruction instead of 32 rows x 16 bytes.
-// (Double-buffering these TMEM loads spilled registers: 168 is the limit at
-// 10 warps per CTA.)
-__device__ __forceinline__ void op_half_grad(const GemmParams &p, int lim, uint32_t taddr, int row0, int col0,
-                                             int lab, const float (&scale)[OP_HCH], uint8_t *stg,
-                                             const float4 *stash)
+// `stash` is set), scale[c] = exp(m_c - lse).  Each 32 x 32 chunk of the
+// warp is packed into its 2 KiB staging tile (16-byte pieces XOR-swizzled by
+// row pair: the gradient map's 64-byte swizzle) and lane 0 writes it with a
+// TMA store, which leaves out rows >= M and columns >= N.  (Double-buffering
+// the TMEM loads spilled registers: 168 is the limit at 10 warps per CTA.)
+__device__ __forceinline__ void op_half_grad(const GemmParams &p, const CUtensorMap *tmO, int lim, uint32_t taddr,
+                                             int row0, int col0, int lab, const float (&scale)[OP_HCH], uint8_t *stg,
+                                             uint32_t stg_s, const float4 *stash)
 {
     const int lane = threadIdx.x & 31;
     const int lab_local = lab - col0;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 #pragma unroll
     for (int c = 0; c < OP_HCH; ++c) {
         const int col = col0 + c * 32;
@@ -309,25 +328,27 @@ __device__ __forceinline__ void op_half_grad(const GemmParams &p, int lim, uint3
                     g1 -= 1.f;
                 pk[i] = pack_bf16(g0, g1);
             }
-            // row `lane`, piece j (8 columns) at slot j ^ ((lane >> 1) & 3)
+            // the warp's 32 x 32 chunk: row `lane`, piece j (8 columns) at
+            // slot j ^ ((lane >> 1) & 3) (the TMA 64-byte swizzle); the TMA
+            // store of the previous chunk must have read the buffer
+            if (lane == 0)
+                bulk_wait_group_read<0>();
+            __syncwarp();
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
                     make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            fence_proxy_async_smem();
             __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = 8 * i + (lane >> 2);  // row of the warp's 32
-                const int pc = lane & 3;            // 8-column piece
-                const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((pc ^ ((r >> 1) & 3)) << 4));
-                const int grow = row0 + r;
-                const int gcol = col + pc * 8;  // lim % 8 == 0: a piece is all in or all out
-                if (grow < p.M && gcol < lim)
-                    *reinterpret_cast<uint4 *>(out + static_cast<size_t>(grow) * p.N + gcol) = val;
+            if (lane == 0 && row0 < p.M) {
+                tma_store_2d(tmO, stg_s, col, row0);
+                bulk_commit_group();
             }
-            __syncwarp();
         }
     }
+    if (lane == 0)
+        bulk_wait_group_read<0>();
+    __syncwarp();
 }
 
 // (m, s) <- the merge of two (max, sum of exp(z - max)) statistics; an empty
@@ -345,9 +366,9 @@ __device__ __forceinline__ void op_merge2(float &m, float &s, float m2, float s2
 // an arrive on that tile's TMEM-empty barrier in the leader CTA -- or, for the
 // stashed tile (`stash` set: its accumulator was released after the
 // statistics), from the stash and without an arrive.
-__device__ __forceinline__ void op_grad_release(const GemmParams &p, const OpWork &w, int h, int i,
-                                                const float (&cmi)[OP_HCH], float m, float ls, uint32_t tlane,
-                                                int row0, int lab, uint8_t *stg, uint32_t tempty_bar,
+__device__ __forceinline__ void op_grad_release(const GemmParams &p, const CUtensorMap *tmO, const OpWork &w, int h,
+                                                int i, const float (&cmi)[OP_HCH], float m, float ls, uint32_t tlane,
+                                                int row0, int lab, uint8_t *stg, uint32_t stg_s, uint32_t tempty_bar,
                                                 const float4 *stash)
 {
     const int t = w.swap ? w.ntile - 1 - i : i;
@@ -358,7 +379,7 @@ __device__ __forceinline__ void op_grad_release(const GemmParams &p, const OpWor
     for (int c = 0; c < OP_HCH; ++c)
         scale[c] = ex2_approx(((cmi[c] - m) - ls) * LOG2E);
     if (col0 < lim)
-        op_half_grad(p, lim, tlane + static_cast<uint32_t>(i * BN), row0, col0, lab, scale, stg, stash);
+        op_half_grad(p, tmO, lim, tlane + static_cast<uint32_t>(i * BN), row0, col0, lab, scale, stg, stg_s, stash);
     if (stash)
         return;
     tc_fence_before();
@@ -389,7 +410,7 @@ __device__ __noinline__ bool wait_flag64(const unsigned long long *flag, unsigne
 
 __global__ void __launch_bounds__(OP_THREADS, 1)
     k_xent_onepass(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p)
+                   const __grid_constant__ CUtensorMap tmO, const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -440,6 +461,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmO);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(tmem_slot), OP_TMEM_COLS);
@@ -553,6 +575,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
         const int h = (warp - 2) >> 2;
         const int q = warp & 3;
         uint8_t *stg = gbase + OP_STG_OFF + (warp - 2) * OP_STG_WARP_BYTES;
+        const uint32_t stg_s = base + static_cast<uint32_t>(OP_STG_OFF + (warp - 2) * OP_STG_WARP_BYTES);
         const int rloc = q * 32 + lane;
         uint32_t eph_bits = 0;  // TFULL phase of tile t in bit t
         uint32_t pub_phase = 0, xch_phase = 0, mrg_phase = 0, grp_phase = 0;
@@ -713,10 +736,10 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             //    what the next round's second tile needs; released as soon as
             //    both warpgroups of both CTAs are done), then the stashed one
             if (w.ntile == 2) {
-                op_grad_release(p, w, h, 1, cm[1], m, ls, tlane, row0, lab, stg, TEMPTY_BAR(1), nullptr);
-                op_grad_release(p, w, h, 0, cm[0], m, ls, tlane, row0, lab, stg, 0u, stash);
+                op_grad_release(p, &tmO, w, h, 1, cm[1], m, ls, tlane, row0, lab, stg, stg_s, TEMPTY_BAR(1), nullptr);
+                op_grad_release(p, &tmO, w, h, 0, cm[0], m, ls, tlane, row0, lab, stg, stg_s, 0u, stash);
             } else {
-                op_grad_release(p, w, h, 0, cm[0], m, ls, tlane, row0, lab, stg, TEMPTY_BAR(0), nullptr);
+                op_grad_release(p, &tmO, w, h, 0, cm[0], m, ls, tlane, row0, lab, stg, stg_s, TEMPTY_BAR(0), nullptr);
             }
         }
     }
@@ -757,8 +780,8 @@ cudaError_t set_onepass_smem_attr_once()
 
 }  // namespace
 
-cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid,
-                                cudaStream_t s)
+cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
+                                const GemmParams &p, int grid, cudaStream_t s)
 {
     cudaError_t e = set_onepass_smem_attr_once();
     if (e != cudaSuccess)
@@ -775,7 +798,7 @@ cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, co
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_xent_onepass, ta, tb, p);
+    return cudaLaunchKernelEx(&cfg, k_xent_onepass, ta, tb, to, p);
 }
 
 }  // namespace lf

@@ -87,8 +87,9 @@ int gemm_pair_max_active_clusters();
 
 // One-pass GEMM + cross-entropy + gradient on CTA pairs (no recompute GEMM,
 // no combine kernel).  Requires op_k * op_Q co-resident pairs; grid = 2 * op_k * op_Q.
-cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p, int grid,
-                                cudaStream_t s);
+// `to`: the gradient (p.out) as a 2-D bf16 map, 32 x 32 boxes, 64-byte swizzle.
+cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
+                                const GemmParams &p, int grid, cudaStream_t s);
 
 cudaError_t launch_xent_combine(const float *part_max, const float *part_sum, const float *label_logit,
                                 const int32_t *labels, int M, int N, int num_n_blocks, float *loss,
