@@ -133,6 +133,52 @@ struct WorkIter {
     }
 };
 
+// Stream-K, plain store epilogues: the sum of the contributors' partials for
+// this thread's row (chunks of 32 columns [0, 32 nch)), loaded from L2 and
+// written into the idle accumulator buffer at `tpart` while this tile's own
+// MMAs still run, so the epilogue adds it with a TMEM load.  Two chunks (16
+// loads of 16 bytes) are in flight at a time.
+__device__ __forceinline__ void preload_partials(const PartialAdd &pa, uint32_t tpart, int nch)
+{
+#pragma unroll 1
+    for (int c = 0; c < nch; c += 2) {
+        const bool two = c + 1 < nch;  // warp-uniform
+        float v0[32], v1[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            v0[i] = 0.f;
+            v1[i] = 0.f;
+        }
+#pragma unroll 1
+        for (int e = 0; e < pa.count; ++e) {  // in pair order, as the fix-up adds them
+            const float4 *s4 = reinterpret_cast<const float4 *>(pa.slot + static_cast<size_t>(e) * pa.stride);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 f = __ldcg(s4 + (c * 8 + i) * BM + pa.row);
+                const float4 g = two ? __ldcg(s4 + ((c + 1) * 8 + i) * BM + pa.row) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v0[4 * i + 0] += f.x;
+                v0[4 * i + 1] += f.y;
+                v0[4 * i + 2] += f.z;
+                v0[4 * i + 3] += f.w;
+                v1[4 * i + 0] += g.x;
+                v1[4 * i + 1] += g.y;
+                v1[4 * i + 2] += g.z;
+                v1[4 * i + 3] += g.w;
+            }
+        }
+        uint32_t u0[32], u1[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            u0[i] = __float_as_uint(v0[i]);
+            u1[i] = __float_as_uint(v1[i]);
+        }
+        tmem_st_32x32b_x32(tpart + static_cast<uint32_t>(c * 32), u0);
+        if (two)
+            tmem_st_32x32b_x32(tpart + static_cast<uint32_t>((c + 1) * 32), u1);
+    }
+    tmem_wait_st();
+}
+
 // Stream-K: number of groups after this pair's group that hold the rest of
 // `tile` (their shares start before the tile's N-tile ends).  Contributor e is
 // pair (g + 1 + e) * MB + m.
@@ -581,7 +627,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             const int rloc = q * 32 + lane;
             const int row = mb * PAIR_M + static_cast<int>(rank) * BM + rloc;
             const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
-            PartialAdd pa = {nullptr, 0, 0, rloc};
+            PartialAdd pa = {nullptr, 0, 0, rloc, nullptr, 0, 0u};
             const bool owner_split = g.kb0 == 0 && g.kb1 < p.num_k_blocks;
             const int MB = p.num_m_blocks;
             const int first = (pair / MB + 1) * MB + pair % MB;  // first contributor pair
@@ -600,6 +646,17 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 pa.slot = p.sk_partials + static_cast<size_t>(first * 2 + rank) * SK_SLOT_FLOATS;
                 pa.stride = static_cast<size_t>(MB) * 2 * SK_SLOT_FLOATS;
                 pa.count = n;
+                if ((EPI == EPI_STORE || EPI == EPI_STORE_T) && n > 0) {
+                    // This is the pair's last segment, so the other
+                    // accumulator buffer is idle: sum the partials into it
+                    // while this tile's MMAs still run.
+                    const uint32_t tpart = tmem_base + static_cast<uint32_t>((acc ^ 1) * BN) +
+                                           (static_cast<uint32_t>(q * 32) << 16);
+                    preload_partials(pa, tpart, min((tn + 31) / 32, (p.N - nb * tn + 31) / 32));
+                    pa.in_tmem = 1;
+                    pa.tpart = tpart;
+                    pa.count = 0;
+                }
             }
             const bool ok = wait_bar(TFULL_BAR(acc), acc_phase, abort_flag, p, ERR_EPI, peer_abort);
             if (!__all_sync(0xffffffffu, ok))
