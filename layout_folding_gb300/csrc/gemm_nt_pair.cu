@@ -48,8 +48,6 @@ constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;    // 16 KiB: this CTA's 128 row
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_ACC_BUFS = 2;
 constexpr int PAIR_TMEM_COLS = PAIR_ACC_BUFS * BN;  // 512
-constexpr int PAIR_THREADS = 192;  // producer, MMA, 4 epilogue warps
-constexpr int PAIR_EPI_WARPS = 4;
 constexpr int PAIR_SKC_CHUNKS = BN / 32;  // a contributor's partial arrives in 8 chunks of 32 columns
 constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2 + PAIR_SKC_CHUNKS;
 // Per epilogue warp: two 2 KiB slots, each 32 rows x 32 bf16 columns of output
@@ -63,7 +61,26 @@ constexpr int PAIR_STG_WARP_BYTES = 2 * PAIR_STG_SLOT;
 static_assert(PAIR_STG_WARP_BYTES >= 32 * PAIR_STG_ROW, "transposed staging tile must fit");
 // 1024-byte aligned: the swizzle pattern of a TMA store follows the address bits
 constexpr int PAIR_STG_OFF = ((PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16 + 1023) / 1024) * 1024;
-constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STG_OFF + PAIR_EPI_WARPS * PAIR_STG_WARP_BYTES;
+// Epilogue warps per CTA: the plain store epilogues use two per TMEM lane
+// quarter (each takes half of the tile's columns, so the last tile's
+// epilogue -- the tail of the launch -- and a stream-K partial take half as
+// long); the cross-entropy epilogues reduce a whole row per thread and use one.
+template <int EPI>
+__host__ __device__ constexpr int pair_epi_warps()
+{
+    return (EPI == EPI_STORE || EPI == EPI_STORE_T) ? 8 : 4;
+}
+template <int EPI>
+__host__ __device__ constexpr int pair_threads()
+{
+    return 64 + 32 * pair_epi_warps<EPI>();  // producer, MMA, epilogue warps
+}
+template <int EPI>
+__host__ __device__ constexpr int pair_smem_bytes()
+{
+    return 1024 + PAIR_STG_OFF + pair_epi_warps<EPI>() * PAIR_STG_WARP_BYTES;
+}
+static_assert(pair_smem_bytes<EPI_STORE>() <= 232448, "shared memory per CTA");
 // Operand layouts (LAYOUT bit 0: X stored [K,M], M-major; bit 1: W stored
 // [K,N], N-major; bit 2: batched, 3-D tensor maps with the batch as their
 // outermost coordinate).  An MN-major operand arrives as two 64 x 64 boxes per K
@@ -71,10 +88,10 @@ constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STG_OFF + PAIR_EPI_WARPS * PAIR_STG_
 // an MN-major descriptor; each K=16 step advances two 1024-byte atoms.
 constexpr uint32_t PAIR_MN_HALF = PAIR_A_BYTES / 2;  // = PAIR_B_BYTES / 2
 constexpr uint32_t PAIR_MN_KSTEP = 2 * 1024;
-// The layout variants allocate 8 KiB of unused shared memory past the ring, so
-// that every address the MMA's descriptors can reach lies inside the
-// allocation even for the last stage.
-constexpr int PAIR_SMEM_BYTES_MN = PAIR_SMEM_BYTES + 8192;
+// An MN-major descriptor of the ring's last stage can reach up to 8 KiB past
+// the ring: the barriers and the staging tiles that follow it (at least 16
+// KiB) keep every such address inside the allocation.
+static_assert(4 * PAIR_STG_WARP_BYTES >= 8192, "room past the ring for MN-major descriptors");
 constexpr uint64_t ABORT_SETTLE_NS = 100000;  // after an abort: let copies in flight land
 
 // A run of K blocks [kb0, kb1) of one output tile.
@@ -134,14 +151,14 @@ struct WorkIter {
 };
 
 // Stream-K, plain store epilogues: the sum of the contributors' partials for
-// this thread's row (chunks of 32 columns [0, 32 nch)), loaded from L2 and
+// this thread's row (chunks of 32 columns [32 k0, 32 nch)), loaded from L2 and
 // written into the idle accumulator buffer at `tpart` while this tile's own
 // MMAs still run, so the epilogue adds it with a TMEM load.  Two chunks (16
 // loads of 16 bytes) are in flight at a time.
-__device__ __forceinline__ void preload_partials(const PartialAdd &pa, uint32_t tpart, int nch)
+__device__ __forceinline__ void preload_partials(const PartialAdd &pa, uint32_t tpart, int k0, int nch)
 {
 #pragma unroll 1
-    for (int c = 0; c < nch; c += 2) {
+    for (int c = k0; c < nch; c += 2) {
         const bool two = c + 1 < nch;  // warp-uniform
         float v0[32], v1[32];
 #pragma unroll
@@ -203,12 +220,12 @@ __device__ __forceinline__ int sk_contributors(const GemmParams &p, int pair, in
 // and reads are conflict-free) and stored 8 rows x 64 bytes per instruction
 // instead of 32 rows x 16 bytes.  Returns false if a copy wait gave up.
 __device__ __forceinline__ bool pair_store(const GemmParams &p, __nv_bfloat16 *out, uint32_t taddr, int row0, int nb,
-                                           const PartialAdd &pa, uint32_t skc0, uint8_t *stg,
+                                           int c0, int c1, const PartialAdd &pa, uint32_t skc0, uint8_t *stg,
                                            volatile int *abort_flag, uint32_t peer_abort)
 {
     const int lane = threadIdx.x & 31;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c0; c < c1; c += 32) {
         const int col = nb * BN + c;
         if (col >= p.N)
             break;  // warp-uniform
@@ -289,12 +306,13 @@ __device__ __forceinline__ void tma_store_drain()
 // As pair_store, with the chunks written by TMA stores (tma_store_chunk).
 template <bool BATCHED>
 __device__ __forceinline__ bool pair_store_tma(const GemmParams &p, const CUtensorMap *tmO, uint32_t taddr, int row0,
-                                               int nb, int bz, const PartialAdd &pa, uint32_t skc0, uint8_t *stg,
-                                               uint32_t stg_s, volatile int *abort_flag, uint32_t peer_abort)
+                                               int nb, int bz, int c0, int c1, const PartialAdd &pa, uint32_t skc0,
+                                               uint8_t *stg, uint32_t stg_s, volatile int *abort_flag,
+                                               uint32_t peer_abort)
 {
     bool ok = true;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c0; c < c1; c += 32) {
         const int col = nb * BN + c;
         if (col >= p.N)
             break;  // warp-uniform
@@ -312,7 +330,7 @@ __device__ __forceinline__ bool pair_store_tma(const GemmParams &p, const CUtens
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-        tma_store_chunk<BATCHED>(p, tmO, stg, stg_s, c / 32, pk, col, row0, bz);
+        tma_store_chunk<BATCHED>(p, tmO, stg, stg_s, (c - c0) / 32, pk, col, row0, bz);
     }
     tma_store_drain();
     return ok;
@@ -324,14 +342,14 @@ __device__ __forceinline__ bool pair_store_tma(const GemmParams &p, const CUtens
 // the warp's staging tile (S[m][n], 80-byte rows) with 2-byte stores, then
 // thread t stores output row m = col + t: 32 consecutive n, 64 bytes.
 __device__ __forceinline__ bool pair_store_t(const GemmParams &p, __nv_bfloat16 *out, uint32_t taddr, int row0,
-                                             int nb, int tn, const PartialAdd &pa, uint32_t skc0, uint8_t *stg,
-                                             volatile int *abort_flag, uint32_t peer_abort)
+                                             int nb, int tn, int c0, int c1, const PartialAdd &pa, uint32_t skc0,
+                                             uint8_t *stg, volatile int *abort_flag, uint32_t peer_abort)
 {
     const int lane = threadIdx.x & 31;
     const int M_out = p.N;  // the caller's M (kernel columns)
     const int N_out = p.M;  // the caller's N (kernel rows)
 #pragma unroll 1
-    for (int c = 0; c < tn; c += 32) {
+    for (int c = c0; c < c1; c += 32) {
         const int col = nb * tn + c;
         if (col >= M_out)
             break;  // warp-uniform
@@ -422,7 +440,7 @@ __device__ __forceinline__ void pair_xent_grad(const GemmParams &p, const CUtens
 }
 
 template <int EPI, int LAYOUT>
-__global__ void __launch_bounds__(PAIR_THREADS, 1)
+__global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     k_gemm_nt_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, const GemmParams p)
 {
@@ -461,10 +479,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         }
         for (int b = 0; b < PAIR_ACC_BUFS; ++b) {
             mbar_init(TFULL_BAR(b), 1);                    // the leader's multicast commit
-            mbar_init(TEMPTY_BAR(b), 2 * PAIR_EPI_WARPS);  // leader: one arrive per epilogue warp of each CTA
+            mbar_init(TEMPTY_BAR(b), 2 * pair_epi_warps<EPI>());  // leader: one arrive per epilogue warp of each CTA
         }
         mbar_init(drain_bar, 1);
-        mbar_init(skw_bar, PAIR_EPI_WARPS);
+        mbar_init(skw_bar, pair_epi_warps<EPI>());
         for (int c = 0; c < PAIR_SKC_CHUNKS; ++c)
             mbar_init(skc_bar + 8u * c, 1);
         *abort_flag = 0;
@@ -613,8 +631,16 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (both CTAs)
-        // warp w reads TMEM lanes 32 * (w % 4) .., one row per thread
+        // warp w reads TMEM lanes 32 * (w % 4) .., one row per thread; with 8
+        // epilogue warps, warps 2..5 take the first half of the tile's 32-column
+        // chunks and warps 6..9 the second half
         const int q = warp & 3;
+        constexpr int kParts = pair_epi_warps<EPI>() / 4;
+        const int cpart = (warp - 2) >> 2;
+        const int tile_chunks = (tn + 31) / 32;
+        const int part_chunks = (tile_chunks + kParts - 1) / kParts;
+        const int c0 = cpart * part_chunks * 32;
+        const int c1 = min(tile_chunks, (cpart + 1) * part_chunks) * 32;
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t skw_phase = 0;
@@ -652,7 +678,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                     // while this tile's MMAs still run.
                     const uint32_t tpart = tmem_base + static_cast<uint32_t>((acc ^ 1) * BN) +
                                            (static_cast<uint32_t>(q * 32) << 16);
-                    preload_partials(pa, tpart, min((tn + 31) / 32, (p.N - nb * tn + 31) / 32));
+                    preload_partials(pa, tpart, c0 / 32, min(c1 / 32, (p.N - nb * tn + 31) / 32));
                     pa.in_tmem = 1;
                     pa.tpart = tpart;
                     pa.count = 0;
@@ -665,7 +691,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             if (g.kb0 != 0) {
                 // Not the tile's first K blocks: hand the partial sum to the
                 // pair that owns the tile's start.
-                epi_write_partial(taddr, p.sk_partials + static_cast<size_t>(pair * 2 + rank) * SK_SLOT_FLOATS, rloc);
+                epi_write_partial(taddr, p.sk_partials + static_cast<size_t>(pair * 2 + rank) * SK_SLOT_FLOATS, rloc, c0,
+                                  c1);
                 __threadfence();
                 __syncwarp();
                 if (lane == 0)
@@ -701,16 +728,16 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 bool done = true;
                 if (EPI == EPI_STORE && p.tma_store)
                     done = pair_store_tma<(LAYOUT & 4) != 0>(
-                        p, &tmO, taddr, row - lane, nb, bz, pa, skc_bar,
+                        p, &tmO, taddr, row - lane, nb, bz, c0, c1, pa, skc_bar,
                         gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES,
                         base + static_cast<uint32_t>(PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES), abort_flag,
                         peer_abort);
                 else if (EPI == EPI_STORE)
                     done = pair_store(p, static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(bz) * p.stride_o, taddr,
-                                      row - lane, nb, pa, skc_bar,
+                                      row - lane, nb, c0, c1, pa, skc_bar,
                                       gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES, abort_flag, peer_abort);
                 else if (EPI == EPI_STORE_T)
-                    done = pair_store_t(p, static_cast<__nv_bfloat16 *>(p.out), taddr, row - lane, nb, tn, pa, skc_bar,
+                    done = pair_store_t(p, static_cast<__nv_bfloat16 *>(p.out), taddr, row - lane, nb, tn, c0, c1, pa, skc_bar,
                                         gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES, abort_flag,
                                         peer_abort);
                 else {
@@ -762,12 +789,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     }
 }
 
+template <int EPI>
 cudaLaunchConfig_t pair_config(int grid, cudaStream_t s, cudaLaunchAttribute *attr)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(PAIR_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+    cfg.blockDim = dim3(pair_threads<EPI>(), 1, 1);
+    cfg.dynamicSmemBytes = pair_smem_bytes<EPI>();
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -792,7 +820,7 @@ cudaError_t set_smem_attr_once()
     if (done.load() & bit)
         return cudaSuccess;
     e = cudaFuncSetAttribute(k_gemm_nt_pair<EPI, LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             LAYOUT ? PAIR_SMEM_BYTES_MN : PAIR_SMEM_BYTES);
+                             pair_smem_bytes<EPI>());
     if (e == cudaSuccess)
         done.fetch_or(bit);
     return e;
@@ -806,26 +834,24 @@ cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const CU
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pair_config(grid, s, attr);
-    if (LAYOUT)
-        cfg.dynamicSmemBytes = PAIR_SMEM_BYTES_MN;
+    cudaLaunchConfig_t cfg = pair_config<EPI>(grid, s, attr);
     return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI, LAYOUT>, ta, tb, to, p);
 }
 
 }  // namespace
 
-int gemm_pair_smem_bytes() { return PAIR_SMEM_BYTES; }
+int gemm_pair_smem_bytes() { return pair_smem_bytes<EPI_STORE>(); }
 
 // Number of CTA pairs of the pair kernel that fit on the device at once.
 int gemm_pair_max_active_clusters()
 {
     if (cudaFuncSetAttribute(k_gemm_nt_pair<EPI_STORE, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PAIR_SMEM_BYTES) != cudaSuccess) {
+                             pair_smem_bytes<EPI_STORE>()) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pair_config(2, 0, attr);
+    cudaLaunchConfig_t cfg = pair_config<EPI_STORE>(2, 0, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, k_gemm_nt_pair<EPI_STORE, 0>, &cfg) != cudaSuccess) {
         cudaGetLastError();

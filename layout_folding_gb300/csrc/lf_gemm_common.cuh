@@ -161,12 +161,13 @@ __device__ __forceinline__ void load_chunk(uint32_t taddr, int c, const PartialA
     }
 }
 
-// Store this thread's whole accumulator row (256 fp32) into a stream-K slot.
-__device__ __forceinline__ void epi_write_partial(uint32_t taddr, float *slot, int row)
+// Store columns [c0, c1) of this thread's accumulator row (fp32) into a
+// stream-K slot.
+__device__ __forceinline__ void epi_write_partial(uint32_t taddr, float *slot, int row, int c0 = 0, int c1 = BN)
 {
     float4 *s4 = reinterpret_cast<float4 *>(slot);
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c0; c < c1; c += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + c, v);
         tmem_wait_ld();
