@@ -323,9 +323,9 @@ void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant);
 /*
  * N-tile width of the one-pass cross-entropy-with-gradient kernel, applied to
  * later gemm_nt_xent calls with a gradient: 128, 160, 192, 224 or 256; any
- * other value restores the automatic choice (256, or for a problem that
- * takes a single round of pairs, the width that minimises that round).  A forced width whose
- * group does not fit the resident pairs falls back to the two-pass path.
+ * other value restores the automatic choice (the width with the least rounds
+ * x width among those whose group fits the resident pairs).  A forced width
+ * whose group does not fit the resident pairs falls back to the two-pass path.
  */
 void lf_set_onepass_tile(int width);
 

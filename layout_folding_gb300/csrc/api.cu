@@ -531,12 +531,12 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
     p.labels = labels;
     // With a gradient on CTA pairs: one pass, when a whole 256-row block of
     // tiles (two per pair) fits on the resident pairs -- no recompute GEMM and
-    // no combine kernel.  N-tile width: 256, unless the whole problem takes a
-    // single round, where narrower tiles (more pairs, shorter MMA chains)
-    // shorten that round.  With several rounds narrower tiles measured slower
-    // even when they keep more pairs busy (4096 x 32768 x 4096: 1.011 ms at
-    // 256 with 64 pairs, 1.038 ms at 224 with 74): every pair re-reads its M
-    // block of X per tile, and the extra operand traffic outweighs the MMAs.
+    // no combine kernel.  N-tile width: the one with the least rounds x width
+    // (the time of a round is about proportional to its tiles' width), i.e. the
+    // narrowest that keeps the fewest rounds: more pairs busy, shorter MMA
+    // chains.  (4096 x 32768 x 4096: 0.836 ms at 224 with 74 pairs against
+    // 0.847 ms at 256 with 64.  Before the round's merge overlapped the next
+    // mainloop, 224 measured slower, 1.038 against 1.011 ms.)
     int op_tile = 0;
     long long best = 0;
     const int forced = g_op_tile.load();
@@ -551,8 +551,6 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
         if (k > p.num_m_blocks)
             k = p.num_m_blocks;
         const int rounds = (p.num_m_blocks + k - 1) / k;
-        if (wdt < 256 && rounds > 1 && !forced)
-            continue;
         const long long cost = static_cast<long long>(rounds) * wdt;
         if (op_tile == 0 || cost < best) {
             op_tile = wdt;
