@@ -316,6 +316,66 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
     res = {}
     steps = max(3, min(args.steps, 10))
     want = {p.strip() for p in args.paths.split(",") if p.strip()}
+    # The bandwidth-bound legs run first: in one process, after the
+    # cross-entropy legs' multi-GB allocations had been freed, the 2 GiB K=1
+    # write measured 431 us against 360 us run first or in a fresh process
+    # (an allocation effect, not a thermal one: a fresh process right after a
+    # cross-entropy run measured 360 us too).
+    # K=1: the page's [64,1]x[1,4096] (latency regime) and a scaled column count for bandwidth
+    a, b = synthetic.k1_operands(64, 4096)
+    for label, N in ((("k1_rope", 4096), ("k1_scaled", 1 << 23)) if "k1" in want else ()):
+        bb = torch.arange(N, dtype=torch.float32).reshape(1, N) if N != 4096 else b
+        ad, bd = a.to("cuda"), bb.to("cuda")
+        out = torch.empty(64, N, dtype=torch.float32, device="cuda")
+
+        def step():
+            lf.matmul_k1(ad, bd, out, stream=stream)
+        times = timer.run(step, max(steps, 10), 3)
+        ms = statistics.median(times)
+        nbytes = (64 + N + 64 * N) * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[label] = {"M": 64, "N": N, "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes}
+        del ad, bd, out
+    torch.cuda.empty_cache()
+    # RoPE segment (K=1 matmul + permute + cat + cos/sin -> bf16): the page's 4096
+    # positions, and 2^20 positions (32 sequences of 32768) for bandwidth
+    for label, (S, maxp) in ((("rope_page", (4096, 0)), ("rope_scaled", (1 << 20, 32768))) if "rope" in want else ()):
+        inv, pos = synthetic.rope_operands(64, S, max_position=maxp)
+        inv, pos = inv.to("cuda"), pos.to("cuda")
+        co = torch.empty(S, 128, dtype=torch.bfloat16, device="cuda")
+        so = torch.empty(S, 128, dtype=torch.bfloat16, device="cuda")
+
+        def step():
+            lf.rope_cos_sin(inv, pos, cos_out=co, sin_out=so, stream=stream)
+        times = timer.run(step, max(steps, 10), 3)
+        ms = statistics.median(times)
+        nbytes = 64 * 2 + S * 8 + 2 * S * 128 * 2
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[label] = {"H": 64, "S": S, "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes,
+                      "angles_per_s": round(S * 64 / (ms * 1e-3), 1),
+                      "traffic": recorded_traffic("k_rope_cos_sin_v8", label)}
+        del inv, pos, co, so
+    # fused fp8 cast, both layouts: the page's 4096 x 4096 and a scaled case larger than L2
+    scale = torch.tensor([10.0], dtype=torch.float32, device="cuda")
+    for label, (M, K) in ((("fp8_cast_page", (4096, 4096)), ("fp8_cast_scaled", (16384, 16384))) if "fp8" in want
+                          else ()):
+        x = synthetic.bf16_normal((M, K), 1.0, 15).to("cuda")
+        out = torch.empty(M, K, dtype=torch.float8_e4m3fn, device="cuda")
+        out_t = torch.empty(K, M, dtype=torch.float8_e4m3fn, device="cuda").t()
+
+        def step():
+            lf.fp8_cast_dual(x, scale, out=out, out_t=out_t, stream=stream)
+        times = timer.run(step, max(steps, 10), 3)
+        ms = statistics.median(times)
+        nbytes = M * K * (2 + 1 + 1)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[label] = {"M": M, "K": K, "scale": 10.0, "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes,
+                      "traffic": recorded_traffic("k_fp8_cast_dual_v16", label)}
+        del x, out, out_t
+    torch.cuda.empty_cache()
     for name, want_grad in ((("xent_grad", True), ("xent_loss", False), ("xent_loss", True)) if "xent" in want
                             else ()):
         wl = synthetic.WORKLOADS[name]
@@ -363,23 +423,6 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
             del logits, lab64
         del x, w, lab, loss, grad, inp
         torch.cuda.empty_cache()
-    # K=1: the page's [64,1]x[1,4096] (latency regime) and a scaled column count for bandwidth
-    a, b = synthetic.k1_operands(64, 4096)
-    for label, N in ((("k1_rope", 4096), ("k1_scaled", 1 << 23)) if "k1" in want else ()):
-        bb = torch.arange(N, dtype=torch.float32).reshape(1, N) if N != 4096 else b
-        ad, bd = a.to("cuda"), bb.to("cuda")
-        out = torch.empty(64, N, dtype=torch.float32, device="cuda")
-
-        def step():
-            lf.matmul_k1(ad, bd, out, stream=stream)
-        times = timer.run(step, max(steps, 10), 3)
-        ms = statistics.median(times)
-        nbytes = (64 + N + 64 * N) * 4
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        res[label] = {"M": 64, "N": N, "ms": round(ms, 5), "GB/s": round(gbs, 1),
-                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes}
-        del ad, bd, out
-    torch.cuda.empty_cache()
     # other operand layouts at the headline shape: W stored [K,N] (the trace's
     # transposed copy, read as is), X stored [K,M], both
     if "layouts" in want:
@@ -438,43 +481,6 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
         del xd, wd, outb, xpad, xs64, outs
         del out, inp
         torch.cuda.empty_cache()
-    # RoPE segment (K=1 matmul + permute + cat + cos/sin -> bf16): the page's 4096
-    # positions, and 2^20 positions (32 sequences of 32768) for bandwidth
-    for label, (S, maxp) in ((("rope_page", (4096, 0)), ("rope_scaled", (1 << 20, 32768))) if "rope" in want else ()):
-        inv, pos = synthetic.rope_operands(64, S, max_position=maxp)
-        inv, pos = inv.to("cuda"), pos.to("cuda")
-        co = torch.empty(S, 128, dtype=torch.bfloat16, device="cuda")
-        so = torch.empty(S, 128, dtype=torch.bfloat16, device="cuda")
-
-        def step():
-            lf.rope_cos_sin(inv, pos, cos_out=co, sin_out=so, stream=stream)
-        times = timer.run(step, max(steps, 10), 3)
-        ms = statistics.median(times)
-        nbytes = 64 * 2 + S * 8 + 2 * S * 128 * 2
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        res[label] = {"H": 64, "S": S, "ms": round(ms, 5), "GB/s": round(gbs, 1),
-                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes,
-                      "angles_per_s": round(S * 64 / (ms * 1e-3), 1),
-                      "traffic": recorded_traffic("k_rope_cos_sin_v8", label)}
-        del inv, pos, co, so
-    # fused fp8 cast, both layouts: the page's 4096 x 4096 and a scaled case larger than L2
-    scale = torch.tensor([10.0], dtype=torch.float32, device="cuda")
-    for label, (M, K) in ((("fp8_cast_page", (4096, 4096)), ("fp8_cast_scaled", (16384, 16384))) if "fp8" in want
-                          else ()):
-        x = synthetic.bf16_normal((M, K), 1.0, 15).to("cuda")
-        out = torch.empty(M, K, dtype=torch.float8_e4m3fn, device="cuda")
-        out_t = torch.empty(K, M, dtype=torch.float8_e4m3fn, device="cuda").t()
-
-        def step():
-            lf.fp8_cast_dual(x, scale, out=out, out_t=out_t, stream=stream)
-        times = timer.run(step, max(steps, 10), 3)
-        ms = statistics.median(times)
-        nbytes = M * K * (2 + 1 + 1)
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        res[label] = {"M": M, "K": K, "scale": 10.0, "ms": round(ms, 5), "GB/s": round(gbs, 1),
-                      "pct_of_hbm": round(100 * gbs / peaks["hbm_gbs"], 1), "bytes": nbytes,
-                      "traffic": recorded_traffic("k_fp8_cast_dual_v16", label)}
-        del x, out, out_t
     torch.cuda.empty_cache()
     return res
 
