@@ -19,18 +19,22 @@
 // memory holds a 6-deep ring instead of a 4-deep one (50% more load latency
 // covered).
 //
-// Roles (192 threads per CTA, cluster of 2 CTAs, rank 0 = leader):
+// Roles (320 threads per CTA for the plain store epilogues, 192 for the
+// cross-entropy ones; cluster of 2 CTAs, rank 0 = leader):
 //   warp 0 (both CTAs): TMA producer for this CTA's halves; both CTAs' copies
 //            complete on the LEADER's full barrier (the leader arms it for the
 //            bytes of both halves).
 //   warp 1 (both CTAs): TMEM allocation (pair form); in the leader one lane
 //            issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and commits
 //            with a multicast arrive to both CTAs' barriers.
-//   warps 2..5 (both CTAs): epilogue on this CTA's 128 accumulator rows; one
-//            lane per warp arrives on the leader's accumulator-free barrier.
-//            bf16 results (the plain store and the cross-entropy gradient)
-//            are packed into 32 x 32 staging tiles and leave through TMA
-//            stores, so the epilogue issues no global stores of its own.
+//   warps 2..9 or 2..5 (both CTAs): epilogue on this CTA's 128 accumulator
+//            rows (warp w reads TMEM lanes 32 (w % 4) ..; with 8 warps each
+//            takes half of a tile's columns); one lane per warp arrives on
+//            the leader's accumulator-free barrier.  bf16 results (the plain
+//            store and the cross-entropy gradient) are packed into 32 x 32
+//            staging tiles and leave through TMA stores.  A stream-K owner's
+//            idle epilogue warps sum its contributors' fp32 partials into the
+//            second TMEM accumulator while its last MMAs run.
 // Bounded waits everywhere; an abort raised in either CTA is mirrored into the
 // peer, and both meet at a final cluster barrier before TMEM is freed.
 #include <atomic>
