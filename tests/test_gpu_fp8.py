@@ -160,3 +160,19 @@ def test_four_row_tiles_with_ragged_tails():
     cols = [0, 63, 64, K - 17, K - 16, K - 1]
     ref_cols, _ = oracle.fp8_cast_dual(x_cpu[:, cols].contiguous(), 10.0)
     np.testing.assert_array_equal(out_t.view(torch.uint8)[:, cols].cpu().numpy(), ref_cols)
+
+
+def test_bench_shape_16384_sampled():
+    """The bench's bandwidth case, 16384 x 16384 with scale 10 (the four-row
+    tile path): the two layouts hold the same codes everywhere, sampled rows
+    and columns match the oracle bit for bit."""
+    M = K = 16384
+    x_cpu = synthetic.bf16_normal((M, K), 1.0, 15)
+    out, out_t = run(x_cpu, 10.0)
+    assert torch.equal(out.view(torch.uint8), out_t.contiguous().view(torch.uint8))
+    rows = sorted({0, 255, 256, 8191, M - 1} | set(np.random.default_rng(4).integers(0, M, 27).tolist()))
+    ref, _ = oracle.fp8_cast_dual(x_cpu[rows], 10.0)
+    np.testing.assert_array_equal(out.view(torch.uint8)[rows].cpu().numpy(), ref)
+    cols = [0, 63, 64, K - 1]
+    ref_cols, _ = oracle.fp8_cast_dual(x_cpu[:, cols].contiguous(), 10.0)
+    np.testing.assert_array_equal(out_t.view(torch.uint8)[:, cols].cpu().numpy(), ref_cols)

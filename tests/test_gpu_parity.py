@@ -385,3 +385,22 @@ def test_skinny_gemm_swapped_whole_tiles_and_streamk(variant):
     for out in (out_auto, out_v):
         err = np.abs(f64(out) - ref)
         assert err.max() <= 1e-2 * np.abs(ref).max()
+
+
+def test_matmul_k1_bandwidth_shape_sampled_bitexact():
+    """The bench's bandwidth case, [64,1] x [1, 8388608] (2 GiB out), in the
+    bench's launch configuration: sampled rows bit-exact against the oracle,
+    and the whole output against the fp32 broadcast product on the device
+    (one fp32 multiply per element, so any correct kernel is bit-identical)."""
+    N = 1 << 23
+    a, _ = synthetic.k1_operands(64, 4096)
+    b = torch.arange(N, dtype=torch.float32).reshape(1, N)
+    ad, bd = a.to(DEV), b.to(DEV)
+    out = lf.matmul_k1(ad, bd)
+    torch.cuda.synchronize()
+    assert out.shape == (64, N)
+    rows = [0, 1, 31, 63]
+    want = oracle.matmul_k1(a.numpy()[rows], b.numpy())
+    got = out[rows].cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    assert torch.equal(out, ad.reshape(64, 1) * bd)

@@ -102,3 +102,23 @@ def test_launches_one_kernel():
     n0 = lf.launch_count()
     lf.rope_cos_sin(inv, pos)
     assert lf.launch_count() - n0 == 1
+
+
+def test_bench_shape_2_20_positions_sampled():
+    """The bench's bandwidth case: 2^20 positions (32 sequences of 32768),
+    H = 64, with sine; sampled positions against the oracle (the same
+    one-ulp bound), the whole output checked for the cat duplicate."""
+    S = 1 << 20
+    inv_cpu, pos_cpu = synthetic.rope_operands(64, S, max_position=32768)
+    inv, pos = inv_cpu.to(DEV), pos_cpu.to(DEV)
+    c, s = lf.rope_cos_sin(inv, pos)
+    torch.cuda.synchronize()
+    assert c.shape == (S, 128) and s.shape == (S, 128)
+    assert torch.equal(c[:, :64], c[:, 64:]) and torch.equal(s[:, :64], s[:, 64:])
+    idx = np.unique(np.concatenate([[0, 1, 32767, 32768, S - 1],
+                                    np.random.default_rng(11).integers(0, S, 4096)]))
+    rc, rs = oracle.rope_cos_sin(inv_cpu, pos_cpu.numpy()[idx])
+    for got, ref in ((bits(c[torch.from_numpy(idx).to(DEV)]), rc), (bits(s[torch.from_numpy(idx).to(DEV)]), rs)):
+        d = np.abs(ordered(got.reshape(ref.shape)) - ordered(ref))
+        assert d.max() <= 1, "more than one bf16 ulp from the oracle"
+        assert (d != 0).mean() <= 1e-3
