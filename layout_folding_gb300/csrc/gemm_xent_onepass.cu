@@ -21,7 +21,10 @@
 // W tiles alternate their order every round so the next round starts on the
 // W rows L2 still holds.  Per round:
 //   1. mainloop of the pair's one or two tiles (same TMA/MMA machinery as the
-//      pair GEMM kernel);
+//      pair GEMM kernel); the first tile of a round is the previous round's
+//      last, and its K blocks are walked downwards, so the first loads find
+//      the slices L2 still holds (the second tiles of a round, ~136 MB at the
+//      bench shape, do not all fit; ascending, almost none hit);
 //   2. epilogue (8 warps; a thread owns a row, warpgroup h takes columns
 //      [128h, 128h + 128) of every tile): per-(row, half tile) statistics
 //      (max, sum exp(z - max), label logit) in one pass over TMEM with a
@@ -492,7 +495,11 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                 for (int i = 0; ok && i < w.ntile; ++i) {
                     const int t = w.swap ? w.ntile - 1 - i : i;
                     const int brow = (w.nb0 + t) * p.op_tile + static_cast<int>(rank) * (p.op_tile / 2);
-                    for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    // a round's first tile is the previous round's last one: walk its K
+                    // blocks downwards, so the first loads find the slices L2 still holds
+                    const bool down = i == 0 && r > 0 && w.ntile == 2;
+                    for (int kk = 0; kk < p.num_k_blocks; ++kk) {
+                        const int kb = down ? p.num_k_blocks - 1 - kk : kk;
                         if (!wait_bar(EMPTY_BAR(stage), phase ^ 1u, abort_flag, p, ERR_PRODUCER, peer_abort)) {
                             ok = false;
                             break;
@@ -539,7 +546,11 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(i * BN);
-                    for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    // a round's first tile is the previous round's last one: walk its K
+                    // blocks downwards, so the first loads find the slices L2 still holds
+                    const bool down = i == 0 && r > 0 && w.ntile == 2;
+                    for (int kk = 0; kk < p.num_k_blocks; ++kk) {
+                        const int kb = down ? p.num_k_blocks - 1 - kk : kk;
                         if (!wait_bar(FULL_BAR(stage), phase, abort_flag, p, ERR_MMA_FULL, peer_abort)) {
                             ok = false;
                             break;
@@ -550,7 +561,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
 #pragma unroll
                         for (int k = 0; k < BK / OP_UMMA_K; ++k)
                             umma_f16_pair(d_tmem, smem_desc_k128(a0 + k * OP_UMMA_K * 2),
-                                          smem_desc_k128(b0 + k * OP_UMMA_K * 2), idesc, (kb | k) != 0 ? 1u : 0u);
+                                          smem_desc_k128(b0 + k * OP_UMMA_K * 2), idesc, (kk | k) != 0 ? 1u : 0u);
                         umma_commit_pair_mc(EMPTY_BAR(stage), 0x3);
                         if (++stage == OP_STAGES) {
                             stage = 0;
