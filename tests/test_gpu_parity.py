@@ -404,3 +404,29 @@ def test_matmul_k1_bandwidth_shape_sampled_bitexact():
     got = out[rows].cpu().numpy()
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
     assert torch.equal(out, ad.reshape(64, 1) * bd)
+
+
+@pytest.mark.parametrize("width", [224, 256])
+def test_xent_onepass_multi_round(width):
+    """Several rounds of the one-pass kernel (M = 1500: 6 row blocks, the last
+    one ragged; N = 16384: at 224 columns 74 tiles, the last 32 wide), so the
+    rounds after the first walk their first tile's K blocks downwards; every
+    row against the oracle."""
+    M, N, K = 1500, 16384, 136
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N, seed=12)
+    lab[0], lab[1], lab[2] = 0, N - 1, 16352
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    lf.set_onepass_tile(width)
+    try:
+        b0 = lf.launch_count()
+        loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        b1 = lf.launch_count()
+        lf.check_device_error()
+    finally:
+        lf.set_onepass_tile(0)
+    assert b1 - b0 == 1
+    rows = list(range(M))
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    assert_loss_close(f64(loss), rloss, "multi-round width %d" % width)
+    assert_grad_close(f64(grad), rgrad, "multi-round width %d" % width)
