@@ -4,11 +4,18 @@
 Headline line (one JSON line on rank 0): TFLOP/s of ``gemm_nt`` on the NT
 projection workload -- X bf16[384,2,13824] viewed [768,13824], W
 bf16[5120,13824] in its stored layout, out bf16[384,2,5120] -- one step = one
-``gemm_nt`` call on inputs resident in HBM, with L2 flushed (a 256 MiB write)
-between steps and each step timed with CUDA events on the launching stream.
-The same line carries the other paths of the metric under "paths": the fused
-GEMM + cross-entropy with gradient (4096x32768x4096), the loss-only
-large-vocabulary case (8192x128256x4096) and the K=1 product (GB/s).
+``gemm_nt`` call on inputs resident in HBM, with L2 flushed (a 256 MiB write,
+then a 256 MiB read) between steps and each step timed with CUDA events on the
+launching stream.  The line also carries ``roofline`` (the headline kernel
+against the measured bf16 peak, with its DRAM traffic from the committed ncu
+capture), ``e2e`` (the same call with host buffers and the copies inside the
+timed region), ``clocks`` and ``cpu_baseline``.  Under "paths": the K=1 product
+(the page's [64,4096] and 2 GiB out), the RoPE segment and the fp8 dual-layout
+cast (bandwidth-bound legs, run first), the fused GEMM + cross-entropy with
+gradient (4096x32768x4096, one pass), the loss-only large-vocabulary case
+(8192x128256x4096) with the unfused comparison, the large-vocabulary gradient
+(two passes), the other operand layouts, batched and strided views, and the
+skinny swapped-operand GEMM.
 
 ``--impl reference`` times the CPU oracle (fp64, plain loops) on a bounded
 sample of the same workload, on this machine's host cores.
