@@ -428,6 +428,24 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
                                         "logits_bytes": wl.M * wl.N * 2,
                                         "fused_speedup": round(ms_u / ms, 3)}
             del logits, lab64
+        if want_grad and name == "xent_grad":
+            # the same gradient with the weight stored [K, N] (read N-major in
+            # place, e.g. a tied embedding used transposed): the two-pass form
+            w_kn = w.t().contiguous()
+
+            def step_kn():
+                lf.gemm_nt_xent(x, w_kn, lab, loss=loss, grad=grad, stream=stream, w_mn=True)
+            times, launches = timer.run(step_kn, steps, 3, counter=lf.launch_count)
+            lf.check_device_error(stream)
+            ms = statistics.mean(times)
+            res["xent_grad_w_stored_kn"] = {"M": wl.M, "N": wl.N, "K": wl.K, "grad": True, "w_stored": "[K,N]",
+                                            "ms": round(ms, 4),
+                                            "tflops_algorithmic": round(flops / ms / 1e9, 1),
+                                            "tflops_executed": round(2 * flops / ms / 1e9, 1),
+                                            "pct_of_peak_algorithmic": round(100 * flops / ms / 1e9 / peak, 1),
+                                            "pct_of_peak_executed": round(100 * 2 * flops / ms / 1e9 / peak, 1),
+                                            "peak": peak, "launches_per_step": launches / steps}
+            del w_kn
         del x, w, lab, loss, grad, inp
         torch.cuda.empty_cache()
     # other operand layouts at the headline shape: W stored [K,N] (the trace's

@@ -187,6 +187,28 @@ lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_
                        int64_t batch, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
+ * gemm_nt_xent_layout -- gemm_nt_xent with either operand in either stored
+ * layout, read in place (no transposed copy).
+ *
+ * Source: as gemm_nt_xent ("Allow reductions in matmul epilogues", NVIDIA/Fuser
+ * issue 2213), whose scheduler canonicalises any operand layout of the matmul
+ * to one contraction; the layouts as in gemm_layout ("Strength reduction: fold
+ * transpose into a subsequent GEMM call", the transposed weight read as is).
+ *
+ *   x_layout : LF_K_MAJOR (x is [M,K]) or LF_MN_MAJOR (x is [K,M], M % 8 == 0)
+ *   w_layout : LF_K_MAJOR (w is [N,K]) or LF_MN_MAJOR (w is [K,N])
+ *   K % 8 == 0 when either operand is K-major; N % 8 == 0 always.
+ *   labels, loss, grad_or_null, M, N, K and the results: as gemm_nt_xent.
+ * Any other layout value: LF_ERR_SHAPE.  With two K-major operands this is
+ * gemm_nt_xent.  Otherwise the work is the two-pass form on CTA pairs (tile
+ * partials + combine, and with grad a recompute pass); the workspace rules of
+ * gemm_nt_xent apply.
+ */
+lf_status gemm_nt_xent_layout(const void *x, int x_layout, const void *w, int w_layout, const int32_t *labels,
+                              float *loss, void *grad_or_null, int64_t M, int64_t N, int64_t K,
+                              cudaStream_t stream);
+
+/*
  * rope_cos_sin -- the RoPE segment around the K=1 matmul, in one kernel.
  *
  * Source: "Feature request: Schedule a small matmul op as a reduction (or

@@ -56,6 +56,8 @@ def lib():
         L.gemm_nt.restype = I32
         L.gemm_nt_xent.argtypes = [P, P, P, P, P, I64, I64, I64, P]
         L.gemm_nt_xent.restype = I32
+        L.gemm_nt_xent_layout.argtypes = [P, I32, P, I32, P, P, P, I64, I64, I64, P]
+        L.gemm_nt_xent_layout.restype = I32
         L.matmul_k1.argtypes = [P, P, P, I64, I64, P]
         L.matmul_k1.restype = I32
         L.fp8_cast_dual.argtypes = [P, P, P, P, I64, I64, P]
@@ -132,17 +134,26 @@ def gemm_nt(x, w, out=None, stream=None):
     return out
 
 
-def gemm_nt_xent(x, w, labels, want_grad=False, loss=None, grad=None, stream=None):
-    """Fused x @ w.T + row-wise cross-entropy.  Returns (loss fp32 [M], grad bf16 [M, N] or None)."""
+def gemm_nt_xent(x, w, labels, want_grad=False, loss=None, grad=None, stream=None, x_mn=False, w_mn=False):
+    """Fused x @ w.T + row-wise cross-entropy.  Returns (loss fp32 [M], grad bf16 [M, N] or None).
+    x is stored [M, K] (any leading dims flattened into M), or [K, M] with x_mn;
+    w is stored [N, K], or [K, N] with w_mn -- read in place either way."""
     import torch
     _require(x, torch.bfloat16, "x")
     _require(w, torch.bfloat16, "w")
     _require(labels, torch.int32, "labels")
-    K = x.shape[-1]
-    N = w.shape[0]
-    if w.dim() != 2 or w.shape[1] != K:
-        raise ValueError("w must be [N, K] with K = x.shape[-1]")
-    M = x.numel() // K
+    if x_mn:
+        if x.dim() != 2:
+            raise ValueError("an [K, M] x must be 2-D")
+        K, M = x.shape
+    else:
+        K = x.shape[-1]
+        M = x.numel() // K
+    if w.dim() != 2:
+        raise ValueError("w must be 2-D")
+    Kw, N = w.shape if w_mn else (w.shape[1], w.shape[0])
+    if Kw != K:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, Kw))
     if labels.numel() != M:
         raise ValueError("labels must have M elements")
     if loss is None:
@@ -154,9 +165,14 @@ def gemm_nt_xent(x, w, labels, want_grad=False, loss=None, grad=None, stream=Non
         _require(grad, torch.bfloat16, "grad")
         if grad.numel() != M * N:
             raise ValueError("grad must be [M, N]")
-    _check(lib().gemm_nt_xent(x.data_ptr(), w.data_ptr(), labels.data_ptr(), loss.data_ptr(),
-                              grad.data_ptr() if grad is not None else None, M, N, K, _stream(stream)),
-           "gemm_nt_xent")
+    gptr = grad.data_ptr() if grad is not None else None
+    if x_mn or w_mn:
+        _check(lib().gemm_nt_xent_layout(x.data_ptr(), LF_MN_MAJOR if x_mn else LF_K_MAJOR, w.data_ptr(),
+                                         LF_MN_MAJOR if w_mn else LF_K_MAJOR, labels.data_ptr(), loss.data_ptr(),
+                                         gptr, M, N, K, _stream(stream)), "gemm_nt_xent_layout")
+    else:
+        _check(lib().gemm_nt_xent(x.data_ptr(), w.data_ptr(), labels.data_ptr(), loss.data_ptr(), gptr, M, N, K,
+                                  _stream(stream)), "gemm_nt_xent")
     return loss, grad
 
 

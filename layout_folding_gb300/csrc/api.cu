@@ -496,8 +496,17 @@ lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_
     return launched(run_gemm(lf::EPI_STORE, g, stream), 1);
 }
 
-lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
-                       int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+// gemm_nt_xent with X stored [M,K] (x_mn false) or [K,M], W stored [N,K]
+// (w_mn false) or [K,N].  Operands in their stored layouts are read in place
+// (MN-major ones through MN-major tensor-core descriptors); the one-pass
+// gradient kernel takes K-major operands only, other layouts use the two-pass
+// form on CTA pairs.
+lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const int32_t *labels, float *loss,
+                    void *grad_or_null, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     if (!x || !w || !labels || !loss)
         return LF_ERR_NULL;
@@ -506,14 +515,18 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
         return st;
     if (K == 1)
         return LF_ERR_SHAPE;
+    // row pitches must be multiples of 16 bytes: K for a K-major operand, M
+    // (resp. N) for an MN-major one
     if (!aligned16(x) || !aligned16(w) || !aligned4(labels) || !aligned4(loss) ||
-        (grad_or_null && !aligned16(grad_or_null)) || N % 8 != 0 || K % 8 != 0)
+        (grad_or_null && !aligned16(grad_or_null)) || N % 8 != 0 || (x_mn && M % 8 != 0) ||
+        ((!x_mn || !w_mn) && K % 8 != 0))
         return LF_ERR_ALIGN;
     DeviceState *d = nullptr;
     if ((st = current_device(&d)) != LF_OK)
         return st;
+    const int layout = (x_mn ? 1 : 0) | (w_mn ? 2 : 0);
     GemmPlan g;
-    if ((st = plan_gemm(d, x, w, M, N, K, &g)) != LF_OK)
+    if ((st = plan_gemm(d, x, w, M, N, K, &g, layout)) != LF_OK)
         return st;
     lf::GemmParams &p = g.p;
     // workspace: part_max, part_sum [M, NB]; label_logit, row_max, row_logsum [M]
@@ -540,7 +553,7 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
     int op_tile = 0;
     long long best = 0;
     const int forced = g_op_tile.load();
-    for (int wdt = 256; wdt >= 128 && grad_or_null && g.pair; wdt -= 32) {
+    for (int wdt = 256; wdt >= 128 && grad_or_null && g.pair && layout == 0; wdt -= 32) {
         if (forced && wdt != forced)
             continue;
         const int nt = static_cast<int>((N + wdt - 1) / wdt);
@@ -595,6 +608,25 @@ lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, floa
     p.row_logsum = row_logsum;
     p.inject = 0;
     return launched(run_gemm(lf::EPI_XENT_GRAD, g, stream), 1);
+}
+
+}  // namespace
+
+extern "C" {
+
+lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
+                       int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    return xent_impl(x, false, w, false, labels, loss, grad_or_null, M, N, K, stream);
+}
+
+lf_status gemm_nt_xent_layout(const void *x, int x_layout, const void *w, int w_layout, const int32_t *labels,
+                              float *loss, void *grad_or_null, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    if ((x_layout != LF_K_MAJOR && x_layout != LF_MN_MAJOR) || (w_layout != LF_K_MAJOR && w_layout != LF_MN_MAJOR))
+        return LF_ERR_SHAPE;
+    return xent_impl(x, x_layout == LF_MN_MAJOR, w, w_layout == LF_MN_MAJOR, labels, loss, grad_or_null, M, N, K,
+                     stream);
 }
 
 lf_status matmul_k1(const float *a, const float *b, float *out, int64_t M, int64_t N, cudaStream_t stream)

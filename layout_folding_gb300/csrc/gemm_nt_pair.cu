@@ -867,7 +867,31 @@ int gemm_pair_max_active_clusters()
 cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, const CUtensorMap &tb,
                                 const CUtensorMap &to, const GemmParams &p, int grid, cudaStream_t s)
 {
-    if (layout != 0) {  // other operand layouts: plain store epilogue only
+    if (layout != 0 && epi == EPI_XENT_PARTIAL) {  // the cross-entropy epilogues: layouts 1..3
+        switch (layout) {
+        case 1:
+            return launch_pair_t<EPI_XENT_PARTIAL, 1>(ta, tb, to, p, grid, s);
+        case 2:
+            return launch_pair_t<EPI_XENT_PARTIAL, 2>(ta, tb, to, p, grid, s);
+        case 3:
+            return launch_pair_t<EPI_XENT_PARTIAL, 3>(ta, tb, to, p, grid, s);
+        default:
+            return cudaErrorInvalidValue;
+        }
+    }
+    if (layout != 0 && epi == EPI_XENT_GRAD) {
+        switch (layout) {
+        case 1:
+            return launch_pair_t<EPI_XENT_GRAD, 1>(ta, tb, to, p, grid, s);
+        case 2:
+            return launch_pair_t<EPI_XENT_GRAD, 2>(ta, tb, to, p, grid, s);
+        case 3:
+            return launch_pair_t<EPI_XENT_GRAD, 3>(ta, tb, to, p, grid, s);
+        default:
+            return cudaErrorInvalidValue;
+        }
+    }
+    if (layout != 0) {  // other operand layouts, plain store epilogue (batched: bit 2)
         if (epi != EPI_STORE)
             return cudaErrorInvalidValue;
         switch (layout) {

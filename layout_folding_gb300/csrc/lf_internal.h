@@ -76,7 +76,8 @@ int gemm_smem_bytes();
 // [K rows, M columns], 64x64 boxes), else [M,K] (64-column x 128-row boxes);
 // bit 1: W stored [K,N] likewise, else [N,K]; bit 2: batched (3-D tensor
 // maps, batch outermost; p.batch, p.w_batched, p.ldo, p.stride_o).  Layouts
-// other than 0 support the EPI_STORE epilogue only.  `to`: the output as a
+// 1..3 take the EPI_STORE and cross-entropy epilogues, batched layouts
+// EPI_STORE only.  `to`: the output as a
 // bf16 tensor map (2-D [M rows, N columns], row pitch p.ldo; 3-D with the
 // batch outermost when batched), 32 x 32 boxes, 64-byte swizzle -- read only
 // when p.tma_store is set.

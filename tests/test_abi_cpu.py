@@ -12,7 +12,8 @@ from layout_folding_gb300 import build as lfbuild
 
 EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
             "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
-            "fp8_cast_dual", "rope_cos_sin", "gemm_layout", "lf_set_onepass_tile", "gemm_batched"}
+            "fp8_cast_dual", "rope_cos_sin", "gemm_layout", "lf_set_onepass_tile", "gemm_batched",
+            "gemm_nt_xent_layout"}
 
 
 @pytest.fixture(scope="module")
@@ -112,6 +113,21 @@ def test_gemm_layout_rejects_on_host(L):
     assert L.gemm_layout(P(A16), 1, P(A16), 1, P(A16), 8, 12, 8, None) == 3    # N % 8
     assert L.gemm_layout(P(A16 + 8), 1, P(A16), 1, P(A16), 8, 8, 8, None) == 3
     assert L.gemm_layout(P(A16), 1, P(A16), 1, P(A16), 0, 8, 8, None) == 2
+
+
+def test_gemm_nt_xent_layout_rejects_on_host(L):
+    L.gemm_nt_xent_layout.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, P, P] + [ctypes.c_int64] * 3 + [P]
+    f = L.gemm_nt_xent_layout
+    assert f(None, 0, P(A16), 0, P(A16), P(A16), None, 8, 8, 8, None) == 1
+    assert f(P(A16), 0, P(A16), 0, P(A16), None, None, 8, 8, 8, None) == 1      # loss is required
+    assert f(P(A16), 2, P(A16), 0, P(A16), P(A16), None, 8, 8, 8, None) == 2     # no such layout
+    assert f(P(A16), 0, P(A16), 3, P(A16), P(A16), None, 8, 8, 8, None) == 2
+    assert f(P(A16), 1, P(A16), 1, P(A16), P(A16), None, 8, 8, 1, None) == 2     # K = 1
+    assert f(P(A16), 1, P(A16), 0, P(A16), P(A16), None, 12, 8, 8, None) == 3    # X [K,M] pitch M*2
+    assert f(P(A16), 0, P(A16), 1, P(A16), P(A16), None, 8, 8, 12, None) == 3    # X [M,K] pitch K*2
+    assert f(P(A16), 1, P(A16), 1, P(A16), P(A16), None, 8, 12, 8, None) == 3    # N % 8
+    assert f(P(A16), 1, P(A16), 1, P(A16), P(A16), P(A16 + 8), 8, 8, 8, None) == 3  # grad alignment
+    assert f(P(A16), 1, P(A16), 1, P(A16), P(A16), None, 0, 8, 8, None) == 2
 
 
 def test_gemm_batched_rejects_on_host(L):

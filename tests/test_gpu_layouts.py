@@ -125,3 +125,69 @@ def test_invalid_layout_and_alignment_raise():
     w = torch.zeros(16, 16, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(lf.LayoutFoldError):
         lf.gemm_layout(x, w, x_mn=True, w_mn=True)
+
+
+@pytest.mark.parametrize("x_mn,w_mn", LAYOUTS)
+@pytest.mark.parametrize("M,N,K", [(600, 1032, 264), (256, 2048, 128), (520, 776, 136)])
+def test_xent_layouts_match_oracle(M, N, K, x_mn, w_mn):
+    """gemm_nt_xent with X stored [K,M] and/or W stored [K,N] (read in place):
+    loss (rel 1e-3) and gradient (abs 2e-3) of every row against the oracle
+    on the logical operands, with labels on tile edges."""
+    x = synthetic.bf16_normal((M, K), 1.0, 41)
+    w = synthetic.bf16_normal((N, K), 1.0 / np.sqrt(K), 42)
+    lab = synthetic.labels_uniform(M, N, seed=43)
+    lab[0], lab[1], lab[2], lab[3] = 0, N - 1, min(255, N - 1), min(256, N - 1)
+    xs, ws = stored(x, w, x_mn, w_mn)
+    ld = lab.to(DEV)
+    n0 = lf.launch_count()
+    loss, grad = lf.gemm_nt_xent(xs, ws, ld, want_grad=True, x_mn=x_mn, w_mn=w_mn)
+    n1 = lf.launch_count()
+    loss_only, none = lf.gemm_nt_xent(xs, ws, ld, x_mn=x_mn, w_mn=w_mn)
+    torch.cuda.synchronize()
+    lf.check_device_error()
+    assert none is None
+    assert n1 - n0 == 3          # partials, combine, recompute pass
+    rows = list(range(M))
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    for got in (loss, loss_only):
+        rel = np.abs(f64(got) - rloss) / np.abs(rloss)
+        assert rel.max() <= 1e-3, rel.max()
+    assert np.abs(f64(grad) - rgrad).max() <= 2e-3
+
+
+def test_xent_layout_k_major_is_gemm_nt_xent():
+    """Two K-major operands through the layout entry point are gemm_nt_xent
+    itself (the one-pass kernel: one launch), bit for bit."""
+    M, N, K = 512, 4096, 256
+    x = synthetic.bf16_normal((M, K), 1.0, 44).to(DEV)
+    w = synthetic.bf16_normal((N, K), 1.0 / 16, 45).to(DEV)
+    lab = synthetic.labels_uniform(M, N, seed=46).to(DEV)
+    loss_a, grad_a = lf.gemm_nt_xent(x, w, lab, want_grad=True)
+    lib = lf.lib()
+    loss_b = torch.empty_like(loss_a)
+    grad_b = torch.empty_like(grad_a)
+    n0 = lf.launch_count()
+    assert lib.gemm_nt_xent_layout(x.data_ptr(), lf.LF_K_MAJOR, w.data_ptr(), lf.LF_K_MAJOR, lab.data_ptr(),
+                                   loss_b.data_ptr(), grad_b.data_ptr(), M, N, K,
+                                   torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert lf.launch_count() - n0 == 1
+    assert torch.equal(loss_a, loss_b) and torch.equal(grad_a, grad_b)
+
+
+def test_xent_layout_large_vocab_w_stored_kn_sampled():
+    """The LM-head shape with the weight stored [K, N] (as a tied embedding
+    read transposed): 4096 x 32768 x 4096, sampled rows, every column."""
+    M, N, K = 4096, 32768, 4096
+    x = synthetic.bf16_normal((M, K), 1.0, 47)
+    w = synthetic.bf16_normal((N, K), 1.0 / 64, 48)
+    lab = synthetic.labels_uniform(M, N, seed=49)
+    xs, ws = stored(x, w, False, True)
+    loss, grad = lf.gemm_nt_xent(xs, ws, lab.to(DEV), want_grad=True, w_mn=True)
+    torch.cuda.synchronize()
+    lf.check_device_error()
+    rows = [0, 1, 255, 256, 2047, 4095]
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    rel = np.abs(f64(loss)[rows] - rloss) / np.abs(rloss)
+    assert rel.max() <= 1e-3, rel.max()
+    assert np.abs(f64(grad)[rows] - rgrad).max() <= 2e-3
