@@ -200,9 +200,9 @@ lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_
  *   K % 8 == 0 when either operand is K-major; N % 8 == 0 always.
  *   labels, loss, grad_or_null, M, N, K and the results: as gemm_nt_xent.
  * Any other layout value: LF_ERR_SHAPE.  With two K-major operands this is
- * gemm_nt_xent.  Otherwise the work is the two-pass form on CTA pairs (tile
- * partials + combine, and with grad a recompute pass); the workspace rules of
- * gemm_nt_xent apply.
+ * gemm_nt_xent.  The work is that of gemm_nt_xent in every layout (with grad
+ * one launch when a row block of tiles fits the resident CTA pairs; with an
+ * N-major W its N tiles are 128 or 256 wide), and its workspace rules apply.
  */
 lf_status gemm_nt_xent_layout(const void *x, int x_layout, const void *w, int w_layout, const int32_t *labels,
                               float *loss, void *grad_or_null, int64_t M, int64_t N, int64_t K,

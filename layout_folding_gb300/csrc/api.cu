@@ -502,9 +502,9 @@ namespace {
 
 // gemm_nt_xent with X stored [M,K] (x_mn false) or [K,M], W stored [N,K]
 // (w_mn false) or [K,N].  Operands in their stored layouts are read in place
-// (MN-major ones through MN-major tensor-core descriptors); the one-pass
-// gradient kernel takes K-major operands only, other layouts use the two-pass
-// form on CTA pairs.
+// (MN-major ones through MN-major tensor-core descriptors), by the one-pass
+// gradient kernel as by the two-pass form; with an N-major W the one-pass
+// N-tile width is 128 or 256.
 lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const int32_t *labels, float *loss,
                     void *grad_or_null, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
@@ -553,8 +553,10 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
     int op_tile = 0;
     long long best = 0;
     const int forced = g_op_tile.load();
-    for (int wdt = 256; wdt >= 128 && grad_or_null && g.pair && layout == 0; wdt -= 32) {
+    for (int wdt = 256; wdt >= 128 && grad_or_null && g.pair; wdt -= 32) {
         if (forced && wdt != forced)
+            continue;
+        if (w_mn && wdt != 256 && wdt != 128)  // an N-major W arrives in 64-row boxes per CTA half tile
             continue;
         const int nt = static_cast<int>((N + wdt - 1) / wdt);
         const int q = (nt + 1) / 2;
@@ -573,9 +575,9 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
     if (op_tile > 0) {
         if ((st = ensure_onepass_flags(d)) != LF_OK)
             return st;
-        CUtensorMap tb_op;  // W in boxes of op_tile / 2 rows (each CTA's half of a tile)
-        if (!make_tmap(&tb_op, w, N, K, static_cast<uint32_t>(op_tile / 2)))
-            return LF_ERR_LAUNCH;
+        CUtensorMap tb_op = g.tb;  // an N-major W: the plan's 64 x 64 boxes
+        if (!w_mn && !make_tmap(&tb_op, w, N, K, static_cast<uint32_t>(op_tile / 2)))
+            return LF_ERR_LAUNCH;  // a K-major W: boxes of op_tile / 2 rows (each CTA's half of a tile)
         p.streamk = 0;
         p.op_tile = op_tile;
         p.op_ntiles = static_cast<int>((N + op_tile - 1) / op_tile);
@@ -592,7 +594,7 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
         CUtensorMap to;  // the gradient, written by TMA stores
         if (!make_tmap_out(&to, grad_or_null, M, N, N, 1, M * N, false))
             return LF_ERR_LAUNCH;
-        return launched(lf::launch_xent_onepass(g.ta, tb_op, to, p, 2 * p.op_k * p.op_Q, stream), 1);
+        return launched(lf::launch_xent_onepass(layout, g.ta, tb_op, to, p, 2 * p.op_k * p.op_Q, stream), 1);
     }
     if ((st = launched(run_gemm(lf::EPI_XENT_PARTIAL, g, stream), 1)) != LF_OK)
         return st;

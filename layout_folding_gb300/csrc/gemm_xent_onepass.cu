@@ -11,6 +11,10 @@
 // a row of tiles has to be resident at once so the result can be broadcast
 // back.  That is what this kernel does, one 256-row block of rows at a time.
 //
+// Operand layouts (template LAYOUT, as in the pair GEMM kernel): bit 0 X stored
+// [K,M], bit 1 W stored [K,N] -- loaded as 64 x 64 boxes and read through
+// MN-major descriptors, never transposed in memory.
+//
 // Schedule: CTA pairs (tcgen05 cta_group::2, M=256 x N=op_tile MMAs; op_tile
 // is 256, or 128..224 for problems that fit one round of pairs) form groups of
 // Q = ceil(N_tiles / 2) pairs; pair qi of a group owns N tiles 2qi and 2qi+1
@@ -77,6 +81,11 @@ constexpr int OP_STG_OFF =
     ((OP_STAGES * OP_STAGE_BYTES + OP_NUM_BARS * 8 + 16 + OP_XCH_BYTES + 1023) / 1024) * 1024;
 constexpr int OP_SMEM_BYTES = 1024 + OP_STG_OFF + 2 * OP_EPI_WARPS * OP_STG_WARP_BYTES;
 constexpr uint64_t OP_ABORT_SETTLE_NS = 100000;
+// MN-major operands (LAYOUT bit 0: X stored [K,M]; bit 1: W stored [K,N]) arrive
+// as 64 (M or N) x 64 (K) boxes per K slice, the next box 8 KiB further; each
+// K=16 step of the MMA advances two 1024-byte atoms.
+constexpr uint32_t OP_MN_BOX = 8192;
+constexpr uint32_t OP_MN_KSTEP = 2 * 1024;
 constexpr int ERR_OP_FLAG = 0x108;  // a group member never published its partials
 
 // L2 eviction policy: lines written with it are evicted after other lines.
@@ -411,6 +420,7 @@ __device__ __noinline__ bool wait_flag64(const unsigned long long *flag, unsigne
     }
 }
 
+template <int LAYOUT>
 __global__ void __launch_bounds__(OP_THREADS, 1)
     k_xent_onepass(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, const GemmParams p)
@@ -512,8 +522,20 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                                 mbar_arrive_expect_tx(FULL_BAR(stage), stage_tx);
                                 ++armed[stage];
                             }
-                            tma_load_2d_pair(sA + stage * OP_A_BYTES, &tmA, kb * BK, arow, full_leader);
-                            tma_load_2d_pair(sB + stage * OP_B_BYTES, &tmB, kb * BK, brow, full_leader);
+                            const uint32_t a_dst = sA + stage * OP_A_BYTES, b_dst = sB + stage * OP_B_BYTES;
+                            if (LAYOUT & 1) {
+                                tma_load_2d_pair(a_dst, &tmA, arow, kb * BK, full_leader);
+                                tma_load_2d_pair(a_dst + OP_MN_BOX, &tmA, arow + 64, kb * BK, full_leader);
+                            } else {
+                                tma_load_2d_pair(a_dst, &tmA, kb * BK, arow, full_leader);
+                            }
+                            if (LAYOUT & 2) {  // op_tile / 2 = 64 or 128 rows: one or two boxes
+                                for (int bx = 0; bx < p.op_tile / 128; ++bx)
+                                    tma_load_2d_pair(b_dst + bx * OP_MN_BOX, &tmB, brow + 64 * bx, kb * BK,
+                                                     full_leader);
+                            } else {
+                                tma_load_2d_pair(b_dst, &tmB, kb * BK, brow, full_leader);
+                            }
                         }
                         if (++stage == OP_STAGES) {
                             stage = 0;
@@ -534,7 +556,8 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t tph[2] = {0u, 0u};
-            const uint32_t idesc = idesc_bf16_f32(OP_M, static_cast<uint32_t>(p.op_tile));
+            const uint32_t idesc =
+                idesc_bf16_f32_major(OP_M, static_cast<uint32_t>(p.op_tile), (LAYOUT & 1) != 0, (LAYOUT & 2) != 0);
             bool ok = true;
             OpWork w;
             for (int r = 0; ok && r < p.op_rounds && op_work(p, pair, r, w); ++r) {
@@ -546,11 +569,9 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(i * BN);
-                    // a round's first tile is the previous round's last one: walk its K
-                    // blocks downwards, so the first loads find the slices L2 still holds
-                    const bool down = i == 0 && r > 0 && w.ntile == 2;
+                    // the stages arrive in the producer's K order (downwards for a
+                    // round's first tile); the first one starts the accumulation
                     for (int kk = 0; kk < p.num_k_blocks; ++kk) {
-                        const int kb = down ? p.num_k_blocks - 1 - kk : kk;
                         if (!wait_bar(FULL_BAR(stage), phase, abort_flag, p, ERR_MMA_FULL, peer_abort)) {
                             ok = false;
                             break;
@@ -560,8 +581,12 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
                         const uint32_t b0 = sB + stage * OP_B_BYTES;
 #pragma unroll
                         for (int k = 0; k < BK / OP_UMMA_K; ++k)
-                            umma_f16_pair(d_tmem, smem_desc_k128(a0 + k * OP_UMMA_K * 2),
-                                          smem_desc_k128(b0 + k * OP_UMMA_K * 2), idesc, (kk | k) != 0 ? 1u : 0u);
+                            umma_f16_pair(d_tmem,
+                                          (LAYOUT & 1) ? smem_desc_mn128(a0 + k * OP_MN_KSTEP, OP_MN_BOX)
+                                                       : smem_desc_k128(a0 + k * OP_UMMA_K * 2),
+                                          (LAYOUT & 2) ? smem_desc_mn128(b0 + k * OP_MN_KSTEP, OP_MN_BOX)
+                                                       : smem_desc_k128(b0 + k * OP_UMMA_K * 2),
+                                          idesc, (kk | k) != 0 ? 1u : 0u);
                         umma_commit_pair_mc(EMPTY_BAR(stage), 0x3);
                         if (++stage == OP_STAGES) {
                             stage = 0;
@@ -773,6 +798,7 @@ __global__ void __launch_bounds__(OP_THREADS, 1)
     }
 }
 
+template <int LAYOUT>
 cudaError_t set_onepass_smem_attr_once()
 {
     static std::atomic<unsigned long long> done{0};
@@ -783,18 +809,17 @@ cudaError_t set_onepass_smem_attr_once()
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load() & bit)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(k_xent_onepass, cudaFuncAttributeMaxDynamicSharedMemorySize, OP_SMEM_BYTES);
+    e = cudaFuncSetAttribute(k_xent_onepass<LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, OP_SMEM_BYTES);
     if (e == cudaSuccess)
         done.fetch_or(bit);
     return e;
 }
 
-}  // namespace
-
-cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
-                                const GemmParams &p, int grid, cudaStream_t s)
+template <int LAYOUT>
+cudaError_t launch_onepass_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to, const GemmParams &p,
+                             int grid, cudaStream_t s)
 {
-    cudaError_t e = set_onepass_smem_attr_once();
+    cudaError_t e = set_onepass_smem_attr_once<LAYOUT>();
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -809,7 +834,26 @@ cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, co
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_xent_onepass, ta, tb, to, p);
+    return cudaLaunchKernelEx(&cfg, k_xent_onepass<LAYOUT>, ta, tb, to, p);
+}
+
+}  // namespace
+
+cudaError_t launch_xent_onepass(int layout, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
+                                const GemmParams &p, int grid, cudaStream_t s)
+{
+    switch (layout) {
+    case 0:
+        return launch_onepass_t<0>(ta, tb, to, p, grid, s);
+    case 1:
+        return launch_onepass_t<1>(ta, tb, to, p, grid, s);
+    case 2:
+        return launch_onepass_t<2>(ta, tb, to, p, grid, s);
+    case 3:
+        return launch_onepass_t<3>(ta, tb, to, p, grid, s);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace lf

@@ -89,7 +89,10 @@ int gemm_pair_max_active_clusters();
 // One-pass GEMM + cross-entropy + gradient on CTA pairs (no recompute GEMM,
 // no combine kernel).  Requires op_k * op_Q co-resident pairs; grid = 2 * op_k * op_Q.
 // `to`: the gradient (p.out) as a 2-D bf16 map, 32 x 32 boxes, 64-byte swizzle.
-cudaError_t launch_xent_onepass(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
+// layout bit 0: X stored [K,M] (ta as for the pair kernel: 64 x 64 boxes); bit
+// 1: W stored [K,N] (tb with 64 x 64 boxes; op_tile 128 or 256), else tb's box
+// is op_tile / 2 rows of W [N,K].
+cudaError_t launch_xent_onepass(int layout, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to,
                                 const GemmParams &p, int grid, cudaStream_t s);
 
 cudaError_t launch_xent_combine(const float *part_max, const float *part_sum, const float *label_logit,

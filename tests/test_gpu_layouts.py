@@ -130,9 +130,10 @@ def test_invalid_layout_and_alignment_raise():
 @pytest.mark.parametrize("x_mn,w_mn", LAYOUTS)
 @pytest.mark.parametrize("M,N,K", [(600, 1032, 264), (256, 2048, 128), (520, 776, 136)])
 def test_xent_layouts_match_oracle(M, N, K, x_mn, w_mn):
-    """gemm_nt_xent with X stored [K,M] and/or W stored [K,N] (read in place):
-    loss (rel 1e-3) and gradient (abs 2e-3) of every row against the oracle
-    on the logical operands, with labels on tile edges."""
+    """gemm_nt_xent with X stored [K,M] and/or W stored [K,N] (read in place),
+    the gradient by the one-pass kernel: loss (rel 1e-3) and gradient (abs
+    2e-3) of every row against the oracle on the logical operands, with labels
+    on tile edges."""
     x = synthetic.bf16_normal((M, K), 1.0, 41)
     w = synthetic.bf16_normal((N, K), 1.0 / np.sqrt(K), 42)
     lab = synthetic.labels_uniform(M, N, seed=43)
@@ -146,7 +147,7 @@ def test_xent_layouts_match_oracle(M, N, K, x_mn, w_mn):
     torch.cuda.synchronize()
     lf.check_device_error()
     assert none is None
-    assert n1 - n0 == 3          # partials, combine, recompute pass
+    assert n1 - n0 == 1          # the one-pass kernel
     rows = list(range(M))
     _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
     for got in (loss, loss_only):
@@ -191,3 +192,47 @@ def test_xent_layout_large_vocab_w_stored_kn_sampled():
     rel = np.abs(f64(loss)[rows] - rloss) / np.abs(rloss)
     assert rel.max() <= 1e-3, rel.max()
     assert np.abs(f64(grad)[rows] - rgrad).max() <= 2e-3
+
+
+@pytest.mark.parametrize("x_mn,w_mn", LAYOUTS)
+def test_xent_layouts_two_pass_wide_vocab(x_mn, w_mn):
+    """A vocabulary too wide for one pass (N = 40992) with the operands in
+    other layouts: partials, combine and the recompute pass, all reading the
+    stored layouts; sampled rows, every column, against the oracle."""
+    M, N, K = 256, 40992, 136
+    x = synthetic.bf16_normal((M, K), 1.0, 50)
+    w = synthetic.bf16_normal((N, K), 1.0 / np.sqrt(K), 51)
+    lab = synthetic.labels_uniform(M, N, seed=52)
+    lab[0], lab[1] = 0, N - 1
+    xs, ws = stored(x, w, x_mn, w_mn)
+    n0 = lf.launch_count()
+    loss, grad = lf.gemm_nt_xent(xs, ws, lab.to(DEV), want_grad=True, x_mn=x_mn, w_mn=w_mn)
+    torch.cuda.synchronize()
+    lf.check_device_error()
+    assert lf.launch_count() - n0 == 3
+    rows = [0, 1, 127, 128, 255]
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    rel = np.abs(f64(loss)[rows] - rloss) / np.abs(rloss)
+    assert rel.max() <= 1e-3, rel.max()
+    assert np.abs(f64(grad)[rows] - rgrad).max() <= 2e-3
+
+
+@pytest.mark.parametrize("x_mn,w_mn", LAYOUTS)
+def test_xent_layouts_one_pass_multi_round(x_mn, w_mn):
+    """Several rounds of the one-pass kernel with MN-major operands (M = 1536:
+    6 row blocks; N = 16384 at 256- or 224-wide tiles), every row."""
+    M, N, K = 1536, 16384, 136
+    x = synthetic.bf16_normal((M, K), 1.0, 53)
+    w = synthetic.bf16_normal((N, K), 1.0 / np.sqrt(K), 54)
+    lab = synthetic.labels_uniform(M, N, seed=55)
+    xs, ws = stored(x, w, x_mn, w_mn)
+    n0 = lf.launch_count()
+    loss, grad = lf.gemm_nt_xent(xs, ws, lab.to(DEV), want_grad=True, x_mn=x_mn, w_mn=w_mn)
+    torch.cuda.synchronize()
+    lf.check_device_error()
+    assert lf.launch_count() - n0 == 1
+    rows = list(range(M))
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    rel = np.abs(f64(loss) - rloss) / np.abs(rloss)
+    assert rel.max() <= 1e-3, rel.max()
+    assert np.abs(f64(grad) - rgrad).max() <= 2e-3
