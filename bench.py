@@ -15,7 +15,9 @@ cast (bandwidth-bound legs, run first), the fused GEMM + cross-entropy with
 gradient (4096x32768x4096, one pass), the loss-only large-vocabulary case
 (8192x128256x4096) with the unfused comparison, the large-vocabulary gradient
 (two passes), the other operand layouts, batched and strided views, and the
-skinny swapped-operand GEMM.
+skinny swapped-operand GEMM.  Under "paths.library": the same workloads computed
+by PyTorch's own GPU operators (cuBLAS matmuls, eager elementwise kernels),
+timed the same way, with the ratio of their time to this library's.
 
 ``--impl reference`` times the CPU oracle (fp64, plain loops) on a bounded
 sample of the same workload, on this machine's host cores.
@@ -277,6 +279,17 @@ def run_ours(args, rank, world, local_rank):
     paths = {}
     if not args.headline_only:
         paths = secondary_paths(args, torch, lf, synthetic, timer, stream, peaks)
+        lib = paths.get("library")
+        if lib:
+            # time of PyTorch's operators / time of this library's, per workload
+            ours = {"gemm_nt_projection": kernel_ms, "gemm_skinny_m64": paths.get("skinny_m64", {}).get("ms"),
+                    "xent_grad": paths.get("xent_grad", {}).get("ms"),
+                    "k1_scaled": paths.get("k1_scaled", {}).get("ms"),
+                    "rope_scaled": paths.get("rope_scaled", {}).get("ms"),
+                    "fp8_cast_scaled": paths.get("fp8_cast_scaled", {}).get("ms")}
+            for k, v in lib.items():
+                if ours.get(k):
+                    v["speedup_of_this_library"] = round(v["ms"] / ours[k], 3)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -509,6 +522,111 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
         del xd, wd, outb, xpad, xs64, outs
         del out, inp
         torch.cuda.empty_cache()
+    if "library" in want:
+        res["library"] = library_paths(torch, synthetic, timer, stream, peaks, steps)
+    torch.cuda.empty_cache()
+    return res
+
+
+def library_paths(torch, synthetic, timer, stream, peaks, steps):
+    """The same workloads computed by PyTorch's own GPU operators (cuBLAS for
+    the matmuls, eager elementwise and reduction kernels for the rest), timed
+    the same way: context for the kernels above, not part of this library."""
+    res = {}
+    F = torch.nn.functional
+
+    def timed(fn):
+        def in_stream():
+            with torch.cuda.stream(stream):
+                fn()
+        return statistics.median(timer.run(in_stream, max(steps, 10), 3))
+
+    # the headline GEMM and its skinny (64-row) form through torch.mm
+    wl = synthetic.WORKLOADS["nt_projection"]
+    inp = synthetic.make_workload("nt_projection")
+    x = inp["x"].reshape(wl.M, wl.K).to("cuda")
+    w = inp["w"].to("cuda")
+    out = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+    ms = timed(lambda: torch.mm(x, w.t(), out=out))
+    flops = 2.0 * wl.M * wl.N * wl.K
+    res["gemm_nt_projection"] = {"M": wl.M, "N": wl.N, "K": wl.K, "what": "torch.mm(x, w.t()) (cuBLAS)",
+                                 "ms": round(ms, 5), "tflops": round(flops / ms / 1e9, 1),
+                                 "pct_of_peak": round(100 * flops / ms / 1e9 / peaks["bf16_tflops"], 1)}
+    x64 = x[:64].contiguous()
+    out64 = torch.empty(64, wl.N, dtype=torch.bfloat16, device="cuda")
+    ms = timed(lambda: torch.mm(x64, w.t(), out=out64))
+    wbytes = wl.N * wl.K * 2
+    res["gemm_skinny_m64"] = {"M": 64, "N": wl.N, "K": wl.K, "what": "torch.mm(x[:64], w.t()) (cuBLAS)",
+                              "ms": round(ms, 5), "w_stream_GB/s": round(wbytes / ms / 1e6, 1),
+                              "pct_of_hbm": round(100 * wbytes / ms / 1e6 / peaks["hbm_gbs"], 1)}
+    del x, w, out, x64, out64, inp
+    torch.cuda.empty_cache()
+
+    # cross-entropy loss and logit gradient, unfused: cuBLAS logits in bf16,
+    # then log-sum-exp, the label logit and softmax minus the one-hot label
+    wl = synthetic.WORKLOADS["xent_grad"]
+    inp = synthetic.make_workload("xent_grad")
+    x, w = inp["x"].to("cuda"), inp["w"].to("cuda")
+    lab = inp["labels"].to("cuda").long()
+    logits = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+    rows = torch.arange(wl.M, device="cuda")
+
+    def xent_grad():
+        torch.mm(x, w.t(), out=logits)
+        z = logits.float()
+        lse = torch.logsumexp(z, dim=1)
+        loss = lse - z[rows, lab]
+        g = torch.exp(z - lse[:, None])
+        g[rows, lab] -= 1.0
+        return loss, g.to(torch.bfloat16)
+    ms = timed(xent_grad)
+    flops = 2.0 * wl.M * wl.N * wl.K
+    res["xent_grad"] = {"M": wl.M, "N": wl.N, "K": wl.K,
+                        "what": "torch.mm to bf16 logits, logsumexp, exp(z - lse) minus one-hot, cast to bf16",
+                        "ms": round(ms, 4), "tflops_algorithmic": round(flops / ms / 1e9, 1)}
+    del x, w, lab, logits, rows, inp
+    torch.cuda.empty_cache()
+
+    # the K=1 product through torch.mm, at the bandwidth size
+    a = torch.randn(64, 1, device="cuda")
+    b = torch.arange(1 << 23, dtype=torch.float32, device="cuda").reshape(1, -1)
+    o = torch.empty(64, 1 << 23, dtype=torch.float32, device="cuda")
+    ms = timed(lambda: torch.mm(a, b, out=o))
+    nbytes = (64 + (1 << 23) + 64 * (1 << 23)) * 4
+    res["k1_scaled"] = {"M": 64, "N": 1 << 23, "what": "torch.mm([64,1], [1,N]) fp32", "ms": round(ms, 5),
+                        "GB/s": round(nbytes / ms / 1e6, 1),
+                        "pct_of_hbm": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1)}
+    del a, b, o
+    torch.cuda.empty_cache()
+
+    # RoPE cos/sin in eager PyTorch: outer product, concatenation, cos, sin, casts
+    inv, pos = synthetic.rope_operands(64, 1 << 20, max_position=32768)
+    inv, pos = inv.to("cuda"), pos.to("cuda")
+
+    def rope():
+        f = pos.float()[:, None] * inv[None, :]
+        emb = torch.cat((f, f), dim=-1)
+        return emb.cos().to(torch.bfloat16), emb.sin().to(torch.bfloat16)
+    ms = timed(rope)
+    S = 1 << 20
+    nbytes = 64 * 2 + S * 8 + 2 * S * 128 * 2
+    res["rope_scaled"] = {"H": 64, "S": S, "what": "eager outer product, cat, cos, sin, bf16 casts",
+                          "ms": round(ms, 5), "GB/s_algorithmic": round(nbytes / ms / 1e6, 1)}
+    del inv, pos
+    torch.cuda.empty_cache()
+
+    # the fp8 cast in both layouts, eager: scale, clamp, cast, then a transposed copy
+    xs = synthetic.bf16_normal((16384, 16384), 1.0, 15).to("cuda")
+    scale = torch.tensor([10.0], dtype=torch.float32, device="cuda")
+
+    def fp8():
+        q = (xs.float() * scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+        return q, q.t().contiguous()
+    ms = timed(fp8)
+    nbytes = 16384 * 16384 * 4
+    res["fp8_cast_scaled"] = {"M": 16384, "K": 16384, "what": "eager scale, clamp, cast, transposed copy",
+                              "ms": round(ms, 5), "GB/s_algorithmic": round(nbytes / ms / 1e6, 1)}
+    del xs, scale
     torch.cuda.empty_cache()
     return res
 
@@ -590,8 +708,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true", help="skip every secondary path")
-    ap.add_argument("--paths", default="xent,k1,layouts,rope,fp8",
-                    help="secondary paths to time after the headline (comma list of xent, k1, layouts, rope, fp8)")
+    ap.add_argument("--paths", default="xent,k1,layouts,rope,fp8,library",
+                    help="secondary paths to time after the headline (comma list of xent, k1, layouts, rope, fp8, "
+                         "library)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     args = ap.parse_args(argv)
