@@ -61,7 +61,8 @@ typedef enum {
  * One kernel launch per call.  A skinny X (M <= 128) with few output tiles is
  * computed with the operands swapped (out^T = W . X^T on the tensor cores,
  * stored transposed).  When the output has too few 256x256 tiles to
- * keep every SM busy, the launch splits the K loop across SMs (stream-K) and
+ * keep every SM busy and K is long enough for the split to pay, the launch
+ * splits the K loop across SMs (stream-K) and
  * uses a library-owned per-device workspace (about 20 MB, allocated on first
  * such call); calls on one device must then not run concurrently on
  * different streams.
@@ -337,8 +338,9 @@ lf_status lf_device_query(int *num_sms, int *pair_clusters);
  *     operands swapped (M <= 128; whole tiles or stream-K chosen
  *     automatically), anything else = automatic (swapped operands when M <=
  *     128 and N has fewer 256-column tiles than half the SMs; pairs when M >
- *     128 or a long K would leave most SMs idle; stream-K when whole tiles
- *     would leave more than 15% of the pairs idle in the last wave).
+ *     128 or a long K would leave most SMs idle; stream-K when it shortens
+ *     each pair's run -- waves x K blocks by whole tiles against the split's
+ *     even share -- by more than its fixed cost of about 32 K blocks).
  */
 void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant);
 

@@ -35,6 +35,8 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_inject{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_l2_prefetch{-1};  // -1: per-shape default
+// K blocks of MMA time a stream-K split costs beyond its share of the work
+constexpr double SK_FIXED_KBLOCKS = 32.0;
 std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA, 2 CTA-pair whole tiles, 3 CTA-pair stream-K,
                                      // 4 swapped operands (skinny M)
 std::atomic<int> g_op_tile{0};       // one-pass cross-entropy N-tile width; 0 = automatic
@@ -330,22 +332,27 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
     const int pf = g_l2_prefetch.load();
     p.l2_prefetch = pf >= 0 ? pf : 0;
     if (g->pair) {
-        // Whole tiles leave pairs idle when the last wave is short; then split
-        // the K iterations evenly over all pairs instead (stream-K).
-        const int P = d->pair_clusters;
-        const int waves = (p.num_tiles + P - 1) / P;
-        const double busy = static_cast<double>(p.num_tiles) / (static_cast<double>(waves) * P);
+        // Whole tiles leave pairs idle when the last wave is short; then the K
+        // iterations can be split evenly over all pairs instead (stream-K).
         // Stream-K groups: G groups of MB pairs (one per M block), G <= V so
         // that no pair gets an empty share -- a tile's owner waits on every
         // later group's partial, so each must write one.
+        const int P = d->pair_clusters;
+        const long long waves = (p.num_tiles + P - 1) / P;
         const long long V = static_cast<long long>(p.num_n_blocks) * batch * p.num_k_blocks;
         long long G = p.num_m_blocks <= P ? P / p.num_m_blocks : 0;
         if (G > V)
             G = V;
-        const double sk_busy = static_cast<double>(G * p.num_m_blocks) / P;
-        p.streamk = (G > 0 && (variant == 3 || (variant < 0 && p.num_k_blocks >= 8 && sk_busy > busy + 0.05)))
-                        ? 1
-                        : 0;
+        // The split pays when it shortens each pair's run -- waves x KB K
+        // blocks by whole tiles, V / G when split -- by more than its fixed
+        // cost (partials written, acquired and added; owners that finish after
+        // single-segment pairs), about 32 K blocks of MMA time on a GB300:
+        // 768 x 5120 x 13824 (216 -> 172.8 K blocks) 71.9 -> 68.9 us, while at
+        // K = 4096 (64 -> 51-61) whole tiles measured 30.4-30.9 us against
+        // 33.0-37.9 us split.
+        const double whole_kb = static_cast<double>(waves) * p.num_k_blocks;
+        const double split_kb = G > 0 ? static_cast<double>(V) / static_cast<double>(G) : whole_kb;
+        p.streamk = (G > 0 && (variant == 3 || (variant < 0 && whole_kb - split_kb > SK_FIXED_KBLOCKS))) ? 1 : 0;
         if (p.streamk) {
             lf_status st = ensure_sk_workspace(d);
             if (st != LF_OK)

@@ -132,6 +132,19 @@ def test_gemm_nt_projection_full_size(variant):
     assert_gemm_close(f64(out.reshape(wl.M, wl.N))[rows], ref, "nt_projection")
 
 
+@pytest.mark.parametrize("M,N,K", [(768, 5120, 512), (640, 6000, 136), (700, 4984, 4104)])
+def test_gemm_nt_automatic_schedule_full(M, N, K):
+    """The planner's own choice (whole tiles or stream-K, by the K blocks the
+    split saves against its fixed cost) on shapes with fewer 256x256 tiles
+    than CTA pairs: every element against the oracle."""
+    lf.set_tuning(-1, -1)
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    out = lf.gemm_nt(x.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    lf.check_device_error()
+    assert_gemm_close(f64(out), oracle.gemm_nt(x, w), "auto %dx%dx%d" % (M, N, K))
+
+
 def test_gemm_nt_k1_routes_to_pointwise_bitexact():
     x = synthetic.bf16_normal((96, 1), 2.0, 0)
     w = synthetic.bf16_normal((264, 1), 0.5, 1)
