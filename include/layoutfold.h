@@ -321,6 +321,17 @@ lf_status lf_check_device_error(cudaStream_t stream);
 uint64_t lf_launch_count(void);
 
 /*
+ * The schedule of the last tensor-core GEMM launch in this process (gemm_nt,
+ * gemm_layout, gemm_batched and the two-pass cross-entropy GEMMs; not the
+ * one-pass cross-entropy kernel): its grid in CTAs, whether it ran on CTA
+ * pairs (1) or single CTAs (0), whether the K loop was split over the pairs
+ * (stream-K: 1), and the MMA's N-tile width.  All zero before the first such
+ * launch.  Any pointer may be NULL.  Not synchronised with other threads'
+ * launches; meant for tests and tuning.
+ */
+void lf_last_gemm_plan(int *grid, int *cta_pairs, int *stream_k, int *tile_n);
+
+/*
  * Sets up the current device if needed and reports its SM count and how many
  * CTA pairs of the pair GEMM kernel can be resident at once (either pointer
  * may be NULL).  LF_ERR_ARCH on a device that is not sm_103.

@@ -74,6 +74,8 @@ def lib():
         L.lf_check_device_error.restype = I32
         L.lf_launch_count.argtypes = []
         L.lf_launch_count.restype = ctypes.c_uint64
+        L.lf_last_gemm_plan.argtypes = [ctypes.POINTER(ctypes.c_int)] * 4
+        L.lf_last_gemm_plan.restype = None
         L.lf_device_query.argtypes = [P, P]
         L.lf_device_query.restype = I32
         L.lf_set_tuning.argtypes = [I32, I32]
@@ -357,6 +359,14 @@ def check_device_error(stream=None):
 
 def launch_count() -> int:
     return int(lib().lf_launch_count())
+
+
+def last_gemm_plan():
+    """Schedule of the last tensor-core GEMM launch in this process: grid
+    (CTAs), cta_pairs (bool), stream_k (bool) and tile_n."""
+    v = [ctypes.c_int(0) for _ in range(4)]
+    lib().lf_last_gemm_plan(*[ctypes.byref(x) for x in v])
+    return {"grid": v[0].value, "cta_pairs": bool(v[1].value), "stream_k": bool(v[2].value), "tile_n": v[3].value}
 
 
 def device_query():

@@ -32,6 +32,9 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_dev[MAX_DEVICES];
 std::atomic<uint64_t> g_launches{0};
+// the schedule of the last tensor-core GEMM launch:
+// grid | (0 single CTA, 1 CTA pairs) << 20 | stream-K << 23 | N-tile width << 24
+std::atomic<uint64_t> g_last_plan{0};
 std::atomic<int> g_inject{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_l2_prefetch{-1};  // -1: per-shape default
@@ -372,6 +375,9 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
 
 cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
 {
+    g_last_plan.store(static_cast<uint64_t>(g.grid) | (static_cast<uint64_t>(g.pair ? 1 : 0) << 20) |
+                      (static_cast<uint64_t>(g.p.streamk ? 1 : 0) << 23) |
+                      (static_cast<uint64_t>(g.p.tile_n ? g.p.tile_n : lf::BN) << 24));
     if (g.p.streamk)
         g.p.epoch = next_epoch(g.dev);  // each launch's flags are distinct from every earlier one
     g.p.tma_store = 0;
@@ -730,6 +736,19 @@ lf_status lf_check_device_error(cudaStream_t stream)
 }
 
 uint64_t lf_launch_count(void) { return g_launches.load(); }
+
+void lf_last_gemm_plan(int *grid, int *cta_pairs, int *stream_k, int *tile_n)
+{
+    const uint64_t v = g_last_plan.load();
+    if (grid)
+        *grid = static_cast<int>(v & 0xfffffu);
+    if (cta_pairs)
+        *cta_pairs = static_cast<int>((v >> 20) & 1u);
+    if (stream_k)
+        *stream_k = static_cast<int>((v >> 23) & 1u);
+    if (tile_n)
+        *tile_n = static_cast<int>(v >> 24);
+}
 
 lf_status lf_device_query(int *num_sms, int *pair_clusters)
 {

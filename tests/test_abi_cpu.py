@@ -11,7 +11,7 @@ import layout_folding_gb300 as lf
 from layout_folding_gb300 import build as lfbuild
 
 EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
-            "lf_launch_count", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
+            "lf_launch_count", "lf_last_gemm_plan", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
             "fp8_cast_dual", "rope_cos_sin", "gemm_layout", "lf_set_onepass_tile", "gemm_batched",
             "gemm_nt_xent_layout"}
 
@@ -162,3 +162,9 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 8, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         lf.gemm_nt(x, x)
+
+
+def test_last_gemm_plan_is_empty_before_any_gemm(L):
+    # no GEMM has run in this process: the record is all zero, and reading it
+    # touches no device
+    assert lf.last_gemm_plan() == {"grid": 0, "cta_pairs": False, "stream_k": False, "tile_n": 0}

@@ -145,6 +145,24 @@ def test_gemm_nt_automatic_schedule_full(M, N, K):
     assert_gemm_close(f64(out), oracle.gemm_nt(x, w), "auto %dx%dx%d" % (M, N, K))
 
 
+@pytest.mark.parametrize("M,N,K,stream_k", [(768, 5120, 13824, True), (768, 5120, 4096, False),
+                                             (512, 8192, 4096, False), (640, 6000, 4096, False)])
+def test_gemm_nt_automatic_schedule_choice(M, N, K, stream_k):
+    """The planner splits K over the CTA pairs only where that saves each
+    pair more than ~32 K blocks: the projection shape (216 -> 172.8 K blocks
+    per pair) is split, the K = 4096 shapes (64 -> 51..61) run whole tiles."""
+    lf.set_tuning(-1, -1)
+    pairs = lf.device_query()[1]
+    x, w = synthetic.make_gemm_inputs(M, N, K, 0.02, 0.02)
+    lf.gemm_nt(x.to(DEV), w.to(DEV))
+    plan = lf.last_gemm_plan()
+    torch.cuda.synchronize()
+    lf.check_device_error()
+    assert plan["cta_pairs"] and plan["tile_n"] == 256, plan
+    if pairs == 76:                       # the split's share depends on the pair count
+        assert plan["stream_k"] == stream_k, plan
+
+
 def test_gemm_nt_k1_routes_to_pointwise_bitexact():
     x = synthetic.bf16_normal((96, 1), 2.0, 0)
     w = synthetic.bf16_normal((264, 1), 0.5, 1)
