@@ -317,6 +317,22 @@ const char *lf_status_string(lf_status status);
  */
 lf_status lf_check_device_error(cudaStream_t stream);
 
+/*
+ * Which device-side wait gave up, for the last LF_ERR_DEVICE_TIMEOUT that
+ * lf_check_device_error reported in this process (0: none yet).  The first
+ * wait to give up in a launch records its code:
+ *   0x101 an operand ring slot was never freed (TMA producer)
+ *   0x102 an operand stage never landed (MMA issuer)
+ *   0x103 an accumulator was never released by the epilogue (MMA issuer)
+ *   0x104 an accumulator was never completed (epilogue)
+ *   0x105 copies or MMAs did not finish while unwinding
+ *   0x106 a stream-K partial never arrived (tile owner)
+ *   0x107 a CTA's own stream-K partial write did not complete
+ *   0x108 a one-pass group member never published its row statistics
+ *   0x109 the copy of a stream-K partial into shared memory did not land
+ */
+int lf_last_device_wait_code(void);
+
 /* Number of kernel launches this library has enqueued in this process (all devices). */
 uint64_t lf_launch_count(void);
 

@@ -76,6 +76,8 @@ def lib():
         L.lf_launch_count.restype = ctypes.c_uint64
         L.lf_last_gemm_plan.argtypes = [ctypes.POINTER(ctypes.c_int)] * 4
         L.lf_last_gemm_plan.restype = None
+        L.lf_last_device_wait_code.argtypes = []
+        L.lf_last_device_wait_code.restype = ctypes.c_int
         L.lf_device_query.argtypes = [P, P]
         L.lf_device_query.restype = I32
         L.lf_set_tuning.argtypes = [I32, I32]
@@ -352,9 +354,28 @@ def bmm(a, b, out=None, stream=None):
     return out3[0] if a.dim() == 2 and b.dim() == 2 and out.dim() == 3 else out
 
 
+# which device-side wait gave up (lf_last_device_wait_code)
+WAIT_CODES = {0x101: "operand ring slot never freed", 0x102: "operand stage never landed",
+              0x103: "accumulator never released", 0x104: "accumulator never completed",
+              0x105: "unwinding did not finish", 0x106: "stream-K partial never arrived",
+              0x107: "own stream-K partial write incomplete", 0x108: "one-pass group member never published",
+              0x109: "partial copy into shared memory never landed"}
+
+
+def last_device_wait_code() -> int:
+    """Code of the wait behind the last device timeout reported (0: none)."""
+    return int(lib().lf_last_device_wait_code())
+
+
 def check_device_error(stream=None):
-    """Synchronise the stream; raise LayoutFoldError if a device wait timed out."""
-    _check(lib().lf_check_device_error(_stream(stream)), "lf_check_device_error")
+    """Synchronise the stream; raise LayoutFoldError if a device wait timed
+    out (its message names the wait that gave up)."""
+    status = lib().lf_check_device_error(_stream(stream))
+    where = "lf_check_device_error"
+    if status == 6:
+        code = last_device_wait_code()
+        where += " [wait 0x%x: %s]" % (code, WAIT_CODES.get(code, "unknown"))
+    _check(status, where)
 
 
 def launch_count() -> int:

@@ -35,6 +35,8 @@ std::atomic<uint64_t> g_launches{0};
 // the schedule of the last tensor-core GEMM launch:
 // grid | (0 single CTA, 1 CTA pairs) << 20 | stream-K << 23 | N-tile width << 24
 std::atomic<uint64_t> g_last_plan{0};
+// the code of the last device-side wait that gave up, as lf_check_device_error read it
+std::atomic<int> g_last_wait_code{0};
 std::atomic<int> g_inject{0};
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_l2_prefetch{-1};  // -1: per-shape default
@@ -727,6 +729,7 @@ lf_status lf_check_device_error(cudaStream_t stream)
     }
     if (code == 0)
         return LF_OK;
+    g_last_wait_code.store(code);
     if (cudaMemsetAsync(d->err_word, 0, sizeof(int), stream) != cudaSuccess ||
         cudaStreamSynchronize(stream) != cudaSuccess) {
         cudaGetLastError();
@@ -736,6 +739,8 @@ lf_status lf_check_device_error(cudaStream_t stream)
 }
 
 uint64_t lf_launch_count(void) { return g_launches.load(); }
+
+int lf_last_device_wait_code(void) { return g_last_wait_code.load(); }
 
 void lf_last_gemm_plan(int *grid, int *cta_pairs, int *stream_k, int *tile_n)
 {

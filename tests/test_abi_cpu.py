@@ -5,13 +5,15 @@ import ctypes
 import os
 import subprocess
 
+import re
+
 import pytest
 
 import layout_folding_gb300 as lf
 from layout_folding_gb300 import build as lfbuild
 
 EXPECTED = {"gemm_nt", "gemm_nt_xent", "matmul_k1", "lf_status_string", "lf_check_device_error",
-            "lf_launch_count", "lf_last_gemm_plan", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
+            "lf_launch_count", "lf_last_gemm_plan", "lf_last_device_wait_code", "lf_set_test_hooks", "lf_set_tuning", "lf_device_query", "gemm_nt_xent_noalloc",
             "fp8_cast_dual", "rope_cos_sin", "gemm_layout", "lf_set_onepass_tile", "gemm_batched",
             "gemm_nt_xent_layout"}
 
@@ -168,3 +170,12 @@ def test_last_gemm_plan_is_empty_before_any_gemm(L):
     # no GEMM has run in this process: the record is all zero, and reading it
     # touches no device
     assert lf.last_gemm_plan() == {"grid": 0, "cta_pairs": False, "stream_k": False, "tile_n": 0}
+
+
+def test_wait_codes_match_the_header(L):
+    # the binding's table of wait codes is the header's, and nothing has timed out yet
+    text = open(lf.HEADER).read()
+    block = text[text.index("int lf_last_device_wait_code") - 1200:text.index("int lf_last_device_wait_code")]
+    codes = {int(c, 16) for c in re.findall(r"\*\s+(0x1[0-9a-f]{2}) ", block)}
+    assert codes == set(lf.WAIT_CODES)
+    assert lf.last_device_wait_code() == 0

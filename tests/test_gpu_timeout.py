@@ -33,6 +33,8 @@ def test_stalled_wait_times_out_and_context_survives(variant):
         with pytest.raises(lf.LayoutFoldError) as info:
             lf.check_device_error()
         assert info.value.status == 6            # LF_ERR_DEVICE_TIMEOUT
+        assert lf.last_device_wait_code() in lf.WAIT_CODES   # the wait that gave up is named
+        assert "wait 0x" in str(info.value)
     finally:
         lf.set_test_hooks(False, 0)
     try:
