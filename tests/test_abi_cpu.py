@@ -3,9 +3,8 @@ every function the public header declares, and rejects invalid arguments on
 the host before any CUDA call is made."""
 import ctypes
 import os
-import subprocess
-
 import re
+import subprocess
 
 import pytest
 
@@ -164,6 +163,13 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 8, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         lf.gemm_nt(x, x)
+
+
+def test_last_gemm_plan_accepts_null_pointers(L):
+    L.lf_last_gemm_plan(None, None, None, None)      # every output is optional
+    g = ctypes.c_int(-1)
+    L.lf_last_gemm_plan(ctypes.byref(g), None, None, None)
+    assert g.value == 0                              # no GEMM has run in this process
 
 
 def test_last_gemm_plan_is_empty_before_any_gemm(L):
