@@ -288,7 +288,7 @@ def run_ours(args, rank, world, local_rank):
                     "rope_scaled": paths.get("rope_scaled", {}).get("ms"),
                     "fp8_cast_scaled": paths.get("fp8_cast_scaled", {}).get("ms")}
             for k, v in lib.items():
-                if ours.get(k):
+                if isinstance(v, dict) and ours.get(k):
                     v["speedup_of_this_library"] = round(v["ms"] / ours[k], 3)
 
     cpu = None
@@ -523,7 +523,11 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
         del out, inp
         torch.cuda.empty_cache()
     if "library" in want:
-        res["library"] = library_paths(torch, synthetic, timer, stream, peaks, steps)
+        try:
+            res["library"] = library_paths(torch, synthetic, timer, stream, peaks, steps)
+        except Exception as e:  # context only: it never costs the bench line
+            res["library"] = {"error": "%s: %s" % (type(e).__name__, e)}
+            torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
 
