@@ -527,7 +527,6 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
             res["library"] = library_paths(torch, synthetic, timer, stream, peaks, steps)
         except Exception as e:  # context only: it never costs the bench line
             res["library"] = {"error": "%s: %s" % (type(e).__name__, e)}
-            torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
 
