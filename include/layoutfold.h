@@ -64,8 +64,12 @@ typedef enum {
  * keep every SM busy and K is long enough for the split to pay, the launch
  * splits the K loop across SMs (stream-K) and
  * uses a library-owned per-device workspace (about 20 MB, allocated on first
- * such call); calls on one device must then not run concurrently on
- * different streams.
+ * such call).  Such a launch is cooperative (all its CTAs resident at once, as
+ * its tile owners wait for other CTAs' partial sums); if the runtime refuses
+ * that, whole tiles are used.  Calls that use the workspace are ordered: a
+ * call on another stream than the previous one first makes its stream wait
+ * for that call (an event, no host synchronisation), so such calls from
+ * several streams or host threads run one after another on the GPU.
  */
 lf_status gemm_nt(const void *x, const void *w, void *out,
                   int64_t M, int64_t N, int64_t K, cudaStream_t stream);
@@ -95,10 +99,15 @@ lf_status gemm_nt(const void *x, const void *w, void *out,
  * writes loss and gradient, the pairs of a row block exchanging their row
  * partials through flags in global memory; otherwise the two passes above
  * plus a GEMM pass that recomputes the logits and writes the gradient.
+ * The one-pass kernel is launched cooperatively (every CTA resident at once);
+ * if the runtime refuses that, the two-pass form runs instead.
  * Partials, flags and the one-pass kernel's stash (128 KiB per CTA) live in a
  * per-device workspace that the library allocates on first use (and grows,
- * never shrinks) and frees at unload; calls that share a device must
- * therefore not run concurrently on different streams.
+ * never shrinks) and frees at unload.  Calls are ordered as for gemm_nt: one
+ * on another stream than the previous workspace user waits for it on the GPU
+ * (an event), so calls from several streams or threads are correct and run
+ * one after another.  (A stream that is being captured into a graph is not
+ * ordered against other streams.)
  */
 lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels,
                        float *loss, void *grad_or_null,
@@ -153,8 +162,7 @@ typedef enum {
  *   K = 1 is the broadcast product of gemm_nt (either layout is a vector).
  *   An invalid layout value returns LF_ERR_SHAPE; other errors as gemm_nt.
  *   Both K-major is exactly gemm_nt.  Like gemm_nt it may use the stream-K
- *   split and its per-device workspace: such calls on one device must not
- *   run concurrently on different streams.
+ *   split and its per-device workspace, ordered across streams as gemm_nt's.
  */
 lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, void *out,
                       int64_t M, int64_t N, int64_t K, cudaStream_t stream);
@@ -298,7 +306,9 @@ lf_status fp8_cast_dual(const void *x, const float *scale, void *out, void *out_
  * call's contents; calls that overlap on the GPU (different streams, or
  * graphs replayed concurrently) race on it and must be serialised.
  * Device-side wait timeouts are not reported through lf_check_device_error:
- * a call whose device waits ran out writes NaN to every loss[m].
+ * a call whose device waits ran out writes NaN to every loss[m] and, when
+ * grad_or_null is given, to every gradient element.  The wait limit and the
+ * stall injection of lf_set_test_hooks apply to this entry point as well.
  * Arguments, layouts, preconditions and the other error codes are those of
  * gemm_nt_xent.
  */
@@ -389,6 +399,18 @@ void lf_set_onepass_tile(int width);
  * wait_timeout_ns = 0 restores the default limit of 2 s.
  */
 void lf_set_test_hooks(int inject_stall, uint64_t wait_timeout_ns);
+
+/*
+ * Test hook (not for production use): enqueues on `stream` a kernel of `ctas`
+ * CTAs, each holding 200 KiB of shared memory -- one per SM, with no room
+ * beside it for a GEMM CTA -- that wait `duration_ns` on the GPU's global
+ * timer and exit.  It stands in for another application's kernels holding
+ * part of the GPU, e.g. to check that the kernels whose CTAs wait on each
+ * other (stream-K, the one-pass cross-entropy) are launched so that all their
+ * CTAs are resident together.  1 <= ctas <= the SM count and
+ * 0 < duration_ns <= 5 s, else LF_ERR_SHAPE.
+ */
+lf_status lf_test_occupy_sms(int ctas, uint64_t duration_ns, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

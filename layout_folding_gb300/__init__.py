@@ -86,6 +86,10 @@ def lib():
         L.lf_set_onepass_tile.restype = None
         L.lf_set_test_hooks.argtypes = [I32, ctypes.c_uint64]
         L.lf_set_test_hooks.restype = None
+        L.lf_test_occupy_sms.argtypes = [I32, ctypes.c_uint64, P]
+        L.lf_test_occupy_sms.restype = I32
+        L.gemm_nt_xent_noalloc.argtypes = [P, P, P, P, P, I64, I64, I64, P]
+        L.gemm_nt_xent_noalloc.restype = I32
         _lib = L
         return L
 
@@ -412,3 +416,9 @@ def set_onepass_tile(width: int = 0):
 
 def set_test_hooks(inject_stall: bool, wait_timeout_ns: int = 0):
     lib().lf_set_test_hooks(1 if inject_stall else 0, int(wait_timeout_ns))
+
+
+def occupy_sms(ctas: int, duration_ns: int, stream=None):
+    """Test hook: hold `ctas` SMs (200 KiB of shared memory each) for
+    duration_ns on `stream`, standing in for another application's kernels."""
+    _check(lib().lf_test_occupy_sms(int(ctas), int(duration_ns), _stream(stream)), "lf_test_occupy_sms")

@@ -27,6 +27,15 @@ struct DeviceState {
     int *err_word = nullptr;  // device int[64]; [0] = first error code
     void *ws = nullptr;       // cross-entropy workspace (grow-only)
     size_t ws_bytes = 0;
+    // Ordering of the calls that use the workspaces above (WorkspaceOrder).
+    std::mutex order_mutex;
+    cudaEvent_t ws_event = nullptr;    // recorded after the last such call's launches
+    cudaStream_t ws_stream = nullptr;  // the stream it was recorded on
+    bool ws_recorded = false;
+    // Cooperative launches of CTA-pair clusters (stream-K, one-pass
+    // cross-entropy): 0 = not refused so far, -1 = the runtime refused one, so
+    // schedules whose CTAs wait on each other are no longer chosen.
+    std::atomic<int> coop{0};
 };
 
 std::mutex g_mutex;
@@ -90,6 +99,7 @@ lf_status current_device(DeviceState **out)
             d.pair_clusters = lf::gemm_pair_max_active_clusters();
             if (cudaMalloc(&d.err_word, 64 * sizeof(int)) != cudaSuccess ||
                 cudaMemset(d.err_word, 0, 64 * sizeof(int)) != cudaSuccess ||
+                cudaEventCreateWithFlags(&d.ws_event, cudaEventDisableTiming) != cudaSuccess ||
                 cudaDeviceSynchronize() != cudaSuccess) {
                 cudaGetLastError();
                 return LF_ERR_LAUNCH;
@@ -179,6 +189,54 @@ unsigned next_epoch(DeviceState *d)
         e = ++d->sk_epoch;
     return e;
 }
+
+// Orders the calls that use a device's library-owned workspaces (the
+// cross-entropy partials, the stream-K slots and flags, the one-pass flags and
+// stash).  A call on a different stream than the previous such call first
+// makes its stream wait for that call's launches (an event: no host
+// synchronisation), and the lock, held from before the launch's epoch is drawn
+// until its launches are enqueued and recorded, keeps host threads from
+// interleaving -- so such launches run one after another on the GPU, in the
+// order of their epochs, whatever streams and threads they come from.  A
+// stream that is being captured into a graph is neither made to wait nor
+// recorded (graph replays are ordered by the caller).
+class WorkspaceOrder {
+public:
+    WorkspaceOrder(DeviceState *d, cudaStream_t s) : d_(d), s_(s), lock_(d->order_mutex)
+    {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            cs = cudaStreamCaptureStatusNone;
+        }
+        capturing_ = cs != cudaStreamCaptureStatusNone;
+        if (!capturing_ && d->ws_recorded && d->ws_stream != s && cudaStreamWaitEvent(s, d->ws_event, 0) != cudaSuccess) {
+            cudaGetLastError();
+            ok_ = false;
+        }
+    }
+    WorkspaceOrder(const WorkspaceOrder &) = delete;
+    WorkspaceOrder &operator=(const WorkspaceOrder &) = delete;
+    bool ok() const { return ok_; }
+    ~WorkspaceOrder()
+    {
+        if (capturing_ || !ok_)
+            return;
+        if (cudaEventRecord(d_->ws_event, s_) == cudaSuccess) {
+            d_->ws_recorded = true;
+            d_->ws_stream = s_;
+        } else {
+            cudaGetLastError();
+        }
+    }
+
+private:
+    DeviceState *d_;
+    cudaStream_t s_;
+    std::lock_guard<std::mutex> lock_;
+    bool capturing_ = false;
+    bool ok_ = true;
+};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -357,7 +415,10 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
         // 33.0-37.9 us split.
         const double whole_kb = static_cast<double>(waves) * p.num_k_blocks;
         const double split_kb = G > 0 ? static_cast<double>(V) / static_cast<double>(G) : whole_kb;
-        p.streamk = (G > 0 && (variant == 3 || (variant < 0 && whole_kb - split_kb > SK_FIXED_KBLOCKS))) ? 1 : 0;
+        p.streamk = (G > 0 && d->coop.load() >= 0 &&
+                     (variant == 3 || (variant < 0 && whole_kb - split_kb > SK_FIXED_KBLOCKS)))
+                        ? 1
+                        : 0;
         if (p.streamk) {
             lf_status st = ensure_sk_workspace(d);
             if (st != LF_OK)
@@ -390,8 +451,22 @@ cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
         const int64_t stride = batch > 1 ? g.p.stride_o : static_cast<int64_t>(g.p.M) * g.p.ldo;
         g.p.tma_store = make_tmap_out(&g.to, g.p.out, g.p.M, g.p.N, g.p.ldo, batch, stride, b3) ? 1 : 0;
     }
-    return g.pair ? lf::launch_gemm_nt_pair(epi, g.layout, g.ta, g.tb, g.to, g.p, g.grid, stream)
-                  : lf::launch_gemm_nt(epi, g.ta, g.tb, g.p, g.grid, stream);
+    if (!g.pair)
+        return lf::launch_gemm_nt(epi, g.ta, g.tb, g.p, g.grid, stream);
+    cudaError_t e = lf::launch_gemm_nt_pair(epi, g.layout, g.ta, g.tb, g.to, g.p, g.grid, stream);
+    if (e != cudaSuccess && g.p.streamk) {
+        // The stream-K split is launched cooperatively (its tile owners wait for
+        // other CTAs).  If the runtime refuses that, run whole tiles, which have
+        // no cross-CTA waits, and stop choosing schedules that need it.
+        cudaGetLastError();
+        g.p.streamk = 0;
+        g.grid = 2 * (g.p.num_tiles < g.dev->pair_clusters ? g.p.num_tiles : g.dev->pair_clusters);
+        g_last_plan.store((g_last_plan.load() & ~((0xfffffull) | (1ull << 23))) | static_cast<uint64_t>(g.grid));
+        e = lf::launch_gemm_nt_pair(epi, g.layout, g.ta, g.tb, g.to, g.p, g.grid, stream);
+        if (e == cudaSuccess)
+            g.dev->coop.store(-1);
+    }
+    return e;
 }
 
 lf_status launched(cudaError_t e, int n)
@@ -400,6 +475,18 @@ lf_status launched(cudaError_t e, int n)
         return LF_ERR_LAUNCH;
     g_launches.fetch_add(static_cast<uint64_t>(n));
     return LF_OK;
+}
+
+// One planned GEMM launch; a stream-K launch uses the workspace, so it is
+// ordered against the other workspace users (WorkspaceOrder).
+lf_status run_planned(int epi, GemmPlan &g, cudaStream_t stream)
+{
+    if (!g.p.streamk)
+        return launched(run_gemm(epi, g, stream), 1);
+    WorkspaceOrder order(g.dev, stream);
+    if (!order.ok())
+        return LF_ERR_LAUNCH;
+    return launched(run_gemm(epi, g, stream), 1);
 }
 
 lf_status check_gemm_shape(int64_t M, int64_t N, int64_t K)
@@ -413,6 +500,18 @@ lf_status check_gemm_shape(int64_t M, int64_t N, int64_t K)
 }
 
 }  // namespace
+
+namespace lf {
+
+unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+int stall_injection() { return g_inject.load(); }
+void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+bool make_tmap_kmajor(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, uint32_t box_rows)
+{
+    return make_tmap(m, ptr, rows, K, box_rows);
+}
+
+}  // namespace lf
 
 extern "C" {
 
@@ -444,12 +543,12 @@ lf_status gemm_nt(const void *x, const void *w, void *out, int64_t M, int64_t N,
             return st;
         g.p.out = out;
         g.p.ldo = N;
-        return launched(run_gemm(lf::EPI_STORE_T, g, stream), 1);
+        return run_planned(lf::EPI_STORE_T, g, stream);
     }
     if ((st = plan_gemm(d, x, w, M, N, K, &g)) != LF_OK)
         return st;
     g.p.out = out;
-    return launched(run_gemm(lf::EPI_STORE, g, stream), 1);
+    return run_planned(lf::EPI_STORE, g, stream);
 }
 
 lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, void *out, int64_t M, int64_t N,
@@ -477,7 +576,7 @@ lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, 
     if ((st = plan_gemm(d, x, w, M, N, K, &g, (x_mn ? 1 : 0) | (w_mn ? 2 : 0))) != LF_OK)
         return st;
     g.p.out = out;
-    return launched(run_gemm(lf::EPI_STORE, g, stream), 1);
+    return run_planned(lf::EPI_STORE, g, stream);
 }
 
 lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_x, const void *w, int w_layout,
@@ -508,7 +607,7 @@ lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_
     if ((st = plan_gemm(d, x, w, M, N, K, &g, (x_mn ? 1 : 0) | (w_mn ? 2 : 0), &bs)) != LF_OK)
         return st;
     g.p.out = out;
-    return launched(run_gemm(lf::EPI_STORE, g, stream), 1);
+    return run_planned(lf::EPI_STORE, g, stream);
 }
 
 }  // extern "C"
@@ -539,6 +638,9 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
     DeviceState *d = nullptr;
     if ((st = current_device(&d)) != LF_OK)
         return st;
+    WorkspaceOrder order(d, stream);  // every form below uses the per-device workspace
+    if (!order.ok())
+        return LF_ERR_LAUNCH;
     const int layout = (x_mn ? 1 : 0) | (w_mn ? 2 : 0);
     GemmPlan g;
     if ((st = plan_gemm(d, x, w, M, N, K, &g, layout)) != LF_OK)
@@ -568,7 +670,7 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
     int op_tile = 0;
     long long best = 0;
     const int forced = g_op_tile.load();
-    for (int wdt = 256; wdt >= 128 && grad_or_null && g.pair; wdt -= 32) {
+    for (int wdt = 256; wdt >= 128 && grad_or_null && g.pair && d->coop.load() >= 0; wdt -= 32) {
         if (forced && wdt != forced)
             continue;
         if (w_mn && wdt != 256 && wdt != 128)  // an N-major W arrives in 64-row boxes per CTA half tile
@@ -609,7 +711,19 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
         CUtensorMap to;  // the gradient, written by TMA stores
         if (!make_tmap_out(&to, grad_or_null, M, N, N, 1, M * N, false))
             return LF_ERR_LAUNCH;
-        return launched(lf::launch_xent_onepass(layout, g.ta, tb_op, to, p, 2 * p.op_k * p.op_Q, stream), 1);
+        if (lf::launch_xent_onepass(layout, g.ta, tb_op, to, p, 2 * p.op_k * p.op_Q, stream) == cudaSuccess)
+            return launched(cudaSuccess, 1);
+        // The one-pass kernel is launched cooperatively (a group's pairs wait
+        // for each other); the runtime refused that, so take the two-pass
+        // form below, and stop choosing schedules that need it.
+        cudaGetLastError();
+        d->coop.store(-1);
+        if ((st = plan_gemm(d, x, w, M, N, K, &g, layout)) != LF_OK)
+            return st;
+        p.part_max = reinterpret_cast<float *>(wsb);
+        p.part_sum = reinterpret_cast<float *>(wsb + part);
+        p.label_logit = reinterpret_cast<float *>(wsb + 2 * part);
+        p.labels = labels;
     }
     if ((st = launched(run_gemm(lf::EPI_XENT_PARTIAL, g, stream), 1)) != LF_OK)
         return st;
@@ -777,6 +891,17 @@ void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant)
 void lf_set_onepass_tile(int width)
 {
     g_op_tile.store(width >= 128 && width <= 256 && width % 32 == 0 ? width : 0);
+}
+
+lf_status lf_test_occupy_sms(int ctas, uint64_t duration_ns, cudaStream_t stream)
+{
+    DeviceState *d = nullptr;
+    lf_status st = current_device(&d);
+    if (st != LF_OK)
+        return st;
+    if (ctas < 1 || ctas > d->num_sms || duration_ns == 0 || duration_ns > 5000000000ull)
+        return LF_ERR_SHAPE;
+    return launched(lf::launch_occupy_sms(ctas, static_cast<unsigned long long>(duration_ns), stream), 1);
 }
 
 void lf_set_test_hooks(int inject_stall, uint64_t wait_timeout_ns)

@@ -793,8 +793,14 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     }
 }
 
+// Launch configuration: clusters of two CTAs (the tcgen05 pair).  A stream-K
+// launch is also cooperative: a tile's owner waits for its contributors'
+// partials, so every CTA of the grid must be resident at once, which a
+// cooperative launch guarantees even while other kernels hold SMs (without it
+// an owner could spin while its contributor waits for an SM the owner's
+// neighbours hold).  Whole-tile launches have no cross-CTA waits.
 template <int EPI>
-cudaLaunchConfig_t pair_config(int grid, cudaStream_t s, cudaLaunchAttribute *attr)
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t s, cudaLaunchAttribute *attr, bool cooperative)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -805,8 +811,10 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t s, cudaLaunchAttribute *at
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cooperative ? 2 : 1;
     return cfg;
 }
 
@@ -837,8 +845,8 @@ cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const CU
     cudaError_t e = set_smem_attr_once<EPI, LAYOUT>();
     if (e != cudaSuccess)
         return e;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pair_config<EPI>(grid, s, attr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config<EPI>(grid, s, attr, p.streamk != 0);
     return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI, LAYOUT>, ta, tb, to, p);
 }
 
@@ -854,8 +862,8 @@ int gemm_pair_max_active_clusters()
         cudaGetLastError();
         return 0;
     }
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pair_config<EPI_STORE>(2, 0, attr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config<EPI_STORE>(2, 0, attr, false);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, k_gemm_nt_pair<EPI_STORE, 0>, &cfg) != cudaSuccess) {
         cudaGetLastError();

@@ -827,13 +827,21 @@ cudaError_t launch_onepass_t(const CUtensorMap &ta, const CUtensorMap &tb, const
     cfg.blockDim = dim3(OP_THREADS, 1, 1);
     cfg.dynamicSmemBytes = OP_SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // Clusters of two CTAs (the tcgen05 pair), launched cooperatively: the
+    // pairs of a group wait for each other's row statistics, so the whole grid
+    // must be resident at once -- which a cooperative launch guarantees even
+    // while other kernels hold SMs ("Allow reductions in matmul epilogues":
+    // reusing the row reduction in the epilogue needs every CTA of a row of
+    // tiles in the same wave, i.e. a cooperative launch).
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k_xent_onepass<LAYOUT>, ta, tb, to, p);
 }
 

@@ -107,5 +107,18 @@ cudaError_t launch_rope_cos_sin(const void *inv_freq, const int64_t *pos, void *
                                 int64_t S, int num_sms, cudaStream_t s);
 cudaError_t launch_fp8_cast_dual(const void *x, const float *scale, void *out, void *out_t, int64_t M, int64_t K,
                                  int num_sms, cudaStream_t s);
+// Test hook: `ctas` CTAs, each holding 200 KiB of shared memory (one per SM),
+// that wait `ns` nanoseconds on the global timer and exit.
+cudaError_t launch_occupy_sms(int ctas, unsigned long long ns, cudaStream_t s);
+
+// Library state and helpers shared by the entry points of every translation
+// unit (defined in api.cu).
+unsigned long long wait_timeout_ns();  // device-side wait limit (lf_set_test_hooks; 2 s by default)
+int stall_injection();                 // 1 while lf_set_test_hooks asks for a stalled first stage
+void count_launches(int n);            // adds n to the lf_launch_count total
+// 2-D bf16 tensor [rows, K] (K contiguous) as a TMA map: boxes of 64 columns x
+// box_rows rows, 128-byte swizzle, zero fill out of bounds.  False if the
+// driver entry point is missing or rejects the layout.
+bool make_tmap_kmajor(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, uint32_t box_rows);
 
 }  // namespace lf

@@ -18,6 +18,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda_bf16.h>
+
 #include "layoutfold.h"
 #include "lf_internal.h"
 
@@ -39,40 +41,6 @@ struct NoAllocDevice {
 
 std::mutex g_noalloc_mutex;
 NoAllocDevice g_noalloc_dev[MAX_DEVICES];
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-
-EncodeTiledFn noalloc_encode_fn()
-{
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-bool noalloc_tmap(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, uint32_t box_rows)
-{
-    EncodeTiledFn enc = noalloc_encode_fn();
-    if (!enc)
-        return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(lf::BK), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 // Set-up of the current device, done once per device by the first call made
 // with that device current: architecture check and the scratch's device
@@ -113,14 +81,19 @@ lf_status noalloc_device(NoAllocDevice **out)
     return LF_OK;
 }
 
-// A device-side wait that ran out marks every loss of the call NaN, so the
-// failure is visible in the output of this variant.
-__global__ void k_noalloc_poison_loss(const int *err, float *loss, int M)
+// A device-side wait that ran out makes the call's outputs NaN -- every loss
+// and, when a gradient was asked for, every gradient element -- so the failure
+// is visible in the output of this variant.
+__global__ void k_noalloc_poison(const int *err, float *loss, int M, __nv_bfloat16 *grad, size_t grad_elems)
 {
     if (*err == 0)
         return;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < M; i += gridDim.x * blockDim.x)
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (size_t i = i0; i < static_cast<size_t>(M); i += stride)
         loss[i] = __int_as_float(0x7fc00000);
+    for (size_t i = i0; i < grad_elems; i += stride)
+        grad[i] = __ushort_as_bfloat16(static_cast<unsigned short>(0x7fc0));
 }
 
 size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
@@ -165,7 +138,8 @@ extern "C" lf_status gemm_nt_xent_noalloc(const void *x, const void *w, const in
     p.num_k_blocks = static_cast<int>((K + lf::BK - 1) / lf::BK);
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.err = err;
-    p.timeout_ns = 2000000000ull;
+    p.timeout_ns = lf::wait_timeout_ns();
+    p.inject = lf::stall_injection();  // test hook, as for the other entry points
     p.labels = labels;
     p.part_max = reinterpret_cast<float *>(s + ERR_BYTES);
     p.part_sum = reinterpret_cast<float *>(s + ERR_BYTES + part);
@@ -174,7 +148,7 @@ extern "C" lf_status gemm_nt_xent_noalloc(const void *x, const void *w, const in
     float *row_logsum = reinterpret_cast<float *>(s + ERR_BYTES + 2 * part + 2 * vec);
 
     CUtensorMap ta, tb;
-    if (!noalloc_tmap(&ta, x, M, K, lf::BM) || !noalloc_tmap(&tb, w, N, K, lf::BN))
+    if (!lf::make_tmap_kmajor(&ta, x, M, K, lf::BM) || !lf::make_tmap_kmajor(&tb, w, N, K, lf::BN))
         return LF_ERR_LAUNCH;
     const int grid = p.num_tiles < d->num_sms ? p.num_tiles : d->num_sms;
 
@@ -188,16 +162,23 @@ extern "C" lf_status gemm_nt_xent_noalloc(const void *x, const void *w, const in
                                 grad_or_null ? row_max : nullptr, grad_or_null ? row_logsum : nullptr,
                                 stream) != cudaSuccess)
         return LF_ERR_LAUNCH;
+    lf::count_launches(2);
     if (grad_or_null) {
         p.out = grad_or_null;
         p.row_max = row_max;
         p.row_logsum = row_logsum;
+        p.inject = 0;
         if (lf::launch_gemm_nt(lf::EPI_XENT_GRAD, ta, tb, p, grid, stream) != cudaSuccess)
             return LF_ERR_LAUNCH;
+        lf::count_launches(1);
     }
-    const int pgrid = static_cast<int>((M + 255) / 256 < 1024 ? (M + 255) / 256 : 1024);
-    k_noalloc_poison_loss<<<pgrid, 256, 0, stream>>>(err, loss, p.M);
+    const size_t grad_elems = grad_or_null ? static_cast<size_t>(M) * static_cast<size_t>(N) : 0;
+    const size_t work = grad_elems > static_cast<size_t>(M) ? grad_elems : static_cast<size_t>(M);
+    const int pgrid = static_cast<int>((work + 255) / 256 < 1024 ? (work + 255) / 256 : 1024);
+    k_noalloc_poison<<<pgrid, 256, 0, stream>>>(err, loss, p.M, static_cast<__nv_bfloat16 *>(grad_or_null),
+                                                grad_elems);
     if (cudaGetLastError() != cudaSuccess)
         return LF_ERR_LAUNCH;
+    lf::count_launches(1);
     return LF_OK;
 }

@@ -123,6 +123,25 @@ __global__ void __launch_bounds__(256) k_xent_combine(const float *__restrict__ 
     }
 }
 
+// Test hook: hold an SM's shared memory (OCCUPY_SMEM bytes, so no GEMM CTA
+// fits beside it) for `ns` nanoseconds, then exit.  The wait is a fixed time
+// on the global timer, so it always ends.
+constexpr int OCCUPY_SMEM = 200 * 1024;
+
+__global__ void k_occupy_sm(unsigned long long ns)
+{
+    extern __shared__ unsigned char occupy_smem[];
+    if (threadIdx.x != 0)
+        return;
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    do {
+        __nanosleep(1000);
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    } while (t - t0 < ns);
+    occupy_smem[0] = 1;
+}
+
 void grid_for_rows(int64_t M, int64_t cols, int num_sms, dim3 &grid)
 {
     const int64_t gy = M < 65535 ? M : 65535;
@@ -170,6 +189,15 @@ cudaError_t launch_xent_combine(const float *part_max, const float *part_sum, co
     const int grid = (M + rows_per_block - 1) / rows_per_block;
     k_xent_combine<<<grid, 32 * rows_per_block, 0, s>>>(part_max, part_sum, label_logit, labels, M, N,
                                                          num_n_blocks, loss, row_max, row_logsum);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_occupy_sms(int ctas, unsigned long long ns, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(k_occupy_sm, cudaFuncAttributeMaxDynamicSharedMemorySize, OCCUPY_SMEM);
+    if (e != cudaSuccess)
+        return e;
+    k_occupy_sm<<<ctas, 32, OCCUPY_SMEM, s>>>(ns);
     return cudaGetLastError();
 }
 
