@@ -332,6 +332,14 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+def grad_form(want_grad, launches_per_call):
+    """The cross-entropy form a call took, from its launch count: loss only
+    (partials + combine), one pass, exp pass + rescale, or recompute."""
+    if not want_grad:
+        return "loss_only"
+    return {1: "one_pass", 2: "exp_rescale", 3: "recompute"}.get(int(round(launches_per_call)), "unknown")
+
+
 def xent_fractions(flops, executed, ms, peaks):
     """Fractions of the bf16 peak for a cross-entropy leg.  Each call is timed
     alone between L2 flushes (milliseconds, not a seconds-long loop), so the
@@ -442,16 +450,31 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
         lf.check_device_error(stream)
         ms = statistics.mean(times)
         flops = 2.0 * wl.M * wl.N * wl.K
-        # the two-pass gradient (partials, combine, recompute) runs the GEMM
-        # twice; the one-pass kernel (one launch) runs it once
-        one_pass = want_grad and launches == steps
-        executed = flops * (2 if want_grad and not one_pass else 1)
+        form = grad_form(want_grad, launches / steps)
+        # the recompute form runs the GEMM twice; the one-pass kernel and the
+        # exp pass + rescale run it once
+        executed = flops * (2 if form == "recompute" else 1)
         key = name if not (want_grad and name == "xent_loss") else "xent_grad_large_vocab"
         res[key] = {"M": wl.M, "N": wl.N, "K": wl.K, "grad": want_grad, "ms": round(ms, 4),
                     "tflops_algorithmic": round(flops / ms / 1e9, 1),
                     "tflops_executed": round(executed / ms / 1e9, 1),
                     **xent_fractions(flops, executed, ms, peaks),
-                    "launches_per_step": launches / steps, "one_pass": bool(one_pass)}
+                    "launches_per_step": launches / steps, "grad_form": form}
+        if want_grad:
+            # the other gradient forms on the same workload, for comparison
+            for label, path in (("one_pass", 1), ("exp_rescale", 2)):
+                lf.set_xent_grad_path(path)
+                try:
+                    t_alt, n_alt = timer.run(step, steps, 3, counter=lf.launch_count)
+                    lf.check_device_error(stream)
+                finally:
+                    lf.set_xent_grad_path(0)
+                ms_alt = statistics.mean(t_alt)
+                f_alt = grad_form(True, n_alt / steps)
+                res[key]["form_" + label] = {"ms": round(ms_alt, 4), "grad_form": f_alt,
+                                             "tflops_algorithmic": round(flops / ms_alt / 1e9, 1),
+                                             "pct_of_burst_algorithmic":
+                                                 round(100 * flops / ms_alt / 1e9 / peaks["bf16_tflops"], 1)}
         if not want_grad and name == "xent_loss":
             # The unfused comparison of the loss-only fusion ("the IO saving"): this
             # library's GEMM writing the bf16 logits to HBM, then PyTorch's
@@ -480,15 +503,15 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
             times, launches = timer.run(step_kn, steps, 3, counter=lf.launch_count)
             lf.check_device_error(stream)
             ms = statistics.mean(times)
-            one_pass_kn = launches == steps
-            executed = flops * (1 if one_pass_kn else 2)
+            form_kn = grad_form(True, launches / steps)
+            executed = flops * (2 if form_kn == "recompute" else 1)
             res["xent_grad_w_stored_kn"] = {"M": wl.M, "N": wl.N, "K": wl.K, "grad": True, "w_stored": "[K,N]",
                                             "ms": round(ms, 4),
                                             "tflops_algorithmic": round(flops / ms / 1e9, 1),
                                             "tflops_executed": round(executed / ms / 1e9, 1),
                                             **xent_fractions(flops, executed, ms, peaks),
                                             "launches_per_step": launches / steps,
-                                            "one_pass": bool(one_pass_kn)}
+                                            "grad_form": form_kn}
             del w_kn
         del x, w, lab, loss, grad, inp
         torch.cuda.empty_cache()

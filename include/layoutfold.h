@@ -391,6 +391,30 @@ void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant);
 void lf_set_onepass_tile(int width);
 
 /*
+ * How gemm_nt_xent / gemm_nt_xent_layout compute the gradient on CTA pairs,
+ * applied to later calls: 1 = the one-pass kernel when a row block of tiles
+ * fits the resident pairs (else as 0), 2 = the exp pass and the rescale pass
+ * (a GEMM whose epilogue writes the tile partials and fp16 exp(z - tile max)
+ * into grad, then one kernel that merges each row's partials into lse and
+ * loss and rewrites grad in place as bf16; the recompute form when a row has
+ * more than 49,152 tiles of 256 columns), 3 = partials, combine and a second
+ * GEMM pass that recomputes the logits to write the gradient; anything else =
+ * automatic (the exp pass and the rescale pass unless a one-pass tile width is
+ * forced).  The single-CTA kernel always uses the recompute form.
+ */
+void lf_set_xent_grad_path(int path);
+
+/*
+ * Order of whole output tiles on CTA pairs, applied to later launches: bands
+ * of `m_blocks` 256-row blocks, each band sweeping every N block before the
+ * next starts (M block fastest within a band, so the pairs sharing a W tile
+ * run together).  0 = one band of all rows; a negative value restores the
+ * automatic choice (the largest band whose X rows take at most 32 MiB, split
+ * evenly).  Results do not depend on it.
+ */
+void lf_set_tile_band(int m_blocks);
+
+/*
  * Test hooks (not for production use).  inject_stall = 1 makes the next
  * tensor-core GEMM launches skip the first operand load of CTA 0, so that
  * CTA's MMA wait never completes: the bounded wait then gives up after

@@ -86,6 +86,10 @@ def lib():
         L.lf_set_onepass_tile.restype = None
         L.lf_set_test_hooks.argtypes = [I32, ctypes.c_uint64]
         L.lf_set_test_hooks.restype = None
+        L.lf_set_xent_grad_path.argtypes = [I32]
+        L.lf_set_xent_grad_path.restype = None
+        L.lf_set_tile_band.argtypes = [I32]
+        L.lf_set_tile_band.restype = None
         L.lf_test_occupy_sms.argtypes = [I32, ctypes.c_uint64, P]
         L.lf_test_occupy_sms.restype = I32
         L.gemm_nt_xent_noalloc.argtypes = [P, P, P, P, P, I64, I64, I64, P]
@@ -412,6 +416,17 @@ def set_onepass_tile(width: int = 0):
     """N-tile width of the one-pass cross-entropy kernel (128..256, multiple
     of 32); 0 = automatic."""
     lib().lf_set_onepass_tile(int(width))
+
+
+def set_xent_grad_path(path: int = 0):
+    """Gradient form of the cross-entropy on CTA pairs: 1 = one pass, 2 = exp
+    pass + rescale, 3 = recompute pass, 0 = automatic."""
+    lib().lf_set_xent_grad_path(int(path))
+
+
+def set_tile_band(m_blocks: int = -1):
+    """Whole-tile band height in 256-row blocks (0 = one band, -1 = automatic)."""
+    lib().lf_set_tile_band(int(m_blocks))
 
 
 def set_test_hooks(inject_stall: bool, wait_timeout_ns: int = 0):

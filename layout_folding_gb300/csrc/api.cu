@@ -54,6 +54,13 @@ constexpr double SK_FIXED_KBLOCKS = 32.0;
 std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA, 2 CTA-pair whole tiles, 3 CTA-pair stream-K,
                                      // 4 swapped operands (skinny M)
 std::atomic<int> g_op_tile{0};       // one-pass cross-entropy N-tile width; 0 = automatic
+std::atomic<int> g_xent_path{0};     // cross-entropy gradient: 0 auto, 1 one pass, 2 exp + rescale, 3 recompute
+std::atomic<int> g_band{-1};         // whole-tile band height in M blocks: -1 auto, 0 one band, > 0 forced
+// L2 bytes of X a band of whole tiles may keep while it sweeps W (the L2 is
+// 129 MB, but reuse measured as if about half of it were available)
+constexpr double BAND_X_BYTES = 32.0 * 1024 * 1024;
+// the rescale kernel keeps one scale per 256-column tile of a row in shared memory
+constexpr int64_t RESCALE_MAX_TILES = 48 * 1024;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -433,6 +440,26 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
         }
     } else
         g->grid = p.num_tiles < d->num_sms ? p.num_tiles : d->num_sms;
+    if (g->pair && !p.streamk) {
+        // Whole tiles: bands of M blocks whose X rows stay in L2 while the band
+        // sweeps every N block (W then streams from HBM once per band instead
+        // of X once per wave), split evenly.
+        const int MB = p.num_m_blocks;
+        int band = g_band.load();
+        if (band < 0) {
+            const double x_bytes = static_cast<double>(tile_m) * static_cast<double>(K) * 2.0;
+            band = static_cast<int>(BAND_X_BYTES / x_bytes);
+            if (band < 1)
+                band = 1;
+            if (band >= MB) {
+                band = 0;
+            } else {
+                const int nbands = (MB + band - 1) / band;
+                band = (MB + nbands - 1) / nbands;
+            }
+        }
+        p.band_m = band < MB ? band : 0;
+    }
     return LF_OK;
 }
 
@@ -445,7 +472,7 @@ cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
         g.p.epoch = next_epoch(g.dev);  // each launch's flags are distinct from every earlier one
     g.p.tma_store = 0;
     std::memset(&g.to, 0, sizeof g.to);
-    if (g.pair && (epi == lf::EPI_STORE || epi == lf::EPI_XENT_GRAD) && g.p.out) {
+    if (g.pair && (epi == lf::EPI_STORE || epi == lf::EPI_XENT_GRAD || epi == lf::EPI_XENT_EXP) && g.p.out) {
         const bool b3 = (g.layout & 4) != 0;
         const int64_t batch = b3 ? g.p.batch : 1;
         const int64_t stride = batch > 1 ? g.p.stride_o : static_cast<int64_t>(g.p.M) * g.p.ldo;
@@ -667,10 +694,19 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
     // chains.  (4096 x 32768 x 4096: 0.836 ms at 224 with 74 pairs against
     // 0.847 ms at 256 with 64.  Before the round's merge overlapped the next
     // mainloop, 224 measured slower, 1.038 against 1.011 ms.)
+    // Which gradient form: the one-pass kernel (below), the exp pass + rescale
+    // (a GEMM writing fp16 exp(z - tile max) into grad, then one bandwidth-bound
+    // pass), or the recompute pass (single-CTA tiles, or rows too wide for the
+    // rescale kernel's shared memory).
+    // (A forced one-pass tile width selects the one-pass kernel.)
+    const int path = g_xent_path.load();
+    const int forced = g_op_tile.load();
+    const bool exp_ok = grad_or_null && g.pair && p.num_n_blocks <= RESCALE_MAX_TILES;
+    const bool try_onepass = grad_or_null && g.pair && d->coop.load() >= 0 &&
+                             (path == 1 || (path == 0 && (!exp_ok || forced != 0)));
     int op_tile = 0;
     long long best = 0;
-    const int forced = g_op_tile.load();
-    for (int wdt = 256; wdt >= 128 && grad_or_null && g.pair && d->coop.load() >= 0; wdt -= 32) {
+    for (int wdt = 256; wdt >= 128 && try_onepass; wdt -= 32) {
         if (forced && wdt != forced)
             continue;
         if (w_mn && wdt != 256 && wdt != 128)  // an N-major W arrives in 64-row boxes per CTA half tile
@@ -724,6 +760,16 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
         p.part_sum = reinterpret_cast<float *>(wsb + part);
         p.label_logit = reinterpret_cast<float *>(wsb + 2 * part);
         p.labels = labels;
+    }
+    if (exp_ok && path != 3) {
+        // exp pass: partials and e = fp16(exp(z - tile max)) into grad, then
+        // the rescale kernel: lse, loss, and grad rewritten in place as bf16
+        p.out = grad_or_null;
+        if ((st = launched(run_gemm(lf::EPI_XENT_EXP, g, stream), 1)) != LF_OK)
+            return st;
+        return launched(lf::launch_xent_rescale(p.part_max, p.part_sum, p.label_logit, labels, p.M, p.N,
+                                                p.num_n_blocks, loss, grad_or_null, stream),
+                        1);
     }
     if ((st = launched(run_gemm(lf::EPI_XENT_PARTIAL, g, stream), 1)) != LF_OK)
         return st;
@@ -887,6 +933,10 @@ void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant)
     g_l2_prefetch.store(l2_prefetch_kblocks < 0 ? -1 : l2_prefetch_kblocks);
     g_variant.store(gemm_variant >= 1 && gemm_variant <= 4 ? gemm_variant : -1);
 }
+
+void lf_set_xent_grad_path(int path) { g_xent_path.store(path >= 1 && path <= 3 ? path : 0); }
+
+void lf_set_tile_band(int m_blocks) { g_band.store(m_blocks < 0 ? -1 : m_blocks); }
 
 void lf_set_onepass_tile(int width)
 {

@@ -39,6 +39,8 @@
 // peer, and both meet at a final cluster barrier before TMEM is freed.
 #include <atomic>
 
+#include <cuda_fp16.h>
+
 #include "lf_gemm_common.cuh"
 
 namespace lf {
@@ -102,6 +104,23 @@ constexpr uint64_t ABORT_SETTLE_NS = 100000;  // after an abort: let copies in f
 struct Seg {
     int tile, kb0, kb1;
 };
+
+// M block and (batch-major) N block of a tile index.  Whole tiles walk bands
+// of p.band_m M blocks: within a band the M block varies fastest (the pairs
+// that share a W tile run side by side, so W streams from HBM once per band)
+// and the band's X rows stay in L2 while it sweeps every N block.  One band
+// (band_m 0) is the plain M-block-fastest order; stream-K always uses it.
+__device__ __forceinline__ void tile_coords(const GemmParams &p, int tile, int &mb, int &nbt)
+{
+    const int MB = p.num_m_blocks;
+    const int bm = (p.band_m > 0 && p.band_m < MB && !p.streamk) ? p.band_m : MB;
+    const int per_band = bm * (p.num_tiles / MB);
+    const int band = tile / per_band;
+    const int local = tile - band * per_band;
+    const int rows = min(bm, MB - band * bm);
+    mb = band * bm + local % rows;
+    nbt = local / rows;
+}
 
 // The sequence of segments one pair works on.
 // Whole tiles: tiles pair, pair + num_pairs, ... (M-block fastest).
@@ -299,6 +318,32 @@ __device__ __forceinline__ void tma_store_chunk(const GemmParams &p, const CUten
     }
 }
 
+// Plain-store path (when the output map could not be encoded): the warp's 32
+// x 32 chunk (this thread's row as 16 packed pairs) is staged in shared memory
+// and written 8 rows x 64 bytes per instruction, rows >= M and columns >= N
+// left out.
+__device__ __forceinline__ void plain_store_chunk(const GemmParams &p, __nv_bfloat16 *out, uint8_t *stg,
+                                                  const uint32_t (&pk)[16], int col, int row0)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 8 * i + (lane >> 2);
+        const int pc = lane & 3;
+        const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((pc ^ ((r >> 1) & 3)) << 4));
+        const int grow = row0 + r;
+        const int gcol = col + pc * 8;
+        if (grow < p.M && gcol < p.N)
+            *reinterpret_cast<uint4 *>(out + static_cast<size_t>(grow) * p.N + gcol) = val;
+    }
+    __syncwarp();
+}
+
 // After a tile's last chunk: every store has read its staging slot.
 __device__ __forceinline__ void tma_store_drain()
 {
@@ -418,29 +463,102 @@ __device__ __forceinline__ void pair_xent_grad(const GemmParams &p, const CUtens
                 g1 -= 1.f;
             pk[i] = pack_bf16(g0, g1);
         }
-        if (p.tma_store) {
+        if (p.tma_store)
             tma_store_chunk<false>(p, tmO, stg, stg_s, c / 32, pk, col, row0, 0);
-            continue;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = 8 * i + (lane >> 2);
-            const int pc = lane & 3;
-            const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((pc ^ ((r >> 1) & 3)) << 4));
-            const int grow = row0 + r;
-            const int gcol = col + pc * 8;
-            if (grow < p.M && gcol < p.N)
-                *reinterpret_cast<uint4 *>(out + static_cast<size_t>(grow) * p.N + gcol) = val;
-        }
-        __syncwarp();
+        else
+            plain_store_chunk(p, out, stg, pk, col, row0);
     }
     if (p.tma_store)
         tma_store_drain();
+}
+
+// First pass of the cross-entropy gradient without a recompute GEMM ("Allow
+// reductions in matmul epilogues", fusion example: row max, exp, sum-exp and
+// the label logit of the tile, and the exponentials the softmax-minus-onehot
+// output is made of), for the warp's 32 rows (thread `lane` owns row row0 +
+// lane): over the tile's columns n < N,
+//   m_t = max_n z,  s_t = sum_n exp(z - m_t),  z[label] if the label is here,
+// written to part_max / part_sum [row, nb] and label_logit[row], and
+//   e = fp16_rn(exp(z - m_t))  (in [0, 1]; exactly 1 at the tile's max)
+// written into the gradient buffer, which the rescale kernel later rewrites in
+// place as bf16_rn(e * exp(m_t - lse)) once the row's lse is known.  Two
+// passes over TMEM: the max, then the exponentials (one FFMA + ex2.approx each,
+// the sum as a tree) packed two per word and stored like the gradient.
+__device__ __forceinline__ void pair_xent_exp(const GemmParams &p, const CUtensorMap *tmO, uint32_t taddr, int row0,
+                                              int nb, const PartialAdd &pa, uint8_t *stg, uint32_t stg_s)
+{
+    const int lane = threadIdx.x & 31;
+    const int row = row0 + lane;
+    const bool row_ok = row < p.M;
+    const int lab = row_ok ? p.labels[row] : -1;
+    float mx = -CUDART_INF_F, zl = 0.f;
+    bool have = false;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        uint32_t v[32];
+        load_chunk(taddr, c, pa, v);
+        const int nvalid = p.N - col;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nvalid)
+                mx = fmaxf(mx, __uint_as_float(v[i]));
+        const int li = lab - col;
+        if (static_cast<unsigned>(li) < 32u) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i == li)
+                    zl = __uint_as_float(v[i]);
+            have = true;
+        }
+    }
+    const float mxl = mx * LOG2E;
+    float se = 0.f;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int col = nb * BN + c;
+        if (col >= p.N)
+            break;  // warp-uniform
+        uint32_t v[32];
+        load_chunk(taddr, c, pa, v);
+        const int nvalid = p.N - col;
+        float e[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            e[i] = i < nvalid ? ex2_approx(fmaf(__uint_as_float(v[i]), LOG2E, -mxl)) : 0.f;
+        float t[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            t[i] = e[i] + e[i + 16];
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i)
+                t[i] += t[i + w];
+        se += t[0];
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            __half2 h = __floats2half2_rn(e[2 * i], e[2 * i + 1]);  // .x (lower address) = column 2i
+            pk[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        if (p.tma_store)
+            tma_store_chunk<false>(p, tmO, stg, stg_s, c / 32, pk, col, row0, 0);
+        else
+            plain_store_chunk(p, out, stg, pk, col, row0);
+    }
+    if (p.tma_store)
+        tma_store_drain();
+    if (row_ok) {
+        const size_t o = static_cast<size_t>(row) * p.num_n_blocks + nb;
+        p.part_max[o] = mx;
+        p.part_sum[o] = se;
+        if (have && lab < p.N)
+            p.label_logit[row] = zl;
+    }
 }
 
 template <int EPI, int LAYOUT>
@@ -495,7 +613,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
-        if ((EPI == EPI_STORE || EPI == EPI_XENT_GRAD) && p.tma_store)
+        if ((EPI == EPI_STORE || EPI == EPI_XENT_GRAD || EPI == EPI_XENT_EXP) && p.tma_store)
             prefetch_tmap(&tmO);
     }
     if (warp == 1) {
@@ -521,8 +639,8 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
             bool ok = true, first = true;
             WorkIter it(p, pair, num_pairs);
             for (Seg g; ok && it.next(g);) {
-                const int mb = g.tile % p.num_m_blocks;
-                const int nbt = g.tile / p.num_m_blocks;  // batch-major N block
+                int mb, nbt;  // M block, batch-major N block
+                tile_coords(p, g.tile, mb, nbt);
                 const int bz = nbt / p.num_n_blocks;       // batch (0 unless batched)
                 const int nb = nbt % p.num_n_blocks;
                 const int xz = p.x_batched ? bz : 0;
@@ -650,8 +768,8 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
         uint32_t skw_phase = 0;
         WorkIter it(p, pair, num_pairs);
         for (Seg g; it.next(g);) {
-            const int mb = g.tile % p.num_m_blocks;
-            const int nbt = g.tile / p.num_m_blocks;  // batch-major N block
+            int mb, nbt;  // M block, batch-major N block
+            tile_coords(p, g.tile, mb, nbt);
             const int nb = nbt % p.num_n_blocks;
             const int bz = nbt / p.num_n_blocks;
             const int rloc = q * 32 + lane;
@@ -753,6 +871,10 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                     if (done) {
                         if (EPI == EPI_XENT_PARTIAL)
                             epi_xent_partial(p, taddr, row, nb, pa);
+                        else if (EPI == EPI_XENT_EXP)
+                            pair_xent_exp(p, &tmO, taddr, row - lane, nb, pa,
+                                          gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES,
+                                          base + static_cast<uint32_t>(PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES));
                         else
                             pair_xent_grad(p, &tmO, taddr, row - lane, nb, pa,
                                            gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES,
@@ -883,6 +1005,20 @@ cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, cons
             return launch_pair_t<EPI_XENT_PARTIAL, 2>(ta, tb, to, p, grid, s);
         case 3:
             return launch_pair_t<EPI_XENT_PARTIAL, 3>(ta, tb, to, p, grid, s);
+        default:
+            return cudaErrorInvalidValue;
+        }
+    }
+    if (epi == EPI_XENT_EXP) {
+        switch (layout) {
+        case 0:
+            return launch_pair_t<EPI_XENT_EXP, 0>(ta, tb, to, p, grid, s);
+        case 1:
+            return launch_pair_t<EPI_XENT_EXP, 1>(ta, tb, to, p, grid, s);
+        case 2:
+            return launch_pair_t<EPI_XENT_EXP, 2>(ta, tb, to, p, grid, s);
+        case 3:
+            return launch_pair_t<EPI_XENT_EXP, 3>(ta, tb, to, p, grid, s);
         default:
             return cudaErrorInvalidValue;
         }

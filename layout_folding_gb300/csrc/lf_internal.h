@@ -19,6 +19,7 @@ enum Epilogue : int {
     EPI_XENT_PARTIAL = 1,  // per (row, N-tile): max, sum exp(z - max); label logit
     EPI_XENT_GRAD = 2,     // grad = bf16_rn(exp(z - lse) - onehot)
     EPI_STORE_T = 3,       // swapped operands: acc = W . X^T, out[m][n] = bf16_rn(acc[n][m]) (pair kernel)
+    EPI_XENT_EXP = 4,      // partials as EPI_XENT_PARTIAL, and e = exp(z - tile max) as fp16 into out (pair kernel)
 };
 
 struct GemmParams {
@@ -57,9 +58,13 @@ struct GemmParams {
     long long stride_o;               // batch stride of out in elements
     // EPI_STORE_T: the MMA's N (the caller's M, rounded up to 16); 0 = BN
     int tile_n;
-    // pair kernel, EPI_STORE and EPI_XENT_GRAD: 1 = the output tensor map is
-    // valid and the epilogue writes through TMA stores, 0 = plain stores
+    // pair kernel, EPI_STORE, EPI_XENT_GRAD and EPI_XENT_EXP: 1 = the output
+    // tensor map is valid and the epilogue writes through TMA stores, 0 = plain stores
     int tma_store;
+    // pair kernel, whole tiles: the tile order walks bands of band_m M blocks
+    // (M block fastest within a band, then the N blocks, then the next band);
+    // 0 = one band of all M blocks
+    int band_m;
 };
 
 // One stream-K partial slot: a CTA's 128 rows x 256 columns of fp32,
@@ -98,6 +103,14 @@ cudaError_t launch_xent_onepass(int layout, const CUtensorMap &ta, const CUtenso
 cudaError_t launch_xent_combine(const float *part_max, const float *part_sum, const float *label_logit,
                                 const int32_t *labels, int M, int N, int num_n_blocks, float *loss,
                                 float *row_max, float *row_logsum, cudaStream_t s);
+
+// Second pass of the cross-entropy gradient after EPI_XENT_EXP: per row, the
+// combine (lse from the tile partials, loss), then grad rewritten in place
+// from the fp16 e = exp(z - tile max) it holds: grad = bf16_rn(e * exp(tile
+// max - lse)), the label column from the fp32 label logit.
+cudaError_t launch_xent_rescale(const float *part_max, const float *part_sum, const float *label_logit,
+                                const int32_t *labels, int M, int N, int num_n_blocks, float *loss, void *grad,
+                                cudaStream_t s);
 
 cudaError_t launch_matmul_k1_f32(const float *a, const float *b, float *out, int64_t M, int64_t N,
                                  int num_sms, cudaStream_t s);

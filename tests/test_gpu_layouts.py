@@ -127,13 +127,27 @@ def test_invalid_layout_and_alignment_raise():
         lf.gemm_layout(x, w, x_mn=True, w_mn=True)
 
 
+@pytest.fixture
+def grad_path(request):
+    """Force one gradient form of the cross-entropy for the test."""
+    lf.set_xent_grad_path(request.param)
+    yield request.param
+    lf.set_xent_grad_path(0)
+
+
+# launches per call of each gradient form: one pass; exp pass + rescale;
+# partials + combine + recompute pass
+GRAD_LAUNCHES = {1: 1, 2: 2, 3: 3}
+
+
+@pytest.mark.parametrize("grad_path", [1, 2], ids=["one_pass", "exp_rescale"], indirect=True)
 @pytest.mark.parametrize("x_mn,w_mn", LAYOUTS)
 @pytest.mark.parametrize("M,N,K", [(600, 1032, 264), (256, 2048, 128), (520, 776, 136)])
-def test_xent_layouts_match_oracle(M, N, K, x_mn, w_mn):
+def test_xent_layouts_match_oracle(M, N, K, x_mn, w_mn, grad_path):
     """gemm_nt_xent with X stored [K,M] and/or W stored [K,N] (read in place),
-    the gradient by the one-pass kernel: loss (rel 1e-3) and gradient (abs
-    2e-3) of every row against the oracle on the logical operands, with labels
-    on tile edges."""
+    the gradient by the one-pass kernel or by the exp pass + rescale: loss
+    (rel 1e-3) and gradient (abs 2e-3) of every row against the oracle on the
+    logical operands, with labels on tile edges."""
     x = synthetic.bf16_normal((M, K), 1.0, 41)
     w = synthetic.bf16_normal((N, K), 1.0 / np.sqrt(K), 42)
     lab = synthetic.labels_uniform(M, N, seed=43)
@@ -147,7 +161,7 @@ def test_xent_layouts_match_oracle(M, N, K, x_mn, w_mn):
     torch.cuda.synchronize()
     lf.check_device_error()
     assert none is None
-    assert n1 - n0 == 1          # the one-pass kernel
+    assert n1 - n0 == GRAD_LAUNCHES[grad_path]
     rows = list(range(M))
     _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
     for got in (loss, loss_only):
@@ -158,12 +172,14 @@ def test_xent_layouts_match_oracle(M, N, K, x_mn, w_mn):
 
 def test_xent_layout_k_major_is_gemm_nt_xent():
     """Two K-major operands through the layout entry point are gemm_nt_xent
-    itself (the one-pass kernel: one launch), bit for bit."""
+    itself (the same launches), bit for bit."""
     M, N, K = 512, 4096, 256
     x = synthetic.bf16_normal((M, K), 1.0, 44).to(DEV)
     w = synthetic.bf16_normal((N, K), 1.0 / 16, 45).to(DEV)
     lab = synthetic.labels_uniform(M, N, seed=46).to(DEV)
+    na = lf.launch_count()
     loss_a, grad_a = lf.gemm_nt_xent(x, w, lab, want_grad=True)
+    na = lf.launch_count() - na
     lib = lf.lib()
     loss_b = torch.empty_like(loss_a)
     grad_b = torch.empty_like(grad_a)
@@ -172,11 +188,12 @@ def test_xent_layout_k_major_is_gemm_nt_xent():
                                    loss_b.data_ptr(), grad_b.data_ptr(), M, N, K,
                                    torch.cuda.current_stream().cuda_stream) == 0
     torch.cuda.synchronize()
-    assert lf.launch_count() - n0 == 1
+    assert lf.launch_count() - n0 == na
     assert torch.equal(loss_a, loss_b) and torch.equal(grad_a, grad_b)
 
 
-def test_xent_layout_large_vocab_w_stored_kn_sampled():
+@pytest.mark.parametrize("grad_path", [1, 2], ids=["one_pass", "exp_rescale"], indirect=True)
+def test_xent_layout_large_vocab_w_stored_kn_sampled(grad_path):
     """The LM-head shape with the weight stored [K, N] (as a tied embedding
     read transposed): 4096 x 32768 x 4096, sampled rows, every column."""
     M, N, K = 4096, 32768, 4096
@@ -194,11 +211,13 @@ def test_xent_layout_large_vocab_w_stored_kn_sampled():
     assert np.abs(f64(grad)[rows] - rgrad).max() <= 2e-3
 
 
+@pytest.mark.parametrize("grad_path", [2, 3], ids=["exp_rescale", "recompute"], indirect=True)
 @pytest.mark.parametrize("x_mn,w_mn", LAYOUTS)
-def test_xent_layouts_two_pass_wide_vocab(x_mn, w_mn):
+def test_xent_layouts_two_pass_wide_vocab(x_mn, w_mn, grad_path):
     """A vocabulary too wide for one pass (N = 40992) with the operands in
-    other layouts: partials, combine and the recompute pass, all reading the
-    stored layouts; sampled rows, every column, against the oracle."""
+    other layouts: the exp pass + rescale, or partials, combine and the
+    recompute pass, all reading the stored layouts; sampled rows, every
+    column, against the oracle."""
     M, N, K = 256, 40992, 136
     x = synthetic.bf16_normal((M, K), 1.0, 50)
     w = synthetic.bf16_normal((N, K), 1.0 / np.sqrt(K), 51)
@@ -209,7 +228,7 @@ def test_xent_layouts_two_pass_wide_vocab(x_mn, w_mn):
     loss, grad = lf.gemm_nt_xent(xs, ws, lab.to(DEV), want_grad=True, x_mn=x_mn, w_mn=w_mn)
     torch.cuda.synchronize()
     lf.check_device_error()
-    assert lf.launch_count() - n0 == 3
+    assert lf.launch_count() - n0 == GRAD_LAUNCHES[grad_path]
     rows = [0, 1, 127, 128, 255]
     _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
     rel = np.abs(f64(loss)[rows] - rloss) / np.abs(rloss)
@@ -217,8 +236,9 @@ def test_xent_layouts_two_pass_wide_vocab(x_mn, w_mn):
     assert np.abs(f64(grad)[rows] - rgrad).max() <= 2e-3
 
 
+@pytest.mark.parametrize("grad_path", [1], ids=["one_pass"], indirect=True)
 @pytest.mark.parametrize("x_mn,w_mn", LAYOUTS)
-def test_xent_layouts_one_pass_multi_round(x_mn, w_mn):
+def test_xent_layouts_one_pass_multi_round(x_mn, w_mn, grad_path):
     """Several rounds of the one-pass kernel with MN-major operands (M = 1536:
     6 row blocks; N = 16384 at 256- or 224-wide tiles), every row."""
     M, N, K = 1536, 16384, 136

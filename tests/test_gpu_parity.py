@@ -261,6 +261,7 @@ def test_xent_onepass_gradient_is_one_launch():
     lab = synthetic.labels_uniform(M, N)
     xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
     lf.set_tuning(-1, 2)
+    lf.set_xent_grad_path(1)
     try:
         lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
         b0 = lf.launch_count()
@@ -271,6 +272,7 @@ def test_xent_onepass_gradient_is_one_launch():
         lf.check_device_error()
     finally:
         lf.set_tuning(-1, -1)
+        lf.set_xent_grad_path(0)
     assert (b1 - b0, b2 - b1) == (1, 2)
     rows = sample_rows(M, k=16, seed=9)
     _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
@@ -351,12 +353,14 @@ def test_xent_onepass_every_tile_width(width):
     assert_grad_close(f64(grad), rgrad, "width %d" % width)
 
 
+@pytest.mark.parametrize("path", [2, 3], ids=["exp_rescale", "recompute"])
 @pytest.mark.parametrize("variant", [2, 3])
-def test_xent_two_pass_gradient_on_pairs(variant):
+def test_xent_two_pass_gradient_on_pairs(variant, path):
     """A vocabulary too wide for one pass (N = 40992: 161 tiles, more than two
-    per resident pair; the last tile 32 columns wide) takes the two-pass form
-    on CTA pairs: partials, combine, and the recompute pass writing the
-    gradient.  Sampled rows, every column, against the oracle."""
+    per resident pair; the last tile 32 columns wide) on CTA pairs, by whole
+    tiles or stream-K: the exp pass (partials and fp16 exp(z - tile max) into
+    grad) and the rescale pass; or partials, combine, and the recompute pass
+    writing the gradient.  Sampled rows, every column, against the oracle."""
     M, N, K = 512, 40992, 256
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
     lab = synthetic.labels_uniform(M, N, seed=12)
@@ -365,6 +369,7 @@ def test_xent_two_pass_gradient_on_pairs(variant):
     lab[7] = 256 * 160                      # first column of the ragged last tile
     xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
     lf.set_tuning(-1, variant)
+    lf.set_xent_grad_path(path)
     try:
         b0 = lf.launch_count()
         loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
@@ -372,7 +377,9 @@ def test_xent_two_pass_gradient_on_pairs(variant):
         lf.check_device_error()
     finally:
         lf.set_tuning(-1, -1)
-    assert b1 - b0 == 3                     # partials GEMM, combine, gradient GEMM
+        lf.set_xent_grad_path(0)
+    # exp pass + rescale, or partials GEMM, combine, gradient GEMM
+    assert b1 - b0 == (2 if path == 2 else 3)
     rows = sample_rows(M, k=12, seed=13, extra=(5, 6, 7))
     _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
     assert_loss_close(f64(loss)[rows], rloss, "two-pass")
@@ -461,3 +468,131 @@ def test_xent_onepass_multi_round(width):
     _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
     assert_loss_close(f64(loss), rloss, "multi-round width %d" % width)
     assert_grad_close(f64(grad), rgrad, "multi-round width %d" % width)
+
+
+# ------------------------------------------ gradient by exp pass + rescale
+
+@pytest.fixture
+def exp_path():
+    lf.set_xent_grad_path(2)
+    yield
+    lf.set_xent_grad_path(0)
+    lf.set_tile_band(-1)
+
+
+@pytest.mark.parametrize("M,N,K", [(600, 1032, 264), (257, 8, 72), (129, 4104, 520), (1500, 16384, 136)])
+def test_xent_exp_rescale_ragged_full(M, N, K, exp_path):
+    """The exp pass + rescale on ragged shapes (last row block and last
+    256-column tile partial; N = 8: a single 8-column tile), labels at 0,
+    N - 1 and tile edges; every row, every column against the oracle."""
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N, seed=61)
+    for i, e in enumerate([0, N - 1, min(255, N - 1), min(256, N - 1), min(N - 8, 4096)]):
+        lab[i] = e
+    n0 = lf.launch_count()
+    loss, grad = lf.gemm_nt_xent(x.to(DEV), w.to(DEV), lab.to(DEV), want_grad=True)
+    torch.cuda.synchronize()
+    assert lf.launch_count() - n0 == 2
+    lf.check_device_error()
+    _, rloss, _, rgrad = oracle.xent(x, w, lab.numpy())
+    assert_loss_close(f64(loss), rloss, "exp/rescale %dx%dx%d" % (M, N, K))
+    assert_grad_close(f64(grad), rgrad, "exp/rescale %dx%dx%d" % (M, N, K))
+
+
+def test_xent_exp_rescale_near_ties_across_tiles(exp_path):
+    """Rows whose softmax mass sits on three near-equal logits in different
+    256-column tiles (columns 3, 5 and 700; probabilities about 1/3 each, the
+    range where the fp16 intermediate's rounding matters most), the label on
+    one of them or elsewhere; and rows dominated by one logit (p close to 1,
+    which must be its tile's maximum with e = 1 exactly)."""
+    M, N, K = 512, 1024, 128
+    w = synthetic.bf16_normal((N, K), 1.0 / math.sqrt(K), 62).float()
+    w[5] = w[3]
+    w[700] = w[3] + 0.01 * synthetic.bf16_normal((K,), 1.0, 63).float()
+    d = w[3] / w[3].norm()
+    g = torch.Generator().manual_seed(64)
+    scale = torch.where(torch.arange(M) % 2 == 0, torch.tensor(12.0), torch.tensor(40.0))
+    x = scale[:, None] * d[None, :] + 0.05 * torch.randn(M, K, generator=g)
+    x[::4] = 40.0 * w[900] / w[900].norm() + 0.05 * torch.randn(M // 4, K, generator=g)   # one dominant logit
+    x, w = x.to(torch.bfloat16), w.to(torch.bfloat16)
+    lab = synthetic.labels_uniform(M, N, seed=65)
+    lab[1::4], lab[2::4] = 3, 700
+    lab[::8] = 900
+    loss, grad = lf.gemm_nt_xent(x.to(DEV), w.to(DEV), lab.to(DEV), want_grad=True)
+    torch.cuda.synchronize()
+    lf.check_device_error()
+    _, rloss, _, rgrad = oracle.xent(x, w, lab.numpy())
+    p = rgrad + (np.arange(N)[None, :] == lab.numpy()[:, None])
+    assert (p.max(axis=1) > 0.9).sum() >= M // 8 and ((p > 0.25) & (p < 0.5)).sum() >= M
+    assert_loss_close(f64(loss), rloss, "near ties")
+    assert_grad_close(f64(grad), rgrad, "near ties")
+
+
+def test_xent_exp_rescale_zero_weight_and_large_logits(exp_path):
+    M, N, K = 192, 2048, 128
+    x = synthetic.bf16_normal((M, K), 1.0, 0)
+    w = torch.zeros(N, K, dtype=torch.bfloat16)
+    lab = synthetic.labels_uniform(M, N)
+    loss, grad = lf.gemm_nt_xent(x.to(DEV), w.to(DEV), lab.to(DEV), want_grad=True)
+    assert np.allclose(f64(loss), math.log(N), rtol=1e-6, atol=0)
+    want = np.full((M, N), 1.0 / N)
+    want[np.arange(M), lab.numpy()] -= 1.0
+    assert_grad_close(f64(grad), want, "zero weight")
+    x, w = synthetic.make_gemm_inputs(256, 1536, 256, 30.0, 1.0 / 16)
+    lab = synthetic.labels_uniform(256, 1536)
+    _xent_check(x, w, lab, what="exp/rescale large logits")
+
+
+def test_xent_exp_rescale_banded_tile_order(exp_path):
+    """Whole tiles in bands of 2 and 3 row blocks (the order used when X is too
+    large to stay in L2): the same results as one band, bit for bit."""
+    M, N, K = 1800, 3080, 136        # 8 row blocks, the last ragged
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N, seed=66)
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    outs = []
+    for band in (0, 2, 3):
+        lf.set_tile_band(band)
+        loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        out = lf.gemm_nt(xd, wd)
+        outs.append((loss, grad, out))
+    lf.check_device_error()
+    for loss, grad, out in outs[1:]:
+        assert torch.equal(loss, outs[0][0]) and torch.equal(grad, outs[0][1]) and torch.equal(out, outs[0][2])
+    rows = sample_rows(M, k=20, seed=67)
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    assert_loss_close(f64(outs[0][0])[rows], rloss, "banded")
+    assert_grad_close(f64(outs[0][1])[rows], rgrad, "banded")
+    assert_gemm_close(f64(outs[0][2])[rows], oracle.gemm_nt_rows(x, w, rows), "banded gemm")
+
+
+def test_xent_exp_rescale_grad_full_size(exp_path):
+    """The 4096 x 32768 x 4096 workload through the exp pass + rescale, in the
+    bench's configuration; sampled rows with labels at 0, N - 1 and a tile edge."""
+    wl = synthetic.WORKLOADS["xent_grad"]
+    inp = workload("xent_grad")
+    lab = inp["labels"].clone()
+    lab[1], lab[2], lab[3] = 0, wl.N - 1, 256 * 77
+    rows = sample_rows(wl.M, k=28, seed=68, extra=(1, 2, 3))
+    _xent_check(inp["x"], inp["w"], lab, rows=rows, what="xent_grad exp/rescale")
+
+
+def test_xent_grad_large_vocab_full_size():
+    """The 8192 x 128256 x 4096 vocabulary with the gradient, automatic form
+    (the exp pass + rescale: two launches), as the bench runs it; sampled rows,
+    every column, labels at 0, N - 1 and tile edges."""
+    wl = synthetic.WORKLOADS["xent_loss"]
+    inp = workload("xent_loss")
+    lab = inp["labels"].clone()
+    lab[1], lab[2], lab[3], lab[4] = 0, wl.N - 1, 256 * 400, 256 * 500 + 255
+    xd, wd, ld = inp["x"].to(DEV), inp["w"].to(DEV), lab.to(DEV)
+    n0 = lf.launch_count()
+    loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+    torch.cuda.synchronize()
+    assert lf.launch_count() - n0 == 2
+    lf.check_device_error()
+    rows = sample_rows(wl.M, k=12, seed=69, extra=(1, 2, 3, 4))
+    _, rloss, _, rgrad = oracle.xent_rows(inp["x"], inp["w"], lab.numpy(), rows)
+    assert_loss_close(f64(loss)[rows], rloss, "large vocab grad")
+    assert_grad_close(f64(grad[torch.from_numpy(rows).to(DEV)]), rgrad, "large vocab grad")
+

@@ -48,10 +48,13 @@ def test_stalled_wait_times_out_and_context_survives(variant):
     assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
 
 
-def test_stalled_wait_in_onepass_cross_entropy_times_out():
+@pytest.mark.parametrize("path", [1, 2], ids=["one_pass", "exp_rescale"])
+def test_stalled_wait_in_cross_entropy_gradient_times_out(path):
     # the one-pass gradient kernel: a stalled pair also stalls its group's
-    # flag waits; every wait is bounded, the error is reported, the context lives
+    # flag waits; the exp pass: a stalled CTA; every wait is bounded, the
+    # error is reported, the context lives
     torch.cuda.set_device(0)
+    lf.set_xent_grad_path(path)
     M, N, K = 512, 2048, 256
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
     lab = synthetic.labels_uniform(M, N)
@@ -71,6 +74,7 @@ def test_stalled_wait_in_onepass_cross_entropy_times_out():
         lf.check_device_error()
     finally:
         lf.set_tuning(-1, -1)
+        lf.set_xent_grad_path(0)
     _, rloss, _, _ = oracle.xent(x, w, lab.numpy(), want_grad=False)
     got = loss.double().cpu().numpy()
     assert np.max(np.abs(got - rloss) / np.abs(rloss)) <= 1e-3
