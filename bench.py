@@ -436,8 +436,12 @@ def secondary_paths(args, torch, lf, synthetic, timer, stream, peaks):
                       "traffic": recorded_traffic("k_fp8_cast_dual_v16", label)}
         del x, out, out_t
     torch.cuda.empty_cache()
-    for name, want_grad in ((("xent_grad", True), ("xent_loss", False), ("xent_loss", True)) if "xent" in want
-                            else ()):
+    # "xent" selects all three cross-entropy legs; "xent_grad", "xent_loss" and
+    # "xent_grad_large_vocab" one each
+    xent_legs = [(name, g) for name, g, tag in (("xent_grad", True, "xent_grad"), ("xent_loss", False, "xent_loss"),
+                                                 ("xent_loss", True, "xent_grad_large_vocab"))
+                 if "xent" in want or tag in want]
+    for name, want_grad in xent_legs:
         wl = synthetic.WORKLOADS[name]
         inp = synthetic.make_workload(name)
         x, w, lab = inp["x"].to("cuda"), inp["w"].to("cuda"), inp["labels"].to("cuda")
@@ -764,7 +768,7 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip every secondary path")
     ap.add_argument("--paths", default="tiny,xent,k1,layouts,rope,fp8,library",
                     help="secondary paths to time after the headline (comma list of tiny, xent, k1, layouts, rope, "
-                         "fp8, library)")
+                         "fp8, library; xent_grad, xent_loss, xent_grad_large_vocab select one cross-entropy leg)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     args = ap.parse_args(argv)

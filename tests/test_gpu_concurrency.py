@@ -181,8 +181,6 @@ def test_onepass_while_other_kernels_hold_sms():
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
     lab = synthetic.labels_uniform(M, N, seed=41)
     xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
-    lf.gemm_nt_xent(xd, wd, ld, want_grad=True)     # set-up outside the timed window
-    n0 = lf.launch_count()
     rows = np.array([0, 255, 256, 511])
 
     def check(res):
@@ -190,10 +188,18 @@ def test_onepass_while_other_kernels_hold_sms():
         assert (np.abs(f64(res[0])[rows] - rloss) / np.abs(rloss)).max() <= 1e-3
         assert np.abs(f64(res[1])[rows] - rgrad).max() <= 2e-3
 
-    _under_occupation(lambda: lf.gemm_nt_xent(xd, wd, ld, want_grad=True), check)
-    assert lf.launch_count() - n0 in (2, 4)          # occupier + one pass, or + the two-pass form
-    loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)   # the context is usable
-    lf.check_device_error()
+    lf.set_xent_grad_path(1)                          # the one-pass kernel (its pairs wait on each other)
+    try:
+        lf.gemm_nt_xent(xd, wd, ld, want_grad=True)   # set-up outside the occupied window
+        n0 = lf.launch_count()
+        _under_occupation(lambda: lf.gemm_nt_xent(xd, wd, ld, want_grad=True), check)
+        # occupier + the one pass (or + the exp pass and rescale, had the
+        # cooperative launch been refused)
+        assert lf.launch_count() - n0 in (2, 3)
+        loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)   # the context is usable
+        lf.check_device_error()
+    finally:
+        lf.set_xent_grad_path(0)
     check((loss, grad))
 
 

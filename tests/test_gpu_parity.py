@@ -503,8 +503,8 @@ def test_xent_exp_rescale_near_ties_across_tiles(exp_path):
     """Rows whose softmax mass sits on three near-equal logits in different
     256-column tiles (columns 3, 5 and 700; probabilities about 1/3 each, the
     range where the fp16 intermediate's rounding matters most), the label on
-    one of them or elsewhere; and rows dominated by one logit (p close to 1,
-    which must be its tile's maximum with e = 1 exactly)."""
+    one of them or elsewhere; and rows dominated by one logit (p > 1/2, which
+    must be its tile's maximum, where e = 1 exactly)."""
     M, N, K = 512, 1024, 128
     w = synthetic.bf16_normal((N, K), 1.0 / math.sqrt(K), 62).float()
     w[5] = w[3]
@@ -513,7 +513,10 @@ def test_xent_exp_rescale_near_ties_across_tiles(exp_path):
     g = torch.Generator().manual_seed(64)
     scale = torch.where(torch.arange(M) % 2 == 0, torch.tensor(12.0), torch.tensor(40.0))
     x = scale[:, None] * d[None, :] + 0.05 * torch.randn(M, K, generator=g)
-    x[::4] = 40.0 * w[900] / w[900].norm() + 0.05 * torch.randn(M // 4, K, generator=g)   # one dominant logit
+    # every 4th row: one dominant logit (column 900, p about 0.94 -- large
+    # enough to sit at its tile's max, small enough that the loss, about 0.06,
+    # is resolved in fp32: a loss near 0 cancels lse against z[label] to noise)
+    x[::4] = 10.0 * w[900] / w[900].norm() + 0.05 * torch.randn(M // 4, K, generator=g)
     x, w = x.to(torch.bfloat16), w.to(torch.bfloat16)
     lab = synthetic.labels_uniform(M, N, seed=65)
     lab[1::4], lab[2::4] = 3, 700
@@ -523,7 +526,7 @@ def test_xent_exp_rescale_near_ties_across_tiles(exp_path):
     lf.check_device_error()
     _, rloss, _, rgrad = oracle.xent(x, w, lab.numpy())
     p = rgrad + (np.arange(N)[None, :] == lab.numpy()[:, None])
-    assert (p.max(axis=1) > 0.9).sum() >= M // 8 and ((p > 0.25) & (p < 0.5)).sum() >= M
+    assert (p.max(axis=1) > 0.8).sum() >= M // 8 and ((p > 0.25) & (p < 0.5)).sum() >= M
     assert_loss_close(f64(loss), rloss, "near ties")
     assert_grad_close(f64(grad), rgrad, "near ties")
 
