@@ -231,6 +231,8 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     lf.lib()
+    if args.no_cooperative:
+        lf.set_cooperative(False)
     peaks = load_peaks()
     stream = torch.cuda.Stream()
     timer = Timer(torch, stream)
@@ -314,7 +316,8 @@ def run_ours(args, rank, world, local_rank):
                          "read that retires the write's dirty lines (L2 is 129 MB)",
                    "timing": "CUDA events around each call on the launching stream; a 0.1 ms device delay "
                              "precedes each start event so host launch latency is not counted",
-                   "parallelism": "replicas" if world > 1 else "single"},
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "cooperative_launches": not args.no_cooperative},
         "pct_of_peak": round(100.0 * achieved / peak, 1),
         "roofline": {"bound": "tensor", "kernel": HEADLINE_KERNEL, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": "bf16 burst (%s)" % peaks["source"], "unit": "TFLOP/s",
@@ -770,6 +773,9 @@ def main(argv=None):
                     help="secondary paths to time after the headline (comma list of tiny, xent, k1, layouts, rope, "
                          "fp8, library; xent_grad, xent_loss, xent_grad_large_vocab select one cross-entropy leg)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cooperative", action="store_true",
+                    help="launch the stream-K and one-pass kernels without the cooperative attribute (for ncu, "
+                         "which cannot replay cooperative cluster launches); same kernels")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -425,6 +425,16 @@ void lf_set_tile_band(int m_blocks);
 void lf_set_test_hooks(int inject_stall, uint64_t wait_timeout_ns);
 
 /*
+ * enable = 0: later launches of the kernels whose CTAs wait on each other (the
+ * stream-K split, the one-pass cross-entropy) omit the cooperative launch
+ * attribute; 1 (the default) restores it.  Meant for profilers that cannot
+ * replay cooperative cluster launches (they serialise kernels anyway): the
+ * kernels are the same, but nothing then guarantees that all their CTAs are
+ * resident together when other work holds part of the GPU.
+ */
+void lf_set_cooperative(int enable);
+
+/*
  * Test hook (not for production use): enqueues on `stream` a kernel of `ctas`
  * CTAs, each holding 200 KiB of shared memory -- one per SM, with no room
  * beside it for a GEMM CTA -- that wait `duration_ns` on the GPU's global

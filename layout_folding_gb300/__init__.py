@@ -90,6 +90,8 @@ def lib():
         L.lf_set_xent_grad_path.restype = None
         L.lf_set_tile_band.argtypes = [I32]
         L.lf_set_tile_band.restype = None
+        L.lf_set_cooperative.argtypes = [I32]
+        L.lf_set_cooperative.restype = None
         L.lf_test_occupy_sms.argtypes = [I32, ctypes.c_uint64, P]
         L.lf_test_occupy_sms.restype = I32
         L.gemm_nt_xent_noalloc.argtypes = [P, P, P, P, P, I64, I64, I64, P]
@@ -427,6 +429,12 @@ def set_xent_grad_path(path: int = 0):
 def set_tile_band(m_blocks: int = -1):
     """Whole-tile band height in 256-row blocks (0 = one band, -1 = automatic)."""
     lib().lf_set_tile_band(int(m_blocks))
+
+
+def set_cooperative(enable: bool = True):
+    """Launch the CTA-waiting kernels with (True) or without (False) the
+    cooperative attribute -- False only for profilers that cannot replay it."""
+    lib().lf_set_cooperative(1 if enable else 0)
 
 
 def set_test_hooks(inject_stall: bool, wait_timeout_ns: int = 0):

@@ -56,6 +56,7 @@ std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA, 2 CTA-pair whole 
 std::atomic<int> g_op_tile{0};       // one-pass cross-entropy N-tile width; 0 = automatic
 std::atomic<int> g_xent_path{0};     // cross-entropy gradient: 0 auto, 1 one pass, 2 exp + rescale, 3 recompute
 std::atomic<int> g_band{-1};         // whole-tile band height in M blocks: -1 auto, 0 one band, > 0 forced
+std::atomic<int> g_coop_enable{1};   // 0: launch the CTA-waiting kernels without the cooperative attribute
 // L2 bytes of X a band of whole tiles may keep while it sweeps W (the L2 is
 // 129 MB, but reuse measured as if about half of it were available)
 constexpr double BAND_X_BYTES = 32.0 * 1024 * 1024;
@@ -531,6 +532,7 @@ lf_status check_gemm_shape(int64_t M, int64_t N, int64_t K)
 namespace lf {
 
 unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+bool cooperative_launches() { return g_coop_enable.load() != 0; }
 int stall_injection() { return g_inject.load(); }
 void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 bool make_tmap_kmajor(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, uint32_t box_rows)
@@ -937,6 +939,8 @@ void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant)
 void lf_set_xent_grad_path(int path) { g_xent_path.store(path >= 1 && path <= 3 ? path : 0); }
 
 void lf_set_tile_band(int m_blocks) { g_band.store(m_blocks < 0 ? -1 : m_blocks); }
+
+void lf_set_cooperative(int enable) { g_coop_enable.store(enable ? 1 : 0); }
 
 void lf_set_onepass_tile(int width)
 {

@@ -968,7 +968,7 @@ cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const CU
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config<EPI>(grid, s, attr, p.streamk != 0);
+    cudaLaunchConfig_t cfg = pair_config<EPI>(grid, s, attr, p.streamk != 0 && cooperative_launches());
     return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI, LAYOUT>, ta, tb, to, p);
 }
 

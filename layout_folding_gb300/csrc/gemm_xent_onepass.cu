@@ -841,7 +841,7 @@ cudaError_t launch_onepass_t(const CUtensorMap &ta, const CUtensorMap &tb, const
     attr[1].id = cudaLaunchAttributeCooperative;
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = cooperative_launches() ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, k_xent_onepass<LAYOUT>, ta, tb, to, p);
 }
 

@@ -127,6 +127,7 @@ cudaError_t launch_occupy_sms(int ctas, unsigned long long ns, cudaStream_t s);
 // Library state and helpers shared by the entry points of every translation
 // unit (defined in api.cu).
 unsigned long long wait_timeout_ns();  // device-side wait limit (lf_set_test_hooks; 2 s by default)
+bool cooperative_launches();           // false after lf_set_cooperative(0)
 int stall_injection();                 // 1 while lf_set_test_hooks asks for a stalled first stage
 void count_launches(int n);            // adds n to the lf_launch_count total
 // 2-D bf16 tensor [rows, K] (K contiguous) as a TMA map: boxes of 64 columns x
