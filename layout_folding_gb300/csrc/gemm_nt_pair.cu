@@ -173,6 +173,52 @@ struct WorkIter {
     }
 };
 
+// Stream-K, plain store epilogues: the sum of the contributors' partials for
+// this thread's row (chunks of 32 columns [32 k0, 32 nch)), loaded from L2 and
+// written into the idle accumulator buffer at `tpart` while this tile's own
+// MMAs still run, so the epilogue adds it with a TMEM load.  Two chunks (16
+// loads of 16 bytes) are in flight at a time.
+__device__ __forceinline__ void preload_partials(const PartialAdd &pa, uint32_t tpart, int k0, int nch)
+{
+#pragma unroll 1
+    for (int c = k0; c < nch; c += 2) {
+        const bool two = c + 1 < nch;  // warp-uniform
+        float v0[32], v1[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            v0[i] = 0.f;
+            v1[i] = 0.f;
+        }
+#pragma unroll 1
+        for (int e = 0; e < pa.count; ++e) {  // in pair order, as the fix-up adds them
+            const float4 *s4 = reinterpret_cast<const float4 *>(pa.slot + static_cast<size_t>(e) * pa.stride);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 f = __ldcg(s4 + (c * 8 + i) * BM + pa.row);
+                const float4 g = two ? __ldcg(s4 + ((c + 1) * 8 + i) * BM + pa.row) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v0[4 * i + 0] += f.x;
+                v0[4 * i + 1] += f.y;
+                v0[4 * i + 2] += f.z;
+                v0[4 * i + 3] += f.w;
+                v1[4 * i + 0] += g.x;
+                v1[4 * i + 1] += g.y;
+                v1[4 * i + 2] += g.z;
+                v1[4 * i + 3] += g.w;
+            }
+        }
+        uint32_t u0[32], u1[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            u0[i] = __float_as_uint(v0[i]);
+            u1[i] = __float_as_uint(v1[i]);
+        }
+        tmem_st_32x32b_x32(tpart + static_cast<uint32_t>(c * 32), u0);
+        if (two)
+            tmem_st_32x32b_x32(tpart + static_cast<uint32_t>((c + 1) * 32), u1);
+    }
+    tmem_wait_st();
+}
+
 // Stream-K: number of groups after this pair's group that hold the rest of
 // `tile` (their shares start before the tile's N-tile ends).  Contributor e is
 // pair (g + 1 + e) * MB + m.
@@ -720,72 +766,22 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t skw_phase = 0;
-        // Stream-K fix-up traffic is kept out of the mainloop: partial stores
-        // made while this SM's MMAs run slowed them by ~15 % (per-pair
-        // timestamps at 768 x 5120 x 13824).  A pair whose first segment
-        // starts inside a tile (a contributor) and that has exactly one more
-        // segment keeps that first accumulator in its TMEM buffer -- its MMAs
-        // never need the buffer again -- and writes the partial after its
-        // last MMA; owners pull their contributors' partials after their own
-        // last MMA.  Every pair writes before it waits, so there is no cycle.
-        int nseg = 0;
-        {
-            WorkIter cnt(p, pair, num_pairs);
-            for (Seg g; cnt.next(g);)
-                ++nseg;
-        }
-        int def_acc = -1;  // accumulator buffer holding a deferred partial
         WorkIter it(p, pair, num_pairs);
-        int si = 0;
-        for (Seg g; it.next(g); ++si) {
+        for (Seg g; it.next(g);) {
             int mb, nbt;  // M block, batch-major N block
             tile_coords(p, g.tile, mb, nbt);
             const int nb = nbt % p.num_n_blocks;
             const int bz = nbt / p.num_n_blocks;
             const int rloc = q * 32 + lane;
             const int row = mb * PAIR_M + static_cast<int>(rank) * BM + rloc;
-            const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-            const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + lane_off;
-            PartialAdd pa = {nullptr, 0, 0, rloc, nullptr};
+            const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
+            PartialAdd pa = {nullptr, 0, 0, rloc, nullptr, 0, 0u};
             const bool owner_split = g.kb0 == 0 && g.kb1 < p.num_k_blocks;
-            const bool defer = g.kb0 != 0 && si == 0 && nseg == 2;
             const int MB = p.num_m_blocks;
             const int first = (pair / MB + 1) * MB + pair % MB;  // first contributor pair
-            const bool ok = wait_bar(TFULL_BAR(acc), acc_phase, abort_flag, p, ERR_EPI, peer_abort);
-            if (!__all_sync(0xffffffffu, ok))
-                break;
-            tc_fence_after();
-            if (defer) {
-                // keep the accumulator (no TMEM-empty arrive): written below,
-                // after the last segment's MMAs
-                def_acc = acc;
-                if (++acc == PAIR_ACC_BUFS) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
-                continue;
-            }
-            if (g.kb0 != 0 || def_acc >= 0) {
-                // Hand a partial sum (this segment's, or the deferred first
-                // segment's) to the pair that owns the tile's start.
-                const uint32_t src = g.kb0 != 0 ? taddr : tmem_base + static_cast<uint32_t>(def_acc * BN) + lane_off;
-                epi_write_partial(src, p.sk_partials + static_cast<size_t>(pair * 2 + rank) * SK_SLOT_FLOATS, rloc, c0,
-                                  c1);
-                __threadfence();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(skw_bar);
-                if (warp == 2 && lane == 0 &&
-                    wait_bar(skw_bar, skw_phase, abort_flag, p, ERR_SK_SLOT, peer_abort)) {
-                    __threadfence();
-                    st_release_gpu(p.sk_flags + pair * 2 + rank, p.epoch);
-                }
-                skw_phase ^= 1u;
-                def_acc = -1;
-            }
             if (owner_split) {
                 // The tile's first K blocks, the rest held by the next pairs:
-                // acquire their flags (after this pair's last MMA).
+                // acquire their flags while this pair's MMAs still run.
                 const int n = sk_contributors(p, pair, num_pairs, g.tile);
                 bool got = true;
                 if (lane == 0)
@@ -798,8 +794,38 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                 pa.slot = p.sk_partials + static_cast<size_t>(first * 2 + rank) * SK_SLOT_FLOATS;
                 pa.stride = static_cast<size_t>(MB) * 2 * SK_SLOT_FLOATS;
                 pa.count = n;
+                if ((EPI == EPI_STORE || EPI == EPI_STORE_T) && n > 0) {
+                    // This is the pair's last segment, so the other
+                    // accumulator buffer is idle: sum the partials into it
+                    // while this tile's MMAs still run.
+                    const uint32_t tpart = tmem_base + static_cast<uint32_t>((acc ^ 1) * BN) +
+                                           (static_cast<uint32_t>(q * 32) << 16);
+                    preload_partials(pa, tpart, c0 / 32, min(c1 / 32, (p.N - nb * tn + 31) / 32));
+                    pa.in_tmem = 1;
+                    pa.tpart = tpart;
+                    pa.count = 0;
+                }
             }
-            if (g.kb0 == 0) {
+            const bool ok = wait_bar(TFULL_BAR(acc), acc_phase, abort_flag, p, ERR_EPI, peer_abort);
+            if (!__all_sync(0xffffffffu, ok))
+                break;
+            tc_fence_after();
+            if (g.kb0 != 0) {
+                // Not the tile's first K blocks: hand the partial sum to the
+                // pair that owns the tile's start.
+                epi_write_partial(taddr, p.sk_partials + static_cast<size_t>(pair * 2 + rank) * SK_SLOT_FLOATS, rloc, c0,
+                                  c1);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(skw_bar);
+                if (warp == 2 && lane == 0 &&
+                    wait_bar(skw_bar, skw_phase, abort_flag, p, ERR_SK_SLOT, peer_abort)) {
+                    __threadfence();
+                    st_release_gpu(p.sk_flags + pair * 2 + rank, p.epoch);
+                }
+                skw_phase ^= 1u;
+            } else {
                 // chunks of 32 columns that lie inside the matrix: only those
                 // are copied, and each copy is waited for by the warps that
                 // read it (none is left in flight at exit)

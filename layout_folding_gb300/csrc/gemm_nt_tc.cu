@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const int row = mb * BM + q * 32 + lane;
             const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
-            const PartialAdd none = {nullptr, 0, 0, 0, nullptr};
+            const PartialAdd none = {nullptr, 0, 0, 0, nullptr, 0, 0u};
             if (EPI == EPI_STORE)
                 epi_store(p, taddr, row, nb, none);
             else if (EPI == EPI_XENT_PARTIAL)

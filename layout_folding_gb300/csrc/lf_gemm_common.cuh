@@ -117,12 +117,24 @@ struct PartialAdd {
     int count;
     int row;                // this thread's row within its CTA's 128 rows
     const float4 *smem0;    // if set: contributor 0's slot, already copied to shared memory
+    int in_tmem;            // if set: the partials' sum is in TMEM at `tpart` (this thread's lane)
+    uint32_t tpart;
 };
 
 // Read 32 accumulator columns [c, c+32) of this thread's row from TMEM and
 // add the partials, in pair order.
 __device__ __forceinline__ void load_chunk(uint32_t taddr, int c, const PartialAdd &pa, uint32_t (&v)[32])
 {
+    if (pa.in_tmem) {
+        uint32_t w[32];
+        tmem_ld_32x32b_x32(taddr + c, v);
+        tmem_ld_32x32b_x32(pa.tpart + c, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
+        return;
+    }
     tmem_ld_32x32b_x32(taddr + c, v);
     tmem_wait_ld();
     for (int e = 0; e < pa.count; ++e) {

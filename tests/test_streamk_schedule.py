@@ -12,13 +12,6 @@ device code relies on: every (tile, K block) is computed exactly once, no pair
 has an empty share, only a pair's first segment can start inside a tile, and a
 tile's owner waits exactly on the pairs holding the rest of it, each of which
 reaches that work first, before any wait of its own.
-
-Partials are written after the writer's MMAs: a pair whose first segment is a
-contributor and that has exactly two segments keeps that accumulator in its
-first TMEM buffer and writes it after its second segment's MMAs (its MMAs use
-each of the two buffers once, so they never wait for the kept one); every
-pair writes its partial before it waits on any flag, so the waits form no
-cycle.
 """
 import pytest
 
@@ -84,37 +77,3 @@ def test_stream_k_schedule(MB, NB, KB, pairs):
                     got.update(range(a2, b2))
                 assert got == set(range(k1, KB))
     assert all(cover.get((t, k)) == 1 for t in range(MB * NB) for k in range(KB))
-
-
-@pytest.mark.parametrize("MB", [1, 2, 3, 4, 16])
-@pytest.mark.parametrize("NB", [1, 2, 5, 20, 77])
-@pytest.mark.parametrize("KB", [1, 2, 8, 13, 216])
-@pytest.mark.parametrize("pairs", [3, 7, 76])
-def test_deferred_partials_need_no_third_buffer_and_form_no_cycle(MB, NB, KB, pairs):
-    G = plan(MB, NB, KB, pairs)
-    if G == 0:
-        return
-    S = segments(MB, NB, KB, G)
-    # writer of each tile's partial: the pairs whose segment of the tile starts at k0 > 0
-    waits = {}
-    for pair, ss in S.items():
-        deferred = len(ss) == 2 and ss[0][1] != 0
-        if deferred:
-            # the kept accumulator is buffer 0; the second (last) segment uses
-            # buffer 1 and starts at K block 0 (an owner or a whole tile)
-            assert ss[1][1] == 0
-        last = ss[-1]
-        if last[1] == 0 and last[2] < KB:
-            first = (pair // MB + 1) * MB + pair % MB
-            waits[pair] = [first + e * MB for e in range(contributors(MB, NB, KB, G, pair, last[0]))]
-        else:
-            waits[pair] = []
-    # a writer never waits before writing, so a pair's wait can only be stuck
-    # on a writer that never finishes its MMAs: none does; check the wait-for
-    # graph is acyclic anyway (writers hold no waits ahead of their write)
-    for pair, ws in waits.items():
-        for w in ws:
-            assert w != pair
-            seg_w = S[w]
-            assert seg_w[0][1] != 0          # the writer's contributing segment is its first
-
