@@ -89,16 +89,26 @@ lf_status gemm_nt(const void *x, const void *w, void *out,
  *             the -1 term (no ignore-index exists).
  *   loss    : fp32 [M], device; loss[m] = logsumexp_n z[m,n] - z[m,labels[m]]
  *             (per row, no mean).
- *   grad_or_null : NULL, or bf16 [M,N], device;
- *             grad[m,n] = bf16_rn(exp(z[m,n] - lse[m]) - [n == labels[m]]).
+ *   grad_or_null : NULL, or bf16 [M,N], device, 16-byte aligned, overlapping
+ *             none of x, w, labels, loss;
+ *             grad[m,n] = bf16_rn(exp(z[m,n] - lse[m]) - [n == labels[m]])
+ *             (within 2e-3 of the exact value).  While the call runs the
+ *             buffer may hold intermediate values (see Work).
  *             When NULL nothing of size [M,N] is written anywhere.
  * Work: without grad, one GEMM pass writing per-(row, 256-column tile)
  * partials (max, sum-exp) and the label logit, then one combine kernel.  With
- * grad, when a 256-row block of tiles fits on the co-resident CTA pairs (two
- * N tiles per pair: N <= 512 x pairs), ONE launch computes the logits once and
- * writes loss and gradient, the pairs of a row block exchanging their row
- * partials through flags in global memory; otherwise the two passes above
- * plus a GEMM pass that recomputes the logits and writes the gradient.
+ * grad on CTA pairs (always when M > 128 or an operand is MN-major), two
+ * launches: a GEMM pass whose epilogue writes
+ * the partials and fp16 exp(z - tile max) into the grad buffer itself, then a
+ * kernel that merges each row's partials into lse and the loss and rewrites
+ * grad in place as bf16 (the logits are computed once and never stored; rows
+ * longer than 12,582,912 columns take the recompute form below).  On
+ * request (lf_set_xent_grad_path(1)), when a 256-row block of tiles fits on
+ * the co-resident CTA pairs (two N tiles per pair: N <= 512 x pairs), ONE
+ * launch computes the logits once and writes loss and gradient, the pairs of a
+ * row block exchanging their row partials through flags in global memory.  On
+ * single-CTA tiles (small M): the partials pass, the combine and a GEMM pass
+ * that recomputes the logits and writes the gradient.
  * The one-pass kernel is launched cooperatively (every CTA resident at once);
  * if the runtime refuses that, the two-pass form runs instead.
  * Partials, flags and the one-pass kernel's stash (128 KiB per CTA) live in a

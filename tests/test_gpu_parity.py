@@ -599,3 +599,36 @@ def test_xent_grad_large_vocab_full_size():
     assert_loss_close(f64(loss)[rows], rloss, "large vocab grad")
     assert_grad_close(f64(grad[torch.from_numpy(rows).to(DEV)]), rgrad, "large vocab grad")
 
+
+
+@pytest.mark.parametrize("form", [(2, 1), (2, 2), (2, 3), (1, 0)],
+                         ids=["pair_one_pass", "pair_exp_rescale", "pair_recompute", "cta1_recompute"])
+def test_xent_labels_outside_range(form):
+    """A label outside [0, N) (no ignore-index exists): that row's loss is NaN
+    and its gradient row is the softmax without the -1 term, in every form;
+    the other rows are unaffected."""
+    variant, path = form
+    M, N, K = 264, 1032, 136
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N, seed=71)
+    bad = {0: -1, 1: N, 2: N + 5, 3: 1 << 30, 4: -(1 << 30), 200: N + 8}
+    for r, v in bad.items():
+        lab[r] = v
+    lf.set_tuning(-1, variant)
+    lf.set_xent_grad_path(path)
+    try:
+        loss, grad = lf.gemm_nt_xent(x.to(DEV), w.to(DEV), lab.to(DEV), want_grad=True)
+        loss_only, _ = lf.gemm_nt_xent(x.to(DEV), w.to(DEV), lab.to(DEV), want_grad=False)
+        lf.check_device_error()
+    finally:
+        lf.set_tuning(-1, -1)
+        lf.set_xent_grad_path(0)
+    _, rloss, _, rgrad = oracle.xent(x, w, lab.numpy())
+    got_l, got_lo = f64(loss), f64(loss_only)
+    badrows = np.array(sorted(bad))
+    good = np.setdiff1d(np.arange(M), badrows)
+    assert np.all(np.isnan(rloss[badrows]))
+    assert np.all(np.isnan(got_l[badrows])) and np.all(np.isnan(got_lo[badrows]))
+    assert_loss_close(got_l[good], rloss[good], "good rows")
+    assert_loss_close(got_lo[good], rloss[good], "good rows, loss only")
+    assert_grad_close(f64(grad), rgrad, "out-of-range labels")   # bad rows: softmax only
