@@ -95,7 +95,9 @@ lf_status gemm_nt(const void *x, const void *w, void *out,
  *             (within 2e-3 of the exact value).  While the call runs the
  *             buffer may hold intermediate values (see Work).
  *             When NULL nothing of size [M,N] is written anywhere.
- * Work: without grad, one GEMM pass writing per-(row, 256-column tile)
+ * Work: for N <= 256 every row lies in one 256-column tile, so one launch
+ * writes the loss (and the gradient) from the GEMM's epilogue.  Otherwise,
+ * without grad, one GEMM pass writing per-(row, 256-column tile)
  * partials (max, sum-exp) and the label logit, then one combine kernel.  With
  * grad on CTA pairs (always when M > 128 or an operand is MN-major), two
  * launches: a GEMM pass whose epilogue writes

@@ -675,6 +675,15 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
     if ((st = plan_gemm(d, x, w, M, N, K, &g, layout)) != LF_OK)
         return st;
     lf::GemmParams &p = g.p;
+    p.labels = labels;
+    if (p.num_n_blocks == 1) {
+        // N <= 256: one N tile holds whole rows, so the row reduction needs
+        // no merge across tiles -- loss and gradient come from one epilogue,
+        // one launch, no workspace.
+        p.loss = loss;
+        p.out = grad_or_null;
+        return launched(run_gemm(lf::EPI_XENT_ROW, g, stream), 1);
+    }
     // workspace: part_max, part_sum [M, NB]; label_logit, row_max, row_logsum [M]
     const size_t part = round_up(static_cast<size_t>(M) * p.num_n_blocks * sizeof(float), 256);
     const size_t vec = round_up(static_cast<size_t>(M) * sizeof(float), 256);

@@ -871,6 +871,8 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                     if (done) {
                         if (EPI == EPI_XENT_PARTIAL)
                             epi_xent_partial(p, taddr, row, nb, pa);
+                        else if (EPI == EPI_XENT_ROW)
+                            epi_xent_row(p, taddr, row, pa);
                         else if (EPI == EPI_XENT_EXP)
                             pair_xent_exp(p, &tmO, taddr, row - lane, nb, pa,
                                           gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES,
@@ -1005,6 +1007,20 @@ cudaError_t launch_gemm_nt_pair(int epi, int layout, const CUtensorMap &ta, cons
             return launch_pair_t<EPI_XENT_PARTIAL, 2>(ta, tb, to, p, grid, s);
         case 3:
             return launch_pair_t<EPI_XENT_PARTIAL, 3>(ta, tb, to, p, grid, s);
+        default:
+            return cudaErrorInvalidValue;
+        }
+    }
+    if (epi == EPI_XENT_ROW) {
+        switch (layout) {
+        case 0:
+            return launch_pair_t<EPI_XENT_ROW, 0>(ta, tb, to, p, grid, s);
+        case 1:
+            return launch_pair_t<EPI_XENT_ROW, 1>(ta, tb, to, p, grid, s);
+        case 2:
+            return launch_pair_t<EPI_XENT_ROW, 2>(ta, tb, to, p, grid, s);
+        case 3:
+            return launch_pair_t<EPI_XENT_ROW, 3>(ta, tb, to, p, grid, s);
         default:
             return cudaErrorInvalidValue;
         }

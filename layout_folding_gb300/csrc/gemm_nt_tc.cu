@@ -1,5 +1,6 @@
 // gemm_nt_tc.cu -- the NT GEMM  acc = X[M,K] · W[N,K]^T  on the sm_103a tensor
-// cores, with three epilogues (bf16 store, cross-entropy partials, gradient).
+// cores, with four epilogues (bf16 store, cross-entropy partials, gradient, and
+// the whole cross-entropy of rows that fit one tile).
 //
 // Source: "Strength reduction: fold transpose into a subsequent GEMM call"
 // (lightning-thunder issue 1252), Feature/Motivation: the weight is consumed in
@@ -209,6 +210,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 epi_store(p, taddr, row, nb, none);
             else if (EPI == EPI_XENT_PARTIAL)
                 epi_xent_partial(p, taddr, row, nb, none);
+            else if (EPI == EPI_XENT_ROW)
+                epi_xent_row(p, taddr, row, none);
             else
                 epi_xent_grad(p, taddr, row, nb, none);
             tc_fence_before();
@@ -273,6 +276,8 @@ cudaError_t launch_gemm_nt(int epi, const CUtensorMap &ta, const CUtensorMap &tb
         return launch_t<EPI_XENT_PARTIAL>(ta, tb, p, grid, s);
     case EPI_XENT_GRAD:
         return launch_t<EPI_XENT_GRAD>(ta, tb, p, grid, s);
+    case EPI_XENT_ROW:
+        return launch_t<EPI_XENT_ROW>(ta, tb, p, grid, s);
     default:
         return cudaErrorInvalidValue;
     }

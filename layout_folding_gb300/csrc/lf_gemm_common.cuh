@@ -415,6 +415,71 @@ __device__ __forceinline__ void epi_xent_grad_rows(const GemmParams &p, uint32_t
     }
 }
 
+// The whole row in one tile (N <= 256): with a single N tile the row's
+// reduction ("Allow reductions in matmul epilogues", fusion example: max,
+// exp, sum, log-sum-exp, the label logit, softmax minus one-hot) needs no
+// merge across tiles, so this epilogue writes loss[row] and, when p.out is
+// set, the gradient row, with no second kernel.  Three passes over TMEM (max
+// and label logit; sum of exp(z - max); gradient), partials of other CTA pairs
+// (stream-K) added identically in each.
+__device__ __forceinline__ void epi_xent_row(const GemmParams &p, uint32_t taddr, int row, const PartialAdd &pa)
+{
+    const bool row_ok = row < p.M;
+    const int lab = row_ok ? p.labels[row] : -1;
+    float mx = -CUDART_INF_F, zl = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN && c < p.N; c += 32) {
+        uint32_t v[32];
+        load_chunk(taddr, c, pa, v);
+        const int nvalid = p.N - c;
+        const int li = lab - c;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (i < nvalid)
+                mx = fmaxf(mx, __uint_as_float(v[i]));
+            if (i == li)
+                zl = __uint_as_float(v[i]);
+        }
+    }
+    const float mxl = mx * LOG2E;
+    float s = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN && c < p.N; c += 32) {
+        uint32_t v[32];
+        load_chunk(taddr, c, pa, v);
+        const int nvalid = p.N - c;
+        float cs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            cs += i < nvalid ? ex2_approx(fmaf(__uint_as_float(v[i]), LOG2E, -mxl)) : 0.f;
+        s += cs;
+    }
+    const float ls = logf(s);
+    const bool lab_ok = lab >= 0 && lab < p.N;
+    if (row_ok)
+        p.loss[row] = lab_ok ? (mx - zl) + ls : CUDART_NAN_F;
+    if (!p.out)
+        return;
+    const float off = (mx + ls) * LOG2E;
+    __nv_bfloat16 *grow = static_cast<__nv_bfloat16 *>(p.out) + static_cast<size_t>(row) * p.N;
+#pragma unroll 1
+    for (int c = 0; c < BN && c < p.N; c += 32) {
+        uint32_t v[32];
+        load_chunk(taddr, c, pa, v);
+        if (row_ok) {
+            const int li = lab - c;
+            float g[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                g[i] = ex2_approx(fmaf(__uint_as_float(v[i]), LOG2E, -off));
+                if (i == li)
+                    g[i] -= 1.f;
+            }
+            store_row32_bf16(grow + c, g, p.N - c);
+        }
+    }
+}
+
 // Gradient pass of the two-pass form: the row statistics come from the combine kernel.
 __device__ __forceinline__ void epi_xent_grad(const GemmParams &p, uint32_t taddr, int row, int nb,
                                               const PartialAdd &pa)

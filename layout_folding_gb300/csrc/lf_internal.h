@@ -20,6 +20,7 @@ enum Epilogue : int {
     EPI_XENT_GRAD = 2,     // grad = bf16_rn(exp(z - lse) - onehot)
     EPI_STORE_T = 3,       // swapped operands: acc = W . X^T, out[m][n] = bf16_rn(acc[n][m]) (pair kernel)
     EPI_XENT_EXP = 4,      // partials as EPI_XENT_PARTIAL, and e = exp(z - tile max) as fp16 into out (pair kernel)
+    EPI_XENT_ROW = 5,      // N <= 256: the tile holds whole rows; loss (and the gradient when out is set) directly
 };
 
 struct GemmParams {

@@ -156,6 +156,20 @@ def test_xent_loss_only_writes_only_its_output(variant):
         lf.set_tuning(-1, -1)
 
 
+@pytest.mark.parametrize("variant", [1, 2, 3], ids=["cta1", "pair", "pair_streamk"])
+@pytest.mark.parametrize("want_grad", [True, False], ids=["grad", "loss"])
+def test_xent_whole_row_writes_only_its_outputs(variant, want_grad):
+    # N = 136 <= 256: the single-launch whole-row epilogue, ragged M and N
+    M, N, K = 261, 136, 520
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N, seed=26)
+    lf.set_tuning(-1, variant)
+    try:
+        _xent_guarded(x, w, lab, want_grad, "whole row variant %d" % variant)
+    finally:
+        lf.set_tuning(-1, -1)
+
+
 @pytest.mark.parametrize("variant", [1, 2], ids=["cta1", "pair"])
 def test_xent_two_pass_gradient_writes_only_its_outputs(variant):
     # N = 40992: too wide for one pass on the pairs (the single-CTA kernel is

@@ -250,7 +250,7 @@ def test_xent_launch_counts():
     b1 = lf.launch_count()
     lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
     b2 = lf.launch_count()
-    assert (b1 - b0, b2 - b1) == (2, 3)
+    assert (b1 - b0, b2 - b1) == (1, 1)     # N = 256: the whole row in one tile, one launch
 
 
 def test_xent_onepass_gradient_is_one_launch():
@@ -632,3 +632,29 @@ def test_xent_labels_outside_range(form):
     assert_loss_close(got_l[good], rloss[good], "good rows")
     assert_loss_close(got_lo[good], rloss[good], "good rows, loss only")
     assert_grad_close(f64(grad), rgrad, "out-of-range labels")   # bad rows: softmax only
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 256, 128), (1, 8, 8), (200, 136, 264), (600, 256, 72), (129, 248, 4104)])
+def test_xent_whole_row_in_one_tile(M, N, K, variant):
+    """N <= 256: every row lies in one N tile, so loss and gradient come from
+    one epilogue in one launch (single CTA, CTA pairs, and CTA pairs with the
+    K loop split by stream-K, whose owners add the partials in each pass);
+    every row and column against the oracle, labels at 0 and N - 1."""
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N, seed=81)
+    lab[0] = N - 1
+    if M > 1:
+        lab[M - 1] = 0
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    n0 = lf.launch_count()
+    loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+    n1 = lf.launch_count()
+    loss_only, _ = lf.gemm_nt_xent(xd, wd, ld)
+    n2 = lf.launch_count()
+    lf.check_device_error()
+    assert (n1 - n0, n2 - n1) == (1, 1)
+    _, rloss, _, rgrad = oracle.xent(x, w, lab.numpy())
+    assert_loss_close(f64(loss), rloss, "whole row")
+    assert_loss_close(f64(loss_only), rloss, "whole row, loss only")
+    assert_grad_close(f64(grad), rgrad, "whole row")
+

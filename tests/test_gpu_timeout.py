@@ -109,3 +109,32 @@ def test_stalled_wait_times_out_in_layout_and_batched_variants(kind):
     ref = oracle.gemm_nt(x, w)
     got = out.reshape(M, N).float().cpu().double().numpy()
     assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["cta1", "pair"])
+def test_stalled_wait_in_whole_row_cross_entropy_times_out(variant):
+    # N <= 256 (the single-launch whole-row epilogue): same bounded waits
+    torch.cuda.set_device(0)
+    M, N, K = 256, 256, 256
+    x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
+    lab = synthetic.labels_uniform(M, N)
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    lf.check_device_error()
+    lf.set_tuning(-1, variant)
+    lf.set_test_hooks(True, 200_000_000)
+    try:
+        lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        with pytest.raises(lf.LayoutFoldError) as info:
+            lf.check_device_error()
+        assert info.value.status == 6
+    finally:
+        lf.set_test_hooks(False, 0)
+    try:
+        loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+        lf.check_device_error()
+    finally:
+        lf.set_tuning(-1, -1)
+    _, rloss, _, rgrad = oracle.xent(x, w, lab.numpy())
+    assert np.max(np.abs(loss.double().cpu().numpy() - rloss) / np.abs(rloss)) <= 1e-3
+    assert np.max(np.abs(grad.double().cpu().numpy() - rgrad)) <= 2e-3
+
