@@ -403,8 +403,9 @@ void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant);
 void lf_set_onepass_tile(int width);
 
 /*
- * How gemm_nt_xent / gemm_nt_xent_layout compute the gradient on CTA pairs,
- * applied to later calls: 1 = the one-pass kernel when a row block of tiles
+ * How gemm_nt_xent / gemm_nt_xent_layout compute the gradient on CTA pairs
+ * when N > 256 (for N <= 256 one launch always does it), applied to later
+ * calls: 1 = the one-pass kernel when a row block of tiles
  * fits the resident pairs (else as 0), 2 = the exp pass and the rescale pass
  * (a GEMM whose epilogue writes the tile partials and fp16 exp(z - tile max)
  * into grad, then one kernel that merges each row's partials into lse and

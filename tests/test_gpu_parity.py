@@ -480,10 +480,10 @@ def exp_path():
     lf.set_tile_band(-1)
 
 
-@pytest.mark.parametrize("M,N,K", [(600, 1032, 264), (257, 8, 72), (129, 4104, 520), (1500, 16384, 136)])
+@pytest.mark.parametrize("M,N,K", [(600, 1032, 264), (257, 264, 72), (129, 4104, 520), (1500, 16384, 136)])
 def test_xent_exp_rescale_ragged_full(M, N, K, exp_path):
     """The exp pass + rescale on ragged shapes (last row block and last
-    256-column tile partial; N = 8: a single 8-column tile), labels at 0,
+    256-column tile partial; N = 264: the last tile 8 columns wide), labels at 0,
     N - 1 and tile edges; every row, every column against the oracle."""
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
     lab = synthetic.labels_uniform(M, N, seed=61)
