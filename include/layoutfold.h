@@ -16,6 +16,13 @@
  *
  * Every compute call requires an sm_103 device (LF_ERR_ARCH otherwise).  There
  * is no CPU fallback.
+ *
+ * Debugging aids: with LF_DEBUG_SYNC set (to anything but "0") in the
+ * environment when the library is first used, every compute call
+ * synchronises its stream before returning and reports a device-side timeout
+ * or a launch error as its own status.  Built with LAYOUTFOLD_NVTX=1 in the
+ * build environment (the LF_NVTX macro), every call is an NVTX range named
+ * after the entry point.
  */
 #ifndef LAYOUTFOLD_H
 #define LAYOUTFOLD_H

@@ -18,6 +18,9 @@ LIB_PATH = os.path.join(LIB_DIR, "liblayoutfold.so")
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
+# LAYOUTFOLD_NVTX=1 at build time: an NVTX range around every C-ABI call (header-only NVTX 3)
+if os.environ.get("LAYOUTFOLD_NVTX", "0") not in ("", "0"):
+    CFLAGS.append("-DLF_NVTX")
 
 
 def _sources():

@@ -517,6 +517,34 @@ lf_status run_planned(int epi, GemmPlan &g, cudaStream_t stream)
     return launched(run_gemm(epi, g, stream), 1);
 }
 
+}  // namespace
+
+namespace lf {
+
+// LF_DEBUG_SYNC (read once): after every call, synchronise its stream and read
+// the device error word, so asynchronous failures surface as the call's status.
+bool debug_sync_enabled()
+{
+    static const bool on = [] {
+        const char *v = std::getenv("LF_DEBUG_SYNC");
+        return v && v[0] && std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+}  // namespace lf
+
+extern "C" lf_status lf_check_device_error(cudaStream_t stream);
+
+namespace {
+
+lf_status debug_sync(lf_status st, cudaStream_t stream)
+{
+    if (st != LF_OK || !lf::debug_sync_enabled())
+        return st;
+    return lf_check_device_error(stream);
+}
+
 lf_status check_gemm_shape(int64_t M, int64_t N, int64_t K)
 {
     if (M <= 0 || N <= 0 || K <= 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
@@ -544,7 +572,7 @@ bool make_tmap_kmajor(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, 
 
 extern "C" {
 
-lf_status gemm_nt(const void *x, const void *w, void *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+static lf_status gemm_nt_call(const void *x, const void *w, void *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     if (!x || !w || !out)
         return LF_ERR_NULL;
@@ -580,7 +608,7 @@ lf_status gemm_nt(const void *x, const void *w, void *out, int64_t M, int64_t N,
     return run_planned(lf::EPI_STORE, g, stream);
 }
 
-lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, void *out, int64_t M, int64_t N,
+static lf_status gemm_layout_call(const void *x, int x_layout, const void *w, int w_layout, void *out, int64_t M, int64_t N,
                       int64_t K, cudaStream_t stream)
 {
     if (!x || !w || !out)
@@ -608,7 +636,7 @@ lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, 
     return run_planned(lf::EPI_STORE, g, stream);
 }
 
-lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_x, const void *w, int w_layout,
+static lf_status gemm_batched_call(const void *x, int x_layout, int64_t ldx, int64_t stride_x, const void *w, int w_layout,
                        int64_t ldw, int64_t stride_w, void *out, int64_t ldo, int64_t stride_o, int64_t batch,
                        int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
@@ -802,13 +830,13 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
 
 extern "C" {
 
-lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
+static lf_status gemm_nt_xent_call(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
                        int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     return xent_impl(x, false, w, false, labels, loss, grad_or_null, M, N, K, stream);
 }
 
-lf_status gemm_nt_xent_layout(const void *x, int x_layout, const void *w, int w_layout, const int32_t *labels,
+static lf_status gemm_nt_xent_layout_call(const void *x, int x_layout, const void *w, int w_layout, const int32_t *labels,
                               float *loss, void *grad_or_null, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     if ((x_layout != LF_K_MAJOR && x_layout != LF_MN_MAJOR) || (w_layout != LF_K_MAJOR && w_layout != LF_MN_MAJOR))
@@ -817,7 +845,7 @@ lf_status gemm_nt_xent_layout(const void *x, int x_layout, const void *w, int w_
                      stream);
 }
 
-lf_status matmul_k1(const float *a, const float *b, float *out, int64_t M, int64_t N, cudaStream_t stream)
+static lf_status matmul_k1_call(const float *a, const float *b, float *out, int64_t M, int64_t N, cudaStream_t stream)
 {
     if (!a || !b || !out)
         return LF_ERR_NULL;
@@ -832,7 +860,7 @@ lf_status matmul_k1(const float *a, const float *b, float *out, int64_t M, int64
     return launched(lf::launch_matmul_k1_f32(a, b, out, M, N, d->num_sms, stream), 1);
 }
 
-lf_status rope_cos_sin(const void *inv_freq, const int64_t *positions, void *cos_out, void *sin_out_or_null,
+static lf_status rope_cos_sin_call(const void *inv_freq, const int64_t *positions, void *cos_out, void *sin_out_or_null,
                        int64_t H, int64_t S, cudaStream_t stream)
 {
     if (!inv_freq || !positions || !cos_out)
@@ -851,7 +879,7 @@ lf_status rope_cos_sin(const void *inv_freq, const int64_t *positions, void *cos
                     1);
 }
 
-lf_status fp8_cast_dual(const void *x, const float *scale, void *out, void *out_t, int64_t M, int64_t K,
+static lf_status fp8_cast_dual_call(const void *x, const float *scale, void *out, void *out_t, int64_t M, int64_t K,
                         cudaStream_t stream)
 {
     if (!x || !scale || !out || !out_t)
@@ -971,6 +999,68 @@ void lf_set_test_hooks(int inject_stall, uint64_t wait_timeout_ns)
 {
     g_inject.store(inject_stall ? 1 : 0);
     g_timeout_ns.store(wait_timeout_ns ? wait_timeout_ns : 2000000000ull);
+}
+
+}  // extern "C"
+
+// The exported entry points: an optional profiling range around each call and,
+// with LF_DEBUG_SYNC set in the environment, a synchronising check that turns
+// a device-side timeout or launch error into the call's own status.
+extern "C" {
+
+lf_status gemm_nt(const void *x, const void *w, void *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    const lf::CallRange range("gemm_nt");
+    return debug_sync(gemm_nt_call(x, w, out, M, N, K, stream), stream);
+}
+
+lf_status gemm_layout(const void *x, int x_layout, const void *w, int w_layout, void *out, int64_t M, int64_t N,
+                      int64_t K, cudaStream_t stream)
+{
+    const lf::CallRange range("gemm_layout");
+    return debug_sync(gemm_layout_call(x, x_layout, w, w_layout, out, M, N, K, stream), stream);
+}
+
+lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_x, const void *w, int w_layout,
+                       int64_t ldw, int64_t stride_w, void *out, int64_t ldo, int64_t stride_o, int64_t batch,
+                       int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    const lf::CallRange range("gemm_batched");
+    return debug_sync(gemm_batched_call(x, x_layout, ldx, stride_x, w, w_layout, ldw, stride_w, out, ldo, stride_o, batch, M, N, K, stream), stream);
+}
+
+lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
+                       int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    const lf::CallRange range("gemm_nt_xent");
+    return debug_sync(gemm_nt_xent_call(x, w, labels, loss, grad_or_null, M, N, K, stream), stream);
+}
+
+lf_status gemm_nt_xent_layout(const void *x, int x_layout, const void *w, int w_layout, const int32_t *labels,
+                              float *loss, void *grad_or_null, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    const lf::CallRange range("gemm_nt_xent_layout");
+    return debug_sync(gemm_nt_xent_layout_call(x, x_layout, w, w_layout, labels, loss, grad_or_null, M, N, K, stream), stream);
+}
+
+lf_status matmul_k1(const float *a, const float *b, float *out, int64_t M, int64_t N, cudaStream_t stream)
+{
+    const lf::CallRange range("matmul_k1");
+    return debug_sync(matmul_k1_call(a, b, out, M, N, stream), stream);
+}
+
+lf_status rope_cos_sin(const void *inv_freq, const int64_t *positions, void *cos_out, void *sin_out_or_null,
+                       int64_t H, int64_t S, cudaStream_t stream)
+{
+    const lf::CallRange range("rope_cos_sin");
+    return debug_sync(rope_cos_sin_call(inv_freq, positions, cos_out, sin_out_or_null, H, S, stream), stream);
+}
+
+lf_status fp8_cast_dual(const void *x, const float *scale, void *out, void *out_t, int64_t M, int64_t K,
+                        cudaStream_t stream)
+{
+    const lf::CallRange range("fp8_cast_dual");
+    return debug_sync(fp8_cast_dual_call(x, scale, out, out_t, M, K, stream), stream);
 }
 
 }  // extern "C"

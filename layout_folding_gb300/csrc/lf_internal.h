@@ -4,6 +4,9 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#ifdef LF_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
 
 namespace lf {
 
@@ -125,12 +128,34 @@ cudaError_t launch_fp8_cast_dual(const void *x, const float *scale, void *out, v
 // that wait `ns` nanoseconds on the global timer and exit.
 cudaError_t launch_occupy_sms(int ctas, unsigned long long ns, cudaStream_t s);
 
+// A profiling range around one entry-point call: an NVTX range named after
+// the call when the library is built with LF_NVTX defined, nothing otherwise.
+struct CallRange {
+    explicit CallRange(const char *name)
+    {
+#ifdef LF_NVTX
+        nvtxRangePushA(name);
+#else
+        (void)name;
+#endif
+    }
+    ~CallRange()
+    {
+#ifdef LF_NVTX
+        nvtxRangePop();
+#endif
+    }
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
+
 // Library state and helpers shared by the entry points of every translation
 // unit (defined in api.cu).
 unsigned long long wait_timeout_ns();  // device-side wait limit (lf_set_test_hooks; 2 s by default)
 bool cooperative_launches();           // false after lf_set_cooperative(0)
 int stall_injection();                 // 1 while lf_set_test_hooks asks for a stalled first stage
 void count_launches(int n);            // adds n to the lf_launch_count total
+bool debug_sync_enabled();             // LF_DEBUG_SYNC is set in the environment
 // 2-D bf16 tensor [rows, K] (K contiguous) as a TMA map: boxes of 64 columns x
 // box_rows rows, 128-byte swizzle, zero fill out of bounds.  False if the
 // driver entry point is missing or rejects the layout.

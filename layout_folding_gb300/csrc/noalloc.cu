@@ -100,9 +100,8 @@ size_t round_up256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace
 
-extern "C" lf_status gemm_nt_xent_noalloc(const void *x, const void *w, const int32_t *labels, float *loss,
-                                          void *grad_or_null, int64_t M, int64_t N, int64_t K,
-                                          cudaStream_t stream)
+static lf_status noalloc_call(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
+                              int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     if (!x || !w || !labels || !loss)
         return LF_ERR_NULL;
@@ -182,3 +181,27 @@ extern "C" lf_status gemm_nt_xent_noalloc(const void *x, const void *w, const in
     lf::count_launches(1);
     return LF_OK;
 }
+
+// The exported entry point: an optional profiling range and, with
+// LF_DEBUG_SYNC set, a synchronising check of this call's own error word
+// (a wait that ran out returns LF_ERR_DEVICE_TIMEOUT besides the NaN outputs).
+extern "C" lf_status gemm_nt_xent_noalloc(const void *x, const void *w, const int32_t *labels, float *loss,
+                                          void *grad_or_null, int64_t M, int64_t N, int64_t K,
+                                          cudaStream_t stream)
+{
+    const lf::CallRange range("gemm_nt_xent_noalloc");
+    lf_status st = noalloc_call(x, w, labels, loss, grad_or_null, M, N, K, stream);
+    if (st != LF_OK || !lf::debug_sync_enabled())
+        return st;
+    NoAllocDevice *d = nullptr;
+    if ((st = noalloc_device(&d)) != LF_OK)
+        return st;
+    int code = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess ||
+        cudaMemcpy(&code, d->scratch, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return LF_ERR_LAUNCH;
+    }
+    return code ? LF_ERR_DEVICE_TIMEOUT : LF_OK;
+}
+
