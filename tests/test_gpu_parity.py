@@ -658,3 +658,28 @@ def test_xent_whole_row_in_one_tile(M, N, K, variant):
     assert_loss_close(f64(loss_only), rloss, "whole row, loss only")
     assert_grad_close(f64(grad), rgrad, "whole row")
 
+
+
+@pytest.mark.parametrize("N,launches", [(20000 * 256, 2), (49153 * 256, 3)], ids=["80KiB_scales", "past_limit"])
+def test_xent_gradient_very_wide_rows(N, launches):
+    """Rows so wide that the rescale kernel keeps 20,000 tile scales (80 KiB)
+    in shared memory -- past the 48 KiB default, so the launch opts in to more;
+    and one tile past its 49,152-tile limit, where the recompute form runs.
+    M = 130 (CTA pairs), K = 8; sampled rows, every column, against the oracle."""
+    M, K = 130, 8
+    x = synthetic.bf16_normal((M, K), 1.0, 91)
+    w = synthetic.bf16_normal((N, K), 1.0 / math.sqrt(K), 92)
+    lab = synthetic.labels_uniform(M, N, seed=93)
+    lab[0], lab[64], lab[129] = 0, N - 1, 256 * 12345 + 255
+    xd, wd, ld = x.to(DEV), w.to(DEV), lab.to(DEV)
+    n0 = lf.launch_count()
+    loss, grad = lf.gemm_nt_xent(xd, wd, ld, want_grad=True)
+    torch.cuda.synchronize()
+    assert lf.launch_count() - n0 == launches
+    lf.check_device_error()
+    rows = np.array([0, 64, 129])
+    _, rloss, _, rgrad = oracle.xent_rows(x, w, lab.numpy(), rows)
+    assert_loss_close(f64(loss)[rows], rloss, "very wide rows")
+    assert_grad_close(f64(grad[torch.from_numpy(rows).to(DEV)]), rgrad, "very wide rows")
+    del grad
+    torch.cuda.empty_cache()
