@@ -609,7 +609,7 @@ static lf_status gemm_nt_call(const void *x, const void *w, void *out, int64_t M
 }
 
 static lf_status gemm_layout_call(const void *x, int x_layout, const void *w, int w_layout, void *out, int64_t M, int64_t N,
-                      int64_t K, cudaStream_t stream)
+                                  int64_t K, cudaStream_t stream)
 {
     if (!x || !w || !out)
         return LF_ERR_NULL;
@@ -637,8 +637,8 @@ static lf_status gemm_layout_call(const void *x, int x_layout, const void *w, in
 }
 
 static lf_status gemm_batched_call(const void *x, int x_layout, int64_t ldx, int64_t stride_x, const void *w, int w_layout,
-                       int64_t ldw, int64_t stride_w, void *out, int64_t ldo, int64_t stride_o, int64_t batch,
-                       int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+                                   int64_t ldw, int64_t stride_w, void *out, int64_t ldo, int64_t stride_o, int64_t batch,
+                                   int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     if (!x || !w || !out)
         return LF_ERR_NULL;
@@ -725,24 +725,22 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
     float *row_max = reinterpret_cast<float *>(wsb + 2 * part + vec);
     float *row_logsum = reinterpret_cast<float *>(wsb + 2 * part + 2 * vec);
     p.labels = labels;
-    // With a gradient on CTA pairs: one pass, when a whole 256-row block of
-    // tiles (two per pair) fits on the resident pairs -- no recompute GEMM and
-    // no combine kernel.  N-tile width: the one with the least rounds x width
-    // (the time of a round is about proportional to its tiles' width), i.e. the
-    // narrowest that keeps the fewest rounds: more pairs busy, shorter MMA
-    // chains.  (4096 x 32768 x 4096: 0.836 ms at 224 with 74 pairs against
-    // 0.847 ms at 256 with 64.  Before the round's merge overlapped the next
-    // mainloop, 224 measured slower, 1.038 against 1.011 ms.)
-    // Which gradient form: the one-pass kernel (below), the exp pass + rescale
-    // (a GEMM writing fp16 exp(z - tile max) into grad, then one bandwidth-bound
-    // pass), or the recompute pass (single-CTA tiles, or rows too wide for the
-    // rescale kernel's shared memory).
-    // (A forced one-pass tile width selects the one-pass kernel.)
+    // Which gradient form: the exp pass + rescale (a GEMM writing fp16
+    // exp(z - tile max) into grad, then one bandwidth-bound pass) -- the
+    // automatic choice --, the one-pass kernel (on request, or when a
+    // one-pass tile width is forced), or the recompute pass (single-CTA tiles,
+    // or rows too wide for the rescale kernel's shared memory).
     const int path = g_xent_path.load();
     const int forced = g_op_tile.load();
     const bool exp_ok = grad_or_null && g.pair && p.num_n_blocks <= RESCALE_MAX_TILES;
     const bool try_onepass = grad_or_null && g.pair && d->coop.load() >= 0 &&
                              (path == 1 || (path == 0 && (!exp_ok || forced != 0)));
+    // One pass, when a whole 256-row block of tiles (two per pair) fits on the
+    // resident pairs -- no recompute GEMM and no combine kernel.  N-tile width:
+    // the one with the least rounds x width (the time of a round is about
+    // proportional to its tiles' width), i.e. the narrowest that keeps the
+    // fewest rounds: more pairs busy, shorter MMA chains.  (4096 x 32768 x
+    // 4096: 0.836 ms at 224 with 74 pairs against 0.847 ms at 256 with 64.)
     int op_tile = 0;
     long long best = 0;
     for (int wdt = 256; wdt >= 128 && try_onepass; wdt -= 32) {
@@ -831,13 +829,13 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
 extern "C" {
 
 static lf_status gemm_nt_xent_call(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
-                       int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+                                   int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     return xent_impl(x, false, w, false, labels, loss, grad_or_null, M, N, K, stream);
 }
 
 static lf_status gemm_nt_xent_layout_call(const void *x, int x_layout, const void *w, int w_layout, const int32_t *labels,
-                              float *loss, void *grad_or_null, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+                                          float *loss, void *grad_or_null, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     if ((x_layout != LF_K_MAJOR && x_layout != LF_MN_MAJOR) || (w_layout != LF_K_MAJOR && w_layout != LF_MN_MAJOR))
         return LF_ERR_SHAPE;
@@ -861,7 +859,7 @@ static lf_status matmul_k1_call(const float *a, const float *b, float *out, int6
 }
 
 static lf_status rope_cos_sin_call(const void *inv_freq, const int64_t *positions, void *cos_out, void *sin_out_or_null,
-                       int64_t H, int64_t S, cudaStream_t stream)
+                                   int64_t H, int64_t S, cudaStream_t stream)
 {
     if (!inv_freq || !positions || !cos_out)
         return LF_ERR_NULL;
@@ -880,7 +878,7 @@ static lf_status rope_cos_sin_call(const void *inv_freq, const int64_t *position
 }
 
 static lf_status fp8_cast_dual_call(const void *x, const float *scale, void *out, void *out_t, int64_t M, int64_t K,
-                        cudaStream_t stream)
+                                    cudaStream_t stream)
 {
     if (!x || !scale || !out || !out_t)
         return LF_ERR_NULL;
@@ -1026,7 +1024,9 @@ lf_status gemm_batched(const void *x, int x_layout, int64_t ldx, int64_t stride_
                        int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     const lf::CallRange range("gemm_batched");
-    return debug_sync(gemm_batched_call(x, x_layout, ldx, stride_x, w, w_layout, ldw, stride_w, out, ldo, stride_o, batch, M, N, K, stream), stream);
+    return debug_sync(gemm_batched_call(x, x_layout, ldx, stride_x, w, w_layout, ldw, stride_w, out, ldo, stride_o,
+                                        batch, M, N, K, stream),
+                      stream);
 }
 
 lf_status gemm_nt_xent(const void *x, const void *w, const int32_t *labels, float *loss, void *grad_or_null,
@@ -1040,7 +1040,8 @@ lf_status gemm_nt_xent_layout(const void *x, int x_layout, const void *w, int w_
                               float *loss, void *grad_or_null, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
 {
     const lf::CallRange range("gemm_nt_xent_layout");
-    return debug_sync(gemm_nt_xent_layout_call(x, x_layout, w, w_layout, labels, loss, grad_or_null, M, N, K, stream), stream);
+    return debug_sync(
+        gemm_nt_xent_layout_call(x, x_layout, w, w_layout, labels, loss, grad_or_null, M, N, K, stream), stream);
 }
 
 lf_status matmul_k1(const float *a, const float *b, float *out, int64_t M, int64_t N, cudaStream_t stream)
