@@ -224,6 +224,15 @@ class Timer:
         return (times, launches) if counter else times
 
 
+def headline_config(wl, world):
+    """The headline workload's `config`, identical in both arms' lines."""
+    return {"workload": "nt_projection", "path": "gemm_nt", "M": wl.M, "N": wl.N, "K": wl.K,
+            "x_shape": list(wl.x_shape), "accumulate": "fp32", "out": "bf16",
+            "l2": "GPU arm: flushed between steps outside the timed events (a 256 MiB write, then a 256 MiB "
+                  "read that retires the write's dirty lines; L2 is 129 MB); CPU arm: not applicable",
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -311,14 +320,10 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)*0.02 bf16; no dataset)",
-        "config": {"workload": "nt_projection", "path": "gemm_nt", "M": wl.M, "N": wl.N, "K": wl.K,
-                   "x_shape": list(wl.x_shape), "accumulate": "fp32", "out": "bf16",
-                   "l2": "flushed between steps outside the timed events: a 256 MiB write, then a 256 MiB "
-                         "read that retires the write's dirty lines (L2 is 129 MB)",
-                   "timing": "CUDA events around each call on the launching stream; a 0.1 ms device delay "
-                             "precedes each start event so host launch latency is not counted",
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "cooperative_launches": not args.no_cooperative},
+        "config": headline_config(wl, world),
+        "timing": "CUDA events around each call on the launching stream; a 0.1 ms device delay "
+                  "precedes each start event so host launch latency is not counted",
+        "cooperative_launches": not args.no_cooperative,
         "pct_of_peak": round(100.0 * achieved / peak, 1),
         "roofline": {"bound": "tensor", "kernel": HEADLINE_KERNEL, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": "bf16 burst (%s)" % peaks["source"], "unit": "TFLOP/s",
@@ -754,8 +759,8 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1)*0.02 bf16; no dataset)",
-        "config": {"workload": "nt_projection", "path": "gemm_nt", "M": wl.M, "N": wl.N, "K": wl.K,
-                   "sample_rows_per_step": nrows},
+        "config": headline_config(wl, world),
+        "timing": "wall clock around each step's oracle call on the host cores",
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
