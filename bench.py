@@ -243,6 +243,7 @@ def run_ours(args, rank, world, local_rank):
     lf.lib()
     if args.no_cooperative:
         lf.set_cooperative(False)
+    lf.set_tile_schedule({"auto": -1, "fixed": 0, "claimed": 1}[args.tile_schedule])
     peaks = load_peaks()
     stream = torch.cuda.Stream()
     timer = Timer(torch, stream)
@@ -324,6 +325,7 @@ def run_ours(args, rank, world, local_rank):
         "timing": "CUDA events around each call on the launching stream; a 0.1 ms device delay "
                   "precedes each start event so host launch latency is not counted",
         "cooperative_launches": not args.no_cooperative,
+        "tile_schedule": args.tile_schedule,
         "pct_of_peak": round(100.0 * achieved / peak, 1),
         "roofline": {"bound": "tensor", "kernel": HEADLINE_KERNEL, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": "bf16 burst (%s)" % peaks["source"], "unit": "TFLOP/s",
@@ -782,6 +784,9 @@ def main(argv=None):
     ap.add_argument("--no-cooperative", action="store_true",
                     help="launch the stream-K and one-pass kernels without the cooperative attribute (for ncu, "
                          "which cannot replay cooperative cluster launches); same kernels")
+    ap.add_argument("--tile-schedule", choices=["auto", "fixed", "claimed"], default="auto",
+                    help="whole tiles on CTA pairs: the automatic choice, the fixed assignment or tiles claimed at "
+                         "run time (for comparisons; results are identical)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -359,6 +359,7 @@ lf_status lf_check_device_error(cudaStream_t stream);
  *   0x107 a CTA's own stream-K partial write did not complete
  *   0x108 a one-pass group member never published its row statistics
  *   0x109 the copy of a stream-K partial into shared memory did not land
+ *   0x10a a tile claimed at run time never reached one of the pair's roles
  */
 int lf_last_device_wait_code(void);
 
@@ -433,6 +434,19 @@ void lf_set_xent_grad_path(int path);
  * evenly).  Results do not depend on it.
  */
 void lf_set_tile_band(int m_blocks);
+
+/*
+ * Assignment of whole output tiles to CTA pairs, applied to later launches:
+ * 0 = fixed (pair i takes tiles i, i + pairs, ...); 1 = claimed at run time
+ * (pair i starts with tile i, then each pair claims the next unclaimed tile
+ * in the tile order from a counter in the library's workspace, so the pairs
+ * that share a W tile start it together and faster pairs take more tiles);
+ * a negative value restores the automatic choice (claimed from 64 waves of
+ * tiles with K >= 2048 on: long launches, where the fixed assignment's pairs
+ * drift apart).  Each tile is computed by one pair either way:
+ * results do not depend on it.
+ */
+void lf_set_tile_schedule(int mode);
 
 /*
  * Test hooks (not for production use).  inject_stall = 1 makes the next

@@ -90,6 +90,8 @@ def lib():
         L.lf_set_xent_grad_path.restype = None
         L.lf_set_tile_band.argtypes = [I32]
         L.lf_set_tile_band.restype = None
+        L.lf_set_tile_schedule.argtypes = [I32]
+        L.lf_set_tile_schedule.restype = None
         L.lf_set_cooperative.argtypes = [I32]
         L.lf_set_cooperative.restype = None
         L.lf_test_occupy_sms.argtypes = [I32, ctypes.c_uint64, P]
@@ -369,7 +371,8 @@ WAIT_CODES = {0x101: "operand ring slot never freed", 0x102: "operand stage neve
               0x103: "accumulator never released", 0x104: "accumulator never completed",
               0x105: "unwinding did not finish", 0x106: "stream-K partial never arrived",
               0x107: "own stream-K partial write incomplete", 0x108: "one-pass group member never published",
-              0x109: "partial copy into shared memory never landed"}
+              0x109: "partial copy into shared memory never landed",
+              0x10A: "claimed tile index never arrived"}
 
 
 def last_device_wait_code() -> int:
@@ -429,6 +432,12 @@ def set_xent_grad_path(path: int = 0):
 def set_tile_band(m_blocks: int = -1):
     """Whole-tile band height in 256-row blocks (0 = one band, -1 = automatic)."""
     lib().lf_set_tile_band(int(m_blocks))
+
+
+def set_tile_schedule(mode: int = -1):
+    """Whole tiles on CTA pairs: 0 = fixed assignment, 1 = claimed at run time,
+    -1 = automatic."""
+    lib().lf_set_tile_schedule(int(mode))
 
 
 def set_cooperative(enable: bool = True):

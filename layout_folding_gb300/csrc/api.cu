@@ -23,8 +23,9 @@ struct DeviceState {
     void *sk_ws = nullptr;    // stream-K partial slots + flags (fixed size, zeroed once)
     void *op_flags = nullptr; // one-pass cross-entropy: round flags (2 per pair, zeroed once), then
                               // the per-CTA stash of a tile's exp values (128 x 256 fp32 per CTA)
-    unsigned sk_epoch = 0;    // last epoch handed to a stream-K launch
+    unsigned sk_epoch = 0;    // last epoch handed to a launch whose CTAs wait on flags
     int *err_word = nullptr;  // device int[64]; [0] = first error code
+    unsigned *tile_ctl = nullptr;  // claimed whole tiles: counter and count (GemmParams::tile_ctl), zeroed once
     void *ws = nullptr;       // cross-entropy workspace (grow-only)
     size_t ws_bytes = 0;
     // Ordering of the calls that use the workspaces above (WorkspaceOrder).
@@ -56,6 +57,16 @@ std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA, 2 CTA-pair whole 
 std::atomic<int> g_op_tile{0};       // one-pass cross-entropy N-tile width; 0 = automatic
 std::atomic<int> g_xent_path{0};     // cross-entropy gradient: 0 auto, 1 one pass, 2 exp + rescale, 3 recompute
 std::atomic<int> g_band{-1};         // whole-tile band height in M blocks: -1 auto, 0 one band, > 0 forced
+std::atomic<int> g_tile_sched{-1};   // whole tiles on pairs: -1 auto, 0 fixed assignment, 1 claimed at run time
+// Whole tiles on CTA pairs are claimed at run time from this many waves of
+// tiles of at least this many K blocks on.  The fixed assignment's drift
+// grows with the launch (pairs' last tile starts 1.5 tiles apart at 27 waves,
+// 8.5 tiles at 211), while a claim and its hand-over cost every tile a little
+// (1.5-2 % at 13-27 waves of 64 K blocks; 6 % on tiles of 16 K blocks).
+// Measured per launch at 211 waves (8192 x 128256 x 4096, loss only):
+// 4.42 ms claimed, 4.59-4.63 ms fixed, DRAM reads 2.2 GB against 6.8-9.0 GB.
+constexpr long long DYN_MIN_WAVES = 64;
+constexpr int DYN_MIN_KBLOCKS = 32;
 std::atomic<int> g_coop_enable{1};   // 0: launch the CTA-waiting kernels without the cooperative attribute
 // L2 bytes of X a band of whole tiles may keep while it sweeps W (the L2 is
 // 129 MB, but reuse measured as if about half of it were available)
@@ -107,6 +118,8 @@ lf_status current_device(DeviceState **out)
             d.pair_clusters = lf::gemm_pair_max_active_clusters();
             if (cudaMalloc(&d.err_word, 64 * sizeof(int)) != cudaSuccess ||
                 cudaMemset(d.err_word, 0, 64 * sizeof(int)) != cudaSuccess ||
+                cudaMalloc(&d.tile_ctl, 64 * sizeof(unsigned)) != cudaSuccess ||
+                cudaMemset(d.tile_ctl, 0, 64 * sizeof(unsigned)) != cudaSuccess ||
                 cudaEventCreateWithFlags(&d.ws_event, cudaEventDisableTiming) != cudaSuccess ||
                 cudaDeviceSynchronize() != cudaSuccess) {
                 cudaGetLastError();
@@ -164,6 +177,31 @@ lf_status ensure_sk_workspace(DeviceState *d)
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+unsigned next_epoch(DeviceState *d)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    unsigned e = ++d->sk_epoch;
+    if (e == 0)
+        e = ++d->sk_epoch;
+    return e;
+}
+
+// True while `s` is being captured into a CUDA graph.  Such a call plans no
+// schedule whose CTAs wait on each other's flags (stream-K, the one-pass
+// cross-entropy): their flags carry a per-launch epoch, which every replay of
+// the graph would repeat, so a replay could take the flags of the previous
+// one for its own.  The flag-free forms (whole tiles, the exp pass and the
+// rescale) replay correctly.
+bool capturing(cudaStream_t s)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return cs != cudaStreamCaptureStatusNone;
+}
+
 // One-pass cross-entropy workspace, allocated on first use: the round flags
 // (zeroed once; every launch's flags carry a new epoch) and the stash.
 size_t onepass_flag_bytes(const DeviceState *d)
@@ -189,25 +227,16 @@ lf_status ensure_onepass_flags(DeviceState *d)
     return LF_OK;
 }
 
-unsigned next_epoch(DeviceState *d)
-{
-    std::lock_guard<std::mutex> lock(g_mutex);
-    unsigned e = ++d->sk_epoch;
-    if (e == 0)
-        e = ++d->sk_epoch;
-    return e;
-}
-
 // Orders the calls that use a device's library-owned workspaces (the
 // cross-entropy partials, the stream-K slots and flags, the one-pass flags and
-// stash).  A call on a different stream than the previous such call first
-// makes its stream wait for that call's launches (an event: no host
-// synchronisation), and the lock, held from before the launch's epoch is drawn
-// until its launches are enqueued and recorded, keeps host threads from
-// interleaving -- so such launches run one after another on the GPU, in the
-// order of their epochs, whatever streams and threads they come from.  A
-// stream that is being captured into a graph is neither made to wait nor
-// recorded (graph replays are ordered by the caller).
+// stash, the claimed-tile counter).  A call on a different stream than the
+// previous such call first makes its stream wait for that call's launches (an
+// event: no host synchronisation), and the lock, held from before the
+// launch's epoch is drawn until its launches are enqueued and recorded, keeps
+// host threads from interleaving -- so such launches run one after another on
+// the GPU, in the order of their epochs, whatever streams and threads they
+// come from.  A stream that is being captured into a graph is neither made to
+// wait nor recorded (graph replays are ordered by the caller).
 class WorkspaceOrder {
 public:
     WorkspaceOrder(DeviceState *d, cudaStream_t s) : d_(d), s_(s), lock_(d->order_mutex)
@@ -336,6 +365,7 @@ struct GemmPlan {
     CUtensorMap to;  // output map of the pair kernel's TMA-store epilogue (set by run_gemm)
     lf::GemmParams p;
     int grid = 0;
+    bool no_flags = false;  // the call is being captured into a graph (see capturing)
 };
 
 lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int64_t N, int64_t K,
@@ -423,7 +453,7 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
         // 33.0-37.9 us split.
         const double whole_kb = static_cast<double>(waves) * p.num_k_blocks;
         const double split_kb = G > 0 ? static_cast<double>(V) / static_cast<double>(G) : whole_kb;
-        p.streamk = (G > 0 && d->coop.load() >= 0 &&
+        p.streamk = (G > 0 && d->coop.load() >= 0 && !g->no_flags &&
                      (variant == 3 || (variant < 0 && whole_kb - split_kb > SK_FIXED_KBLOCKS)))
                         ? 1
                         : 0;
@@ -460,6 +490,16 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
             }
         }
         p.band_m = band < MB ? band : 0;
+        // Claimed tiles: over a long launch pairs drift apart by several
+        // tiles (4.6 ms at 8192 x 128256 x 4096: 184 us between the pairs'
+        // last tile starts), the pairs that share a W tile stop running side
+        // by side and the last pairs finish late; claiming each next tile in
+        // tile order keeps both tight.
+        const int sched = g_tile_sched.load();
+        p.dyn_tiles = (sched == 1 || (sched < 0 && p.num_tiles >= DYN_MIN_WAVES * d->pair_clusters &&
+                                      p.num_k_blocks >= DYN_MIN_KBLOCKS))
+                          ? 1
+                          : 0;
     }
     return LF_OK;
 }
@@ -471,6 +511,7 @@ cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
                       (static_cast<uint64_t>(g.p.tile_n ? g.p.tile_n : lf::BN) << 24));
     if (g.p.streamk)
         g.p.epoch = next_epoch(g.dev);  // each launch's flags are distinct from every earlier one
+    g.p.tile_ctl = g.dev->tile_ctl;
     g.p.tma_store = 0;
     std::memset(&g.to, 0, sizeof g.to);
     if (g.pair && (epi == lf::EPI_STORE || epi == lf::EPI_XENT_GRAD || epi == lf::EPI_XENT_EXP) && g.p.out) {
@@ -488,6 +529,7 @@ cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
         // no cross-CTA waits, and stop choosing schedules that need it.
         cudaGetLastError();
         g.p.streamk = 0;
+        g.p.dyn_tiles = 0;
         g.grid = 2 * (g.p.num_tiles < g.dev->pair_clusters ? g.p.num_tiles : g.dev->pair_clusters);
         g_last_plan.store((g_last_plan.load() & ~((0xfffffull) | (1ull << 23))) | static_cast<uint64_t>(g.grid));
         e = lf::launch_gemm_nt_pair(epi, g.layout, g.ta, g.tb, g.to, g.p, g.grid, stream);
@@ -505,11 +547,12 @@ lf_status launched(cudaError_t e, int n)
     return LF_OK;
 }
 
-// One planned GEMM launch; a stream-K launch uses the workspace, so it is
-// ordered against the other workspace users (WorkspaceOrder).
+// One planned GEMM launch; a stream-K launch or one that claims its tiles at
+// run time uses the workspace, so it is ordered against the other workspace
+// users (WorkspaceOrder).
 lf_status run_planned(int epi, GemmPlan &g, cudaStream_t stream)
 {
-    if (!g.p.streamk)
+    if (!g.p.streamk && !g.p.dyn_tiles)
         return launched(run_gemm(epi, g, stream), 1);
     WorkspaceOrder order(g.dev, stream);
     if (!order.ok())
@@ -588,6 +631,7 @@ static lf_status gemm_nt_call(const void *x, const void *w, void *out, int64_t M
         return launched(lf::launch_matmul_k1_bf16(x, w, out, M, N, d->num_sms, stream), 1);
     const int variant = g_variant.load();
     GemmPlan g;
+    g.no_flags = capturing(stream);
     const int64_t tiles1 = (N + lf::BN - 1) / lf::BN;  // single-CTA tiles of a skinny X
     if (d->pair_clusters > 0 && M <= lf::BM && (variant == 4 || (variant < 0 && tiles1 * 2 < d->num_sms))) {
         // Skinny X with few output tiles: swap the operands so W's N rows fill
@@ -630,6 +674,7 @@ static lf_status gemm_layout_call(const void *x, int x_layout, const void *w, in
     if (K == 1)  // a [M,1] / [1,M] operand is the same vector either way
         return launched(lf::launch_matmul_k1_bf16(x, w, out, M, N, d->num_sms, stream), 1);
     GemmPlan g;
+    g.no_flags = capturing(stream);
     if ((st = plan_gemm(d, x, w, M, N, K, &g, (x_mn ? 1 : 0) | (w_mn ? 2 : 0))) != LF_OK)
         return st;
     g.p.out = out;
@@ -661,6 +706,7 @@ static lf_status gemm_batched_call(const void *x, int x_layout, int64_t ldx, int
         return st;
     const BatchSpec bs = {batch, ldx, stride_x, ldw, stride_w, ldo, stride_o};
     GemmPlan g;
+    g.no_flags = capturing(stream);
     if ((st = plan_gemm(d, x, w, M, N, K, &g, (x_mn ? 1 : 0) | (w_mn ? 2 : 0), &bs)) != LF_OK)
         return st;
     g.p.out = out;
@@ -700,6 +746,7 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
         return LF_ERR_LAUNCH;
     const int layout = (x_mn ? 1 : 0) | (w_mn ? 2 : 0);
     GemmPlan g;
+    g.no_flags = capturing(stream);
     if ((st = plan_gemm(d, x, w, M, N, K, &g, layout)) != LF_OK)
         return st;
     lf::GemmParams &p = g.p;
@@ -733,7 +780,7 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
     const int path = g_xent_path.load();
     const int forced = g_op_tile.load();
     const bool exp_ok = grad_or_null && g.pair && p.num_n_blocks <= RESCALE_MAX_TILES;
-    const bool try_onepass = grad_or_null && g.pair && d->coop.load() >= 0 &&
+    const bool try_onepass = grad_or_null && g.pair && d->coop.load() >= 0 && !g.no_flags &&
                              (path == 1 || (path == 0 && (!exp_ok || forced != 0)));
     // One pass, when a whole 256-row block of tiles (two per pair) fits on the
     // resident pairs -- no recompute GEMM and no combine kernel.  N-tile width:
@@ -974,6 +1021,8 @@ void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant)
 void lf_set_xent_grad_path(int path) { g_xent_path.store(path >= 1 && path <= 3 ? path : 0); }
 
 void lf_set_tile_band(int m_blocks) { g_band.store(m_blocks < 0 ? -1 : m_blocks); }
+
+void lf_set_tile_schedule(int mode) { g_tile_sched.store(mode < 0 ? -1 : (mode ? 1 : 0)); }
 
 void lf_set_cooperative(int enable) { g_coop_enable.store(enable ? 1 : 0); }
 

@@ -55,7 +55,8 @@ constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_ACC_BUFS = 2;
 constexpr int PAIR_TMEM_COLS = PAIR_ACC_BUFS * BN;  // 512
 constexpr int PAIR_SKC_CHUNKS = BN / 32;  // a contributor's partial arrives in 8 chunks of 32 columns
-constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2 + PAIR_SKC_CHUNKS;
+constexpr int PAIR_TQ = 16;               // ring of claimed tile indices (dynamic whole tiles)
+constexpr int PAIR_NUM_BARS = 2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS + 2 + PAIR_SKC_CHUNKS + PAIR_TQ;
 // Per epilogue warp: two 2 KiB slots, each 32 rows x 32 bf16 columns of output
 // (64-byte rows whose 16-byte pieces are XOR-swizzled by row pair -- the layout
 // of a TMA 64-byte swizzle), so a TMA store can read one slot while the warp
@@ -66,7 +67,9 @@ constexpr int PAIR_STG_SLOT = 32 * 64;
 constexpr int PAIR_STG_WARP_BYTES = 2 * PAIR_STG_SLOT;
 static_assert(PAIR_STG_WARP_BYTES >= 32 * PAIR_STG_ROW, "transposed staging tile must fit");
 // 1024-byte aligned: the swizzle pattern of a TMA store follows the address bits
-constexpr int PAIR_STG_OFF = ((PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16 + 1023) / 1024) * 1024;
+// (after the barriers: 16 bytes of words -- TMEM address, abort flag -- and
+// the PAIR_TQ tile-index slots)
+constexpr int PAIR_STG_OFF = ((PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8 + 16 + PAIR_TQ * 4 + 1023) / 1024) * 1024;
 // Epilogue warps per CTA: the plain store epilogues use two per TMEM lane
 // quarter (each takes half of the tile's columns, so the last tile's
 // epilogue -- the tail of the launch -- and a stream-K partial take half as
@@ -123,7 +126,26 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int tile, int &
 }
 
 // The sequence of segments one pair works on.
-// Whole tiles: tiles pair, pair + num_pairs, ... (M-block fastest).
+// Whole tiles: tiles pair, pair + num_pairs, ... (M-block fastest), or with
+// dyn_tiles tile pair and then the tiles the pair claims at run time:
+// the leader's producer claims each further tile (num_pairs + the old value
+// of the launch's tile counter) when it starts loading its current tile, and
+// 2 K blocks before that tile's last load hands the claim to the pair's other
+// roles -- its own MMA issuer and epilogue warps, the peer CTA's producer and
+// epilogue warps -- through a ring of PAIR_TQ shared-memory slots in each
+// CTA, each with an mbarrier (one arrival per entry).  The leader's own copy
+// is a plain store and a local arrive; the peer's is an asynchronous store
+// that completes as transaction bytes on the peer's barrier, with a relaxed
+// arrive: a release at cluster scope there stalled the producer about 0.5 us
+// per tile.  A claim past the last tile ends every role's sequence.  Claims
+// follow the tile order, so the pairs that share a W tile start it together
+// however far single pairs drift over a long launch, and faster pairs take
+// more tiles.  A slot is overwritten 16 entries after it was filled, and by
+// then every role has taken the entry: when the producer publishes entry
+// j + 1 (during tile j) it has had the stage of entry j - 1 freed, so the MMA
+// issuer (6 stages behind at most) has taken entry j - 7, the epilogue warps
+// of both CTAs (two accumulator buffers behind it) entry j - 9 and the peer's
+// producer (whose copies the MMA waited for) entry j - 7.
 // Stream-K: the pairs form G = num_pairs / MB groups of MB pairs (MB = M
 // blocks); pair m of group g works on M block m.  The V = N-tiles x K-blocks
 // "column iterations" are split evenly over the groups -- group g takes
@@ -132,12 +154,22 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int tile, int &
 // HBM once, while every pair gets an equal share.  Only a pair's first
 // segment can start inside a tile and only its last can end inside one.
 struct WorkIter {
-    bool sk;
+    bool sk, dyn;
     int tile, step, ntiles, KB, MB, m;
     long long v, v_end;
+    // dynamic whole tiles: this CTA's ring, whether this role claims and
+    // publishes (the leader's producer), ring entries taken, the next claim
+    uint32_t tq_slots = 0, tq_bars = 0;
+    bool fetcher = false;
+    int q = 0, claimed = 0;
+    bool started = false;
+    const GemmParams *pp = nullptr;
+    volatile int *abort_flag = nullptr;
+    uint32_t peer_abort = 0;
     __device__ WorkIter(const GemmParams &p, int pair, int num_pairs)
     {
         sk = p.streamk != 0;
+        dyn = !sk && p.dyn_tiles != 0;
         KB = p.num_k_blocks;
         MB = p.num_m_blocks;
         ntiles = p.num_tiles;
@@ -150,8 +182,73 @@ struct WorkIter {
         v = V * g / G;
         v_end = V * (g + 1) / G;
     }
+    // Dynamic whole tiles: the ring and this role's part in it.
+    __device__ void attach(const GemmParams &p, uint32_t slots, uint32_t bars, bool claims, volatile int *abort,
+                           uint32_t peer)
+    {
+        pp = &p;
+        tq_slots = slots;
+        tq_bars = bars;
+        fetcher = claims;
+        abort_flag = abort;
+        peer_abort = peer;
+    }
+    // The fetcher, once per tile, at its first load: claim the pair's next
+    // tile (the atomic's result is first used by publish()).
+    __device__ void claim(unsigned *ctr)
+    {
+        claimed = step + static_cast<int>(atomicAdd(ctr, 1u));
+    }
+    // The fetcher, once per tile after claim(): hand the claimed tile to the
+    // pair's other roles (ring entry q).
+    __device__ void publish()
+    {
+        const uint32_t slot = tq_slots + 4u * static_cast<uint32_t>(q % PAIR_TQ);
+        const uint32_t bar = tq_bars + 8u * static_cast<uint32_t>(q % PAIR_TQ);
+        ++q;
+        st_shared_u32(slot, static_cast<uint32_t>(claimed));
+        mbar_arrive(bar);
+        mbar_arrive_expect_tx_cluster_relaxed(mapa_shared(bar, 1u), 4u);
+        st_async_u32(mapa_shared(slot, 1u), static_cast<uint32_t>(claimed), mapa_shared(bar, 1u));
+        if (claimed >= ntiles)
+            finish_claims();
+    }
+    // The fetcher, exactly once: this pair claims nothing more (see claims_done).
+    bool claims_over = false;
+    __device__ void finish_claims()
+    {
+        if (dyn && fetcher && !claims_over) {
+            claims_over = true;
+            claims_done(pp->tile_ctl, static_cast<unsigned>(step));
+        }
+    }
     __device__ bool next(Seg &s)
     {
+        if (dyn) {
+            int t = tile;  // the first tile: the pair's own index
+            if (started) {
+                if (fetcher) {
+                    t = claimed;  // published during the previous tile
+                } else {
+                    const uint32_t slot = tq_slots + 4u * static_cast<uint32_t>(q % PAIR_TQ);
+                    const uint32_t bar = tq_bars + 8u * static_cast<uint32_t>(q % PAIR_TQ);
+                    const uint32_t parity = static_cast<uint32_t>(q / PAIR_TQ) & 1u;
+                    ++q;
+                    if (!wait_bar(bar, parity, abort_flag, *pp, ERR_TILE_QUEUE, peer_abort))
+                        return false;
+                    t = static_cast<int>(ld_shared_u32(slot));
+                }
+            }
+            if (!started && fetcher && t >= ntiles)
+                finish_claims();  // no tile at all (not planned: the grid has at most one pair per tile)
+            started = true;
+            if (t < 0 || t >= ntiles)  // past the last tile: the end (an index is never below 0)
+                return false;
+            s.tile = t;
+            s.kb0 = 0;
+            s.kb1 = KB;
+            return true;
+        }
         if (!sk) {
             if (tile >= ntiles)
                 return false;
@@ -576,8 +673,10 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     const uint32_t drain_bar = bar0 + 8u * (2 * PAIR_STAGES + 2 * PAIR_ACC_BUFS);
     const uint32_t skw_bar = drain_bar + 8u;  // the epilogue warps finished writing a partial
     const uint32_t skc_bar = skw_bar + 8u;    // chunk c of a contributor's partial landed: skc_bar + 8c
+    const uint32_t tq_bar = skc_bar + 8u * PAIR_SKC_CHUNKS;  // ring entry in slot i published: tq_bar + 8i
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const uint32_t tq_slots = smem_u32(tmem_slot + 4);  // PAIR_TQ claimed tile indices
 #define FULL_BAR(s) (bar0 + 8u * (s))
 #define EMPTY_BAR(s) (bar0 + 8u * (PAIR_STAGES + (s)))
 #define TFULL_BAR(b) (bar0 + 8u * (2 * PAIR_STAGES + (b)))
@@ -607,6 +706,10 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
         mbar_init(skw_bar, pair_epi_warps<EPI>());
         for (int c = 0; c < PAIR_SKC_CHUNKS; ++c)
             mbar_init(skc_bar + 8u * c, 1);
+        for (int i = 0; i < PAIR_TQ; ++i) {
+            mbar_init(tq_bar + 8u * i, 1);       // one arrival per entry (the leader's producer)
+            st_shared_u32(tq_slots + 4u * i, 0x7fffffffu);  // an unwritten slot reads as the end
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -638,7 +741,9 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                 armed[s] = 0;
             bool ok = true, first = true;
             WorkIter it(p, pair, num_pairs);
+            it.attach(p, tq_slots, tq_bar, leader, abort_flag, peer_abort);
             for (Seg g; ok && it.next(g);) {
+                const int claim_kb = g.kb0, publish_kb = max(g.kb0, g.kb1 - 2);
                 int mb, nbt;  // M block, batch-major N block
                 tile_coords(p, g.tile, mb, nbt);
                 const int bz = nbt / p.num_n_blocks;       // batch (0 unless batched)
@@ -648,6 +753,12 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                 const int arow = mb * PAIR_M + static_cast<int>(rank) * BM;
                 const int brow = nb * tn + static_cast<int>(rank) * (tn / 2);
                 for (int kb = g.kb0; kb < g.kb1; ++kb) {
+                    if (it.dyn && leader) {
+                        if (kb == claim_kb)
+                            it.claim(p.tile_ctl);
+                        if (kb == publish_kb)
+                            it.publish();
+                    }
                     if (!wait_bar(EMPTY_BAR(stage), phase ^ 1u, abort_flag, p, ERR_PRODUCER, peer_abort)) {
                         ok = false;
                         break;
@@ -697,6 +808,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                     }
                 }
             }
+            it.finish_claims();  // if the loop ended early (an abort); once only
             if (leader)
                 for (int s = 0; s < PAIR_STAGES; ++s)
                     if (armed[s])
@@ -710,6 +822,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             WorkIter it(p, pair, num_pairs);
+            it.attach(p, tq_slots, tq_bar, false, abort_flag, peer_abort);
             for (Seg g; ok && it.next(g);) {
                 if (!wait_bar(TEMPTY_BAR(acc), acc_phase ^ 1u, abort_flag, p, ERR_MMA_ACC, peer_abort))
                     break;
@@ -767,6 +880,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
         uint32_t acc_phase = 0;
         uint32_t skw_phase = 0;
         WorkIter it(p, pair, num_pairs);
+        it.attach(p, tq_slots, tq_bar, false, abort_flag, peer_abort);
         for (Seg g; it.next(g);) {
             int mb, nbt;  // M block, batch-major N block
             tile_coords(p, g.tile, mb, nbt);

@@ -28,6 +28,7 @@ constexpr int ERR_DRAIN = 0x105;      // copies / MMAs did not finish while unwi
 constexpr int ERR_SK_FLAG = 0x106;    // a stream-K partial never arrived
 constexpr int ERR_SK_SLOT = 0x107;    // a CTA's own partial write did not complete
 constexpr int ERR_SK_COPY = 0x109;    // the copy of a partial into shared memory did not land
+constexpr int ERR_TILE_QUEUE = 0x10A; // a claimed tile index never reached this role
 
 // Record `code` (first writer wins), raise this CTA's abort flag and, in a
 // CTA pair, the peer's (peer_abort: its shared::cluster address, 0 if none).
@@ -176,6 +177,22 @@ __device__ __forceinline__ void epi_write_partial(uint32_t taddr, float *slot, i
             __stcg(s4 + (c / 4 + i) * BM + row,
                    make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+    }
+}
+
+// Claimed whole tiles (GemmParams::tile_ctl): called once per pair, by the
+// pair's claiming thread, when its claiming is over (its last claim went past
+// the last tile, or it is aborting).  The count is a release: the pair's
+// claims precede it; the pair that completes it (an acquire) has seen every
+// claim and zeroes the counter and the count for the next launch.  This runs
+// while the pairs still compute their last tiles, off the launch's tail.
+__device__ __forceinline__ void claims_done(unsigned *ctl, unsigned pairs)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctl + 1) : "memory");
+    if (old == pairs - 1u) {
+        asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(ctl) : "memory");
+        asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(ctl + 1) : "memory");
     }
 }
 

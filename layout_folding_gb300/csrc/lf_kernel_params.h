@@ -44,6 +44,12 @@ struct GemmParams {
     unsigned epoch;             // value the flags of this launch carry
     float *sk_partials;         // [2 * pairs][128 * 256] fp32 partial accumulators
     unsigned *sk_flags;         // [2 * pairs] = epoch once the slot is written
+    // pair kernel, whole tiles: 1 = pair i starts with tile i and claims every
+    // further tile from tile_ctl[0] (tile order as for band_m).  tile_ctl[1]
+    // counts the pairs whose claiming is over; the pair that completes the
+    // count zeroes both words, so every launch finds them zero.
+    int dyn_tiles;
+    unsigned *tile_ctl;
     // one-pass cross-entropy with gradient (pair kernel): groups of op_Q pairs
     // each hold one 256-row M block (two op_tile-column tiles per pair) per round.
     float *loss;                      // [M]

@@ -56,6 +56,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
@@ -87,6 +99,26 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// 4-byte asynchronous store into the shared memory of the other CTA of the
+// cluster (addr, bar: its shared::cluster addresses); the store completes as
+// 4 transaction bytes on that CTA's mbarrier, so a thread that sees the
+// barrier's phase complete sees the value -- no release fence on this side.
+__device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+                 "r"(bar)
+                 : "memory");
+}
+
+// Arrive on an mbarrier of any CTA of the cluster and raise its expected
+// transaction bytes, without release semantics (the data it stands for
+// arrives as transaction bytes).
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster_relaxed(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned *p)

@@ -87,16 +87,19 @@ def _gemm_bound(got, ref, what):
     (3, 768, 5120, 13824),    # the projection shape, stream-K as planned
     (4, 33, 1032, 264),       # swapped operands (transposed store), skinny X
     (4, 1, 4096, 4096),       # swapped, a single row
-], ids=["cta1", "pair", "streamk", "streamk_projection", "swapped", "swapped_m1"])
+    (5, 1800, 20488, 72),     # CTA pairs, whole tiles claimed at run time, ragged
+], ids=["cta1", "pair", "streamk", "streamk_projection", "swapped", "swapped_m1", "pair_claimed"])
 def test_gemm_nt_writes_only_its_output(variant, M, N, K):
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
     out = Guarded((M, N), torch.bfloat16, salt=variant)
-    lf.set_tuning(-1, variant)
+    lf.set_tuning(-1, 2 if variant == 5 else variant)
+    lf.set_tile_schedule(1 if variant == 5 else -1)
     try:
         lf.gemm_nt(x.to(DEV), w.to(DEV), out.t)
         lf.check_device_error()
     finally:
         lf.set_tuning(-1, -1)
+        lf.set_tile_schedule(-1)
     out.check("gemm_nt variant %d %dx%dx%d" % (variant, M, N, K))
     rows = np.unique(np.array([0, M // 3, M // 2, M - 1]))
     _gemm_bound(f64(out.t)[rows], oracle.gemm_nt_rows(x, w, rows), "gemm_nt")

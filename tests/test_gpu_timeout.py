@@ -19,14 +19,18 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3], ids=["cta1", "pair", "pair_streamk"])
+@pytest.mark.parametrize("variant", [1, 2, 3, 5], ids=["cta1", "pair", "pair_streamk", "pair_claimed"])
 def test_stalled_wait_times_out_and_context_survives(variant):
+    # pair_claimed: whole tiles claimed at run time, enough tiles (256) that
+    # the other pairs go on claiming while the stalled pair unwinds; the
+    # launch's last CTA still resets the tile counter, so the next call is right
     torch.cuda.set_device(0)
-    M, N, K = 256, 1024, 512
+    M, N, K = (1024, 16384, 512) if variant == 5 else (256, 1024, 512)
     x, w = synthetic.make_gemm_inputs(M, N, K, 1.0, 1.0 / math.sqrt(K))
     xd, wd = x.to(DEV), w.to(DEV)
     lf.check_device_error()                      # start from a clean error word
-    lf.set_tuning(-1, variant)
+    lf.set_tuning(-1, 2 if variant == 5 else variant)
+    lf.set_tile_schedule(1 if variant == 5 else -1)
     lf.set_test_hooks(True, 200_000_000)         # 200 ms limit per wait
     try:
         lf.gemm_nt(xd, wd)
@@ -43,6 +47,7 @@ def test_stalled_wait_times_out_and_context_survives(variant):
         lf.check_device_error()
     finally:
         lf.set_tuning(-1, -1)
+        lf.set_tile_schedule(-1)
     ref = oracle.gemm_nt(x, w)
     got = out.float().cpu().double().numpy()
     assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
