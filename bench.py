@@ -191,8 +191,15 @@ class Timer:
         """Returns per-step ms; if `counter` is given, also the number of
         library launches inside the timed steps."""
         torch = self.torch
-        for _ in range(warmup):
-            fn()
+        # warm-up steps are the timed steps without events: the flush buffers'
+        # first use (page mapping) then falls outside the timed region
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
+                if flush:
+                    self.flush_buf.fill_(1.0)
+                    torch.sum(self.clean_buf, dim=0, out=self.clean_out)
+                torch.cuda._sleep(LAUNCH_SHADOW_CYCLES)
+                fn()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
