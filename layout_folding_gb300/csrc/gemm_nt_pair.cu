@@ -48,6 +48,11 @@ namespace {
 
 constexpr int PAIR_M = 2 * BM;          // 256 rows of X per pair tile
 constexpr int PAIR_UMMA_K = 16;
+// The operand ring: PAIR_STAGES slots of one K block each, grouped into
+// stages of p.ksub consecutive slots (six stages of one K block, or three of
+// two: one wait, eight MMAs and one commit per stage; the cross-entropy
+// epilogues' whole-tile launches run 3-8 % faster so, the plain store and the
+// stream-K split slower).
 constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_A_BYTES = BM * BK * 2;          // 16 KiB: this CTA's 128 rows of X
 constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;    // 16 KiB: this CTA's 128 rows of W
@@ -658,7 +663,7 @@ __device__ __forceinline__ void pair_xent_exp(const GemmParams &p, const CUtenso
     }
 }
 
-template <int EPI, int LAYOUT>
+template <int EPI, int LAYOUT, int KSUB = 1>
 __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     k_gemm_nt_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, const GemmParams p)
@@ -691,7 +696,9 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     // the MMA's N: BN, or for the swapped-operand store the caller's M rounded up to 16
     const int tn = (EPI == EPI_STORE_T && p.tile_n > 0) ? p.tile_n : BN;
     // bytes both CTAs' copies of one K slice bring: A 128 rows, B tn / 2 rows each
-    const uint32_t stage_tx = 2u * (PAIR_A_BYTES + static_cast<uint32_t>(tn / 2) * BK * 2u);
+    const uint32_t stage_tx = 2u * (PAIR_A_BYTES + static_cast<uint32_t>(tn / 2) * BK * 2u);  // per K block
+    constexpr int ksub = KSUB;  // K blocks per ring stage
+    constexpr int nstages = PAIR_STAGES / KSUB;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < PAIR_STAGES; ++s) {
@@ -752,11 +759,12 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                 const int wz = p.w_batched ? bz : 0;
                 const int arow = mb * PAIR_M + static_cast<int>(rank) * BM;
                 const int brow = nb * tn + static_cast<int>(rank) * (tn / 2);
-                for (int kb = g.kb0; kb < g.kb1; ++kb) {
+                for (int kbs = g.kb0; kbs < g.kb1; kbs += ksub) {
+                    const int nsub = KSUB == 1 ? 1 : min(KSUB, g.kb1 - kbs);  // K blocks in this stage
                     if (it.dyn && leader) {
-                        if (kb == claim_kb)
+                        if (kbs == claim_kb)
                             it.claim(p.tile_ctl);
-                        if (kb == publish_kb)
+                        if (publish_kb >= kbs && publish_kb < kbs + nsub)
                             it.publish();
                     }
                     if (!wait_bar(EMPTY_BAR(stage), phase ^ 1u, abort_flag, p, ERR_PRODUCER, peer_abort)) {
@@ -770,10 +778,16 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                     first = false;
                     if (!skip) {
                         if (leader) {
-                            mbar_arrive_expect_tx(FULL_BAR(stage), stage_tx);
+                            mbar_arrive_expect_tx(FULL_BAR(stage), stage_tx * static_cast<uint32_t>(nsub));
                             ++armed[stage];
                         }
-                        const uint32_t a_dst = sA + stage * PAIR_A_BYTES, b_dst = sB + stage * PAIR_B_BYTES;
+#pragma unroll
+                        for (int j = 0; j < KSUB; ++j) {
+                        if (j >= nsub)
+                            break;
+                        const int kb = kbs + j;
+                        const uint32_t slot = static_cast<uint32_t>(stage * ksub + j);
+                        const uint32_t a_dst = sA + slot * PAIR_A_BYTES, b_dst = sB + slot * PAIR_B_BYTES;
                         if (LAYOUT & 4) {  // batched: the batch is the maps' third coordinate
                             if (LAYOUT & 1) {
                                 tma_load_3d_pair(a_dst, &tmA, arow, kb * BK, xz, full_leader);
@@ -801,8 +815,9 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                                 tma_load_2d_pair(b_dst, &tmB, kb * BK, brow, full_leader);
                             }
                         }
+                        }  // the stage's K blocks
                     }
-                    if (++stage == PAIR_STAGES) {
+                    if (++stage == nstages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -810,7 +825,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
             }
             it.finish_claims();  // if the loop ended early (an abort); once only
             if (leader)
-                for (int s = 0; s < PAIR_STAGES; ++s)
+                for (int s = 0; s < nstages; ++s)
                     if (armed[s])
                         wait_bar_drain(FULL_BAR(s), (armed[s] - 1u) & 1u, abort_flag, p, peer_abort);
         }
@@ -828,26 +843,33 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = g.kb0; kb < g.kb1; ++kb) {
+                for (int kbs = g.kb0; kbs < g.kb1; kbs += ksub) {
+                    const int nsub = KSUB == 1 ? 1 : min(KSUB, g.kb1 - kbs);
                     if (!wait_bar(FULL_BAR(stage), phase, abort_flag, p, ERR_MMA_FULL, peer_abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = sA + stage * PAIR_A_BYTES;
-                    const uint32_t b0 = sB + stage * PAIR_B_BYTES;
                     const uint32_t idesc =
                         idesc_bf16_f32_major(PAIR_M, static_cast<uint32_t>(tn), (LAYOUT & 1) != 0, (LAYOUT & 2) != 0);
 #pragma unroll
-                    for (int k = 0; k < BK / PAIR_UMMA_K; ++k) {
-                        const uint64_t da = (LAYOUT & 1) ? smem_desc_mn128(a0 + k * PAIR_MN_KSTEP, PAIR_MN_HALF)
-                                                         : smem_desc_k128(a0 + k * PAIR_UMMA_K * 2);
-                        const uint64_t db = (LAYOUT & 2) ? smem_desc_mn128(b0 + k * PAIR_MN_KSTEP, PAIR_MN_HALF)
-                                                         : smem_desc_k128(b0 + k * PAIR_UMMA_K * 2);
-                        umma_f16_pair(d_tmem, da, db, idesc, (kb != g.kb0 || k != 0) ? 1u : 0u);
+                    for (int j = 0; j < KSUB; ++j) {
+                        if (j >= nsub)
+                            break;
+                        const uint32_t slot = static_cast<uint32_t>(stage * ksub + j);
+                        const uint32_t a0 = sA + slot * PAIR_A_BYTES;
+                        const uint32_t b0 = sB + slot * PAIR_B_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / PAIR_UMMA_K; ++k) {
+                            const uint64_t da = (LAYOUT & 1) ? smem_desc_mn128(a0 + k * PAIR_MN_KSTEP, PAIR_MN_HALF)
+                                                             : smem_desc_k128(a0 + k * PAIR_UMMA_K * 2);
+                            const uint64_t db = (LAYOUT & 2) ? smem_desc_mn128(b0 + k * PAIR_MN_KSTEP, PAIR_MN_HALF)
+                                                             : smem_desc_k128(b0 + k * PAIR_UMMA_K * 2);
+                            umma_f16_pair(d_tmem, da, db, idesc, (kbs != g.kb0 || j != 0 || k != 0) ? 1u : 0u);
+                        }
                     }
-                    umma_commit_pair_mc(EMPTY_BAR(stage), 0x3);  // both CTAs may refill this slot
-                    if (++stage == PAIR_STAGES) {
+                    umma_commit_pair_mc(EMPTY_BAR(stage), 0x3);  // both CTAs may refill this stage
+                    if (++stage == nstages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -1058,7 +1080,7 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t s, cudaLaunchAttribute *at
 
 // The dynamic shared-memory opt-in is a per-device function attribute: set it
 // once per device and kernel instead of on every launch.
-template <int EPI, int LAYOUT>
+template <int EPI, int LAYOUT, int KSUB>
 cudaError_t set_smem_attr_once()
 {
     static std::atomic<unsigned long long> done{0};
@@ -1069,23 +1091,35 @@ cudaError_t set_smem_attr_once()
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load() & bit)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(k_gemm_nt_pair<EPI, LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_gemm_nt_pair<EPI, LAYOUT, KSUB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              pair_smem_bytes<EPI>());
     if (e == cudaSuccess)
         done.fetch_or(bit);
     return e;
 }
 
-template <int EPI, int LAYOUT>
-cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to, const GemmParams &p,
+template <int EPI, int LAYOUT, int KSUB = 1>
+cudaError_t launch_pair_k(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to, const GemmParams &p,
                           int grid, cudaStream_t s)
 {
-    cudaError_t e = set_smem_attr_once<EPI, LAYOUT>();
+    cudaError_t e = set_smem_attr_once<EPI, LAYOUT, KSUB>();
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config<EPI>(grid, s, attr, p.streamk != 0 && cooperative_launches());
-    return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI, LAYOUT>, ta, tb, to, p);
+    return cudaLaunchKernelEx(&cfg, k_gemm_nt_pair<EPI, LAYOUT, KSUB>, ta, tb, to, p);
+}
+
+// The cross-entropy partial and exp epilogues have a two-K-block-stage form
+// (p.ksub == 2, whole tiles); every other launch uses one-K-block stages.
+template <int EPI, int LAYOUT>
+cudaError_t launch_pair_t(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &to, const GemmParams &p,
+                          int grid, cudaStream_t s)
+{
+    if constexpr (EPI == EPI_XENT_PARTIAL || EPI == EPI_XENT_EXP)
+        if (p.ksub == 2)
+            return launch_pair_k<EPI, LAYOUT, 2>(ta, tb, to, p, grid, s);
+    return launch_pair_k<EPI, LAYOUT, 1>(ta, tb, to, p, grid, s);
 }
 
 }  // namespace

@@ -68,6 +68,9 @@ struct GemmParams {
     // pair kernel, EPI_STORE, EPI_XENT_GRAD and EPI_XENT_EXP: 1 = the output
     // tensor map is valid and the epilogue writes through TMA stores, 0 = plain stores
     int tma_store;
+    // pair kernel: K blocks per stage of the operand ring (1 or 2; the ring's
+    // six one-K-block slots grouped into six or three stages)
+    int ksub;
     // pair kernel, whole tiles: the tile order walks bands of band_m M blocks
     // (M block fastest within a band, then the N blocks, then the next band);
     // 0 = one band of all M blocks
