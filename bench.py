@@ -792,8 +792,8 @@ def main(argv=None):
                     help="launch the stream-K and one-pass kernels without the cooperative attribute (for ncu, "
                          "which cannot replay cooperative cluster launches); same kernels")
     ap.add_argument("--tile-schedule", choices=["auto", "fixed", "claimed"], default="auto",
-                    help="whole tiles on CTA pairs: the automatic choice, the fixed assignment or tiles claimed at "
-                         "run time (for comparisons; results are identical)")
+                    help="whole tiles on CTA pairs: the automatic choice (fixed), the fixed assignment or tiles "
+                         "claimed at run time (for comparisons; results are identical)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -440,11 +440,10 @@ void lf_set_tile_band(int m_blocks);
  * 0 = fixed (pair i takes tiles i, i + pairs, ...); 1 = claimed at run time
  * (pair i starts with tile i, then each pair claims the next unclaimed tile
  * in the tile order from a counter in the library's workspace, so the pairs
- * that share a W tile start it together and faster pairs take more tiles);
- * a negative value restores the automatic choice (claimed from 64 waves of
- * tiles with K >= 2048 on: long launches, where the fixed assignment's pairs
- * drift apart).  Each tile is computed by one pair either way:
- * results do not depend on it.
+ * that share a W tile start it together and faster pairs -- for instance
+ * while other work holds some SMs -- take more tiles); a negative value
+ * restores the automatic choice, the fixed assignment.  Each tile is computed
+ * by one pair either way: results do not depend on it.
  */
 void lf_set_tile_schedule(int mode);
 

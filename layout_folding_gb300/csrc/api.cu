@@ -57,16 +57,15 @@ std::atomic<int> g_variant{-1};      // -1 auto, 1 single-CTA, 2 CTA-pair whole 
 std::atomic<int> g_op_tile{0};       // one-pass cross-entropy N-tile width; 0 = automatic
 std::atomic<int> g_xent_path{0};     // cross-entropy gradient: 0 auto, 1 one pass, 2 exp + rescale, 3 recompute
 std::atomic<int> g_band{-1};         // whole-tile band height in M blocks: -1 auto, 0 one band, > 0 forced
-std::atomic<int> g_tile_sched{-1};   // whole tiles on pairs: -1 auto, 0 fixed assignment, 1 claimed at run time
-// Whole tiles on CTA pairs are claimed at run time from this many waves of
-// tiles of at least this many K blocks on.  The fixed assignment's drift
-// grows with the launch (pairs' last tile starts 1.5 tiles apart at 27 waves,
-// 8.5 tiles at 211), while a claim and its hand-over cost every tile a little
-// (1.5-2 % at 13-27 waves of 64 K blocks; 6 % on tiles of 16 K blocks).
-// Measured per launch at 211 waves (8192 x 128256 x 4096, loss only):
-// 4.42 ms claimed, 4.59-4.63 ms fixed, DRAM reads 2.2 GB against 6.8-9.0 GB.
-constexpr long long DYN_MIN_WAVES = 64;
-constexpr int DYN_MIN_KBLOCKS = 32;
+// Whole tiles on pairs: -1 automatic (the fixed assignment), 0 fixed, 1 claimed
+// at run time.  Claiming won while the cross-entropy launches ran one-K-block
+// ring stages (8192 x 128256 x 4096 loss: 4.42 ms claimed, 4.59-4.92 ms fixed,
+// whose pairs drifted apart and re-read W: 6.8-12.6 GB against 2.2 GB); with
+// their two-K-block stages the fixed assignment keeps its pairs together (2.20
+// GB, 4.16 ms against 4.19 ms claimed), and for the plain store at the same
+// size claiming is slower (4.47 vs 4.33 ms).  Claimed tiles remain an option:
+// they balance the load by themselves when other work holds some SMs.
+std::atomic<int> g_tile_sched{-1};
 std::atomic<int> g_coop_enable{1};   // 0: launch the CTA-waiting kernels without the cooperative attribute
 // L2 bytes of X a band of whole tiles may keep while it sweeps W (the L2 is
 // 129 MB, but reuse measured as if about half of it were available)
@@ -490,16 +489,7 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
             }
         }
         p.band_m = band < MB ? band : 0;
-        // Claimed tiles: over a long launch pairs drift apart by several
-        // tiles (4.6 ms at 8192 x 128256 x 4096: 184 us between the pairs'
-        // last tile starts), the pairs that share a W tile stop running side
-        // by side and the last pairs finish late; claiming each next tile in
-        // tile order keeps both tight.
-        const int sched = g_tile_sched.load();
-        p.dyn_tiles = (sched == 1 || (sched < 0 && p.num_tiles >= DYN_MIN_WAVES * d->pair_clusters &&
-                                      p.num_k_blocks >= DYN_MIN_KBLOCKS))
-                          ? 1
-                          : 0;
+        p.dyn_tiles = g_tile_sched.load() == 1 ? 1 : 0;  // claimed tiles on request
     }
     return LF_OK;
 }
