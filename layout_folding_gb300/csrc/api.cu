@@ -295,6 +295,24 @@ bool make_tmap(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, uint32_
 
 // 2-D bf16 tensor stored [K, rows] (rows contiguous: an MN-major operand),
 // box = 64 rows x 64 K, 128-byte swizzle; out-of-range elements read as zero.
+// The same [K, rows] operand viewed as (64 rows, K, rows / 64): one box of
+// (64, BK, 2) brings two consecutive 64-row halves, in the order two boxes of
+// make_tmap_mn would (each half's 64 K rows of 128 bytes, then the next half).
+// Needs rows to be a multiple of 64.
+bool make_tmap_mn3(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows % 64 != 0)
+        return false;
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(rows) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(lf::BK), 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_mn(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
 {
     EncodeTiledFn enc = encode_fn();
@@ -361,6 +379,11 @@ struct GemmPlan {
     int layout = 0;  // bit 0: X stored [K,M]; bit 1: W stored [K,N] (pair kernel only)
     DeviceState *dev = nullptr;
     CUtensorMap ta, tb;
+    // MN-major operands of the pair kernel: the 3-D views (make_tmap_mn3), valid
+    // for the operands whose bit is set in p.mn3; the pair kernel reads both
+    // 64-row halves of a CTA's rows with one copy through them (W stored [K,N],
+    // 4096^3: 89.7 -> 87.7 us; both operands MN-major 97.9 -> 91.8 us)
+    CUtensorMap ta3, tb3;
     CUtensorMap to;  // output map of the pair kernel's TMA-store epilogue (set by run_gemm)
     lf::GemmParams p;
     int grid = 0;
@@ -390,6 +413,7 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
         return LF_ERR_LAUNCH;
     const int tile_m = g->pair ? 2 * lf::BM : lf::BM;
     bool ok_a, ok_b;
+    int mn3 = 0;  // which operands also have the pair kernel's 3-D MN-major view
     if (bs) {
         // an operand with batch stride 0 (or a batch of 1) is one matrix: a map
         // whose batch extent is 1, read at batch coordinate 0
@@ -402,6 +426,8 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
         ok_b = (layout & 2) ? make_tmap3(&g->tb, w, N, K, bs->ldw, wb, sw, 64)
                             : make_tmap3(&g->tb, w, K, N, bs->ldw, wb, sw, lf::BN / 2);
     } else {
+        mn3 = (g->pair && (layout & 1) && make_tmap_mn3(&g->ta3, x, M, K) ? 1 : 0) |
+              (g->pair && (layout & 2) && make_tmap_mn3(&g->tb3, w, N, K) ? 2 : 0);
         ok_a = (layout & 1) ? make_tmap_mn(&g->ta, x, M, K) : make_tmap(&g->ta, x, M, K, lf::BM);
         const uint32_t b_rows = tile_n ? static_cast<uint32_t>(tile_n / 2) : (g->pair ? lf::BN / 2 : lf::BN);
         ok_b = (layout & 2) ? make_tmap_mn(&g->tb, w, N, K) : make_tmap(&g->tb, w, N, K, b_rows);
@@ -427,6 +453,7 @@ lf_status plan_gemm(DeviceState *d, const void *x, const void *w, int64_t M, int
         return LF_ERR_SHAPE;
     p.num_tiles = static_cast<int>(p.num_m_blocks * p.num_n_blocks * batch);
     p.err = d->err_word;
+    p.mn3 = mn3;
     p.timeout_ns = g_timeout_ns.load();
     p.inject = g_inject.load();
     const int pf = g_l2_prefetch.load();
@@ -518,7 +545,9 @@ cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
     }
     if (!g.pair)
         return lf::launch_gemm_nt(epi, g.ta, g.tb, g.p, g.grid, stream);
-    cudaError_t e = lf::launch_gemm_nt_pair(epi, g.layout, g.ta, g.tb, g.to, g.p, g.grid, stream);
+    const CUtensorMap &ta = (g.p.mn3 & 1) ? g.ta3 : g.ta;
+    const CUtensorMap &tb = (g.p.mn3 & 2) ? g.tb3 : g.tb;
+    cudaError_t e = lf::launch_gemm_nt_pair(epi, g.layout, ta, tb, g.to, g.p, g.grid, stream);
     if (e != cudaSuccess && g.p.streamk) {
         // The stream-K split is launched cooperatively (its tile owners wait for
         // other CTAs).  If the runtime refuses that, run whole tiles, which have
@@ -529,7 +558,7 @@ cudaError_t run_gemm(int epi, GemmPlan &g, cudaStream_t stream)
         g.p.ksub = (epi == lf::EPI_XENT_PARTIAL || epi == lf::EPI_XENT_EXP) ? 2 : 1;
         g.grid = 2 * (g.p.num_tiles < g.dev->pair_clusters ? g.p.num_tiles : g.dev->pair_clusters);
         g_last_plan.store((g_last_plan.load() & ~((0xfffffull) | (1ull << 23))) | static_cast<uint64_t>(g.grid));
-        e = lf::launch_gemm_nt_pair(epi, g.layout, g.ta, g.tb, g.to, g.p, g.grid, stream);
+        e = lf::launch_gemm_nt_pair(epi, g.layout, ta, tb, g.to, g.p, g.grid, stream);
         if (e == cudaSuccess)
             g.dev->coop.store(-1);
     }

@@ -802,13 +802,17 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                                 tma_load_3d_pair(b_dst, &tmB, kb * BK, brow, wz, full_leader);
                             }
                         } else {
-                            if (LAYOUT & 1) {
+                            if ((LAYOUT & 1) && (p.mn3 & 1)) {  // both 64-row halves in one copy
+                                tma_load_3d_pair(a_dst, &tmA, 0, kb * BK, arow / 64, full_leader);
+                            } else if (LAYOUT & 1) {
                                 tma_load_2d_pair(a_dst, &tmA, arow, kb * BK, full_leader);
                                 tma_load_2d_pair(a_dst + PAIR_MN_HALF, &tmA, arow + 64, kb * BK, full_leader);
                             } else {
                                 tma_load_2d_pair(a_dst, &tmA, kb * BK, arow, full_leader);
                             }
-                            if (LAYOUT & 2) {
+                            if ((LAYOUT & 2) && (p.mn3 & 2)) {
+                                tma_load_3d_pair(b_dst, &tmB, 0, kb * BK, brow / 64, full_leader);
+                            } else if (LAYOUT & 2) {
                                 tma_load_2d_pair(b_dst, &tmB, brow, kb * BK, full_leader);
                                 tma_load_2d_pair(b_dst + PAIR_MN_HALF, &tmB, brow + 64, kb * BK, full_leader);
                             } else {

@@ -71,6 +71,10 @@ struct GemmParams {
     // pair kernel: K blocks per stage of the operand ring (1 or 2; the ring's
     // six one-K-block slots grouped into six or three stages)
     int ksub;
+    // pair kernel, MN-major operands (not batched): bit 0 / bit 1 = X's / W's
+    // map is the 3-D view (64 rows, K, rows / 64) whose box brings both 64-row
+    // halves of the CTA's 128 rows in one copy
+    int mn3;
     // pair kernel, whole tiles: the tile order walks bands of band_m M blocks
     // (M block fastest within a band, then the N blocks, then the next band);
     // 0 = one band of all M blocks
