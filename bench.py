@@ -48,8 +48,7 @@ L2_FLUSH_BYTES = 256 << 20
 LAUNCH_SHADOW_CYCLES = 200_000   # ~0.1 ms of device-side delay before each timed step
 # the files the headline kernel's device code is compiled from (host-only declarations excluded)
 KERNEL_SOURCES = ["layout_folding_gb300/csrc/gemm_nt_pair.cu", "layout_folding_gb300/csrc/lf_gemm_common.cuh",
-                  "layout_folding_gb300/csrc/lf_ptx.cuh", "layout_folding_gb300/csrc/lf_kernel_params.h",
-                  "layout_folding_gb300/csrc/lf_xent_rescale.cuh"]
+                  "layout_folding_gb300/csrc/lf_ptx.cuh", "layout_folding_gb300/csrc/lf_kernel_params.h"]
 # source files whose hash a recorded DRAM figure is tied to, per kernel
 TRAFFIC_SOURCES = {
     "k_gemm_nt_pair<EPI_STORE>": KERNEL_SOURCES,

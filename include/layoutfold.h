@@ -378,19 +378,6 @@ uint64_t lf_launch_count(void);
 void lf_last_gemm_plan(int *grid, int *cta_pairs, int *stream_k, int *tile_n);
 
 /*
- * The rescale units of the last gemm_nt_xent / gemm_nt_xent_layout call in
- * this process that took the exp pass and the rescale pass on the current
- * device (a unit: one row and 32 consecutive 256-column tiles of it): *taken
- * = how many of them the GEMM's epilogue warps rescaled (0 when the overlap
- * was off, lf_set_xent_overlap), *total = all of the call's units (0 before
- * the first such call).  Synchronises `stream` (the call's stream) first, then
- * reads the count the GEMM's last CTA left in the library's workspace, so it
- * must come before the next such call.  LF_ERR_NULL if a pointer is NULL,
- * LF_ERR_LAUNCH if the stream or the copy fails.  Meant for tests and tuning.
- */
-lf_status lf_last_xent_overlap(cudaStream_t stream, long long *taken, long long *total);
-
-/*
  * Sets up the current device if needed and reports its SM count and how many
  * CTA pairs of the pair GEMM kernel can be resident at once (either pointer
  * may be NULL).  LF_ERR_ARCH on a device that is not sm_103.
@@ -430,31 +417,13 @@ void lf_set_onepass_tile(int width);
  * fits the resident pairs (else as 0), 2 = the exp pass and the rescale pass
  * (a GEMM whose epilogue writes the tile partials and fp16 exp(z - tile max)
  * into grad, then one kernel that merges each row's partials into lse and
- * loss and rewrites grad in place as bf16), 3 = partials, combine and a second
+ * loss and rewrites grad in place as bf16; the recompute form when a row has
+ * more than 49,152 tiles of 256 columns), 3 = partials, combine and a second
  * GEMM pass that recomputes the logits to write the gradient; anything else =
  * automatic (the exp pass and the rescale pass unless a one-pass tile width is
  * forced).  The single-CTA kernel always uses the recompute form.
  */
 void lf_set_xent_grad_path(int path);
-
-/*
- * The exp pass and the rescale pass of lf_set_xent_grad_path(2), applied to
- * later calls: 1 = overlapped -- the GEMM's whole tiles walk at least two
- * bands of row blocks (lf_set_tile_band; two when it is automatic and would
- * give one), and its epilogue warps, between tiles, rescale the rows of every
- * band whose tiles are all finished, except the last band, while the later
- * bands' MMAs run; the rescale kernel then does only the rows the GEMM did
- * not take.  No step of it waits for another CTA, so it holds whether or not
- * all of the GEMM's CTAs are resident.  0 = the rescale kernel does every
- * row.  A negative value restores the automatic choice, 0: on a GB300 the
- * overlapped call takes as long (the exp pass is power-limited, and the
- * rescale's memory traffic inside it lowers its clock as much as it saves
- * afterwards).  Each row is rescaled once by the same arithmetic either way:
- * results do not depend on it.  Source: "Allow reductions in matmul
- * epilogues", the follow-up on reducing a row across output tiles (a row's
- * log-sum-exp is final once all of its tiles are).
- */
-void lf_set_xent_overlap(int mode);
 
 /*
  * Order of whole output tiles on CTA pairs, applied to later launches: bands

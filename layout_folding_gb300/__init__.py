@@ -90,10 +90,6 @@ def lib():
         L.lf_set_xent_grad_path.restype = None
         L.lf_set_tile_band.argtypes = [I32]
         L.lf_set_tile_band.restype = None
-        L.lf_set_xent_overlap.argtypes = [I32]
-        L.lf_set_xent_overlap.restype = None
-        L.lf_last_xent_overlap.argtypes = [P, ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)]
-        L.lf_last_xent_overlap.restype = I32
         L.lf_set_tile_schedule.argtypes = [I32]
         L.lf_set_tile_schedule.restype = None
         L.lf_set_cooperative.argtypes = [I32]
@@ -431,21 +427,6 @@ def set_xent_grad_path(path: int = 0):
     """Gradient form of the cross-entropy on CTA pairs: 1 = one pass, 2 = exp
     pass + rescale, 3 = recompute pass, 0 = automatic."""
     lib().lf_set_xent_grad_path(int(path))
-
-
-def set_xent_overlap(on=None):
-    """Cross-entropy gradient by the exp pass: rescale finished bands' rows
-    inside the GEMM while later bands compute (True), all rows in the rescale
-    kernel (False), or the automatic choice (None: False)."""
-    lib().lf_set_xent_overlap(-1 if on is None else (1 if on else 0))
-
-
-def last_xent_overlap(stream=None):
-    """(units the GEMM rescaled, all units) of the last exp-pass gradient call
-    on the current device; synchronises the call's stream first."""
-    taken, total = ctypes.c_longlong(0), ctypes.c_longlong(0)
-    _check(lib().lf_last_xent_overlap(_stream(stream), ctypes.byref(taken), ctypes.byref(total)), "lf_last_xent_overlap")
-    return taken.value, total.value
 
 
 def set_tile_band(m_blocks: int = -1):

@@ -25,9 +25,7 @@ struct DeviceState {
                               // the per-CTA stash of a tile's exp values (128 x 256 fp32 per CTA)
     unsigned sk_epoch = 0;    // last epoch handed to a launch whose CTAs wait on flags
     int *err_word = nullptr;  // device int[64]; [0] = first error code
-    // words 0..1: claimed whole tiles (GemmParams::tile_ctl); 4..: the overlapped
-    // rescale (GemmParams::rs_ctl); zeroed once, each launch leaves them zero
-    unsigned *tile_ctl = nullptr;
+    unsigned *tile_ctl = nullptr;  // claimed whole tiles: counter and count (GemmParams::tile_ctl), zeroed once
     void *ws = nullptr;       // cross-entropy workspace (grow-only)
     size_t ws_bytes = 0;
     // Ordering of the calls that use the workspaces above (WorkspaceOrder).
@@ -69,25 +67,11 @@ std::atomic<int> g_band{-1};         // whole-tile band height in M blocks: -1 a
 // they balance the load by themselves when other work holds some SMs.
 std::atomic<int> g_tile_sched{-1};
 std::atomic<int> g_coop_enable{1};   // 0: launch the CTA-waiting kernels without the cooperative attribute
-// Cross-entropy gradient by the exp pass: 1 = the GEMM's epilogue warps
-// rescale the rows of finished bands while later bands' MMAs run (the tiles
-// then walk at least two bands), 0 = the rescale kernel does every row, -1 =
-// automatic: 0.  The overlap runs as designed (4096 x 32768 x 4096: all 8,192
-// units of the first band taken while the second band's MMAs run, 8.5 us per
-// unit, the MMA issuer never waiting for an accumulator), but the exp pass is
-// power-limited (SM clock ~1750 MHz) and the rescale's HBM traffic inside it
-// costs clock (~1700 MHz) and operand latency: the GEMM takes 586 us instead
-// of 554, the rescale kernel 44 us instead of 80 -- the same 0.64 ms call.
-std::atomic<int> g_xent_overlap{-1};
-// the last exp-pass call (lf_last_xent_overlap): its units, the bands the GEMM could take units from
-std::atomic<long long> g_rs_total{0};
-std::atomic<int> g_rs_bands{0};
-// the device's control words: claimed whole tiles at 0..1, the overlapped rescale from RS_CTL_OFF on
-constexpr int RS_CTL_OFF = 4;
-constexpr int TILE_CTL_WORDS = RS_CTL_OFF + lf::RS_CTL_WORDS;
 // L2 bytes of X a band of whole tiles may keep while it sweeps W (the L2 is
 // 129 MB, but reuse measured as if about half of it were available)
 constexpr double BAND_X_BYTES = 32.0 * 1024 * 1024;
+// the rescale kernel keeps one scale per 256-column tile of a row in shared memory
+constexpr int64_t RESCALE_MAX_TILES = 48 * 1024;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -133,8 +117,8 @@ lf_status current_device(DeviceState **out)
             d.pair_clusters = lf::gemm_pair_max_active_clusters();
             if (cudaMalloc(&d.err_word, 64 * sizeof(int)) != cudaSuccess ||
                 cudaMemset(d.err_word, 0, 64 * sizeof(int)) != cudaSuccess ||
-                cudaMalloc(&d.tile_ctl, TILE_CTL_WORDS * sizeof(unsigned)) != cudaSuccess ||
-                cudaMemset(d.tile_ctl, 0, TILE_CTL_WORDS * sizeof(unsigned)) != cudaSuccess ||
+                cudaMalloc(&d.tile_ctl, 64 * sizeof(unsigned)) != cudaSuccess ||
+                cudaMemset(d.tile_ctl, 0, 64 * sizeof(unsigned)) != cudaSuccess ||
                 cudaEventCreateWithFlags(&d.ws_event, cudaEventDisableTiming) != cudaSuccess ||
                 cudaDeviceSynchronize() != cudaSuccess) {
                 cudaGetLastError();
@@ -817,10 +801,11 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
     // Which gradient form: the exp pass + rescale (a GEMM writing fp16
     // exp(z - tile max) into grad, then one bandwidth-bound pass) -- the
     // automatic choice --, the one-pass kernel (on request, or when a
-    // one-pass tile width is forced), or the recompute pass (single-CTA tiles).
+    // one-pass tile width is forced), or the recompute pass (single-CTA tiles,
+    // or rows too wide for the rescale kernel's shared memory).
     const int path = g_xent_path.load();
     const int forced = g_op_tile.load();
-    const bool exp_ok = grad_or_null && g.pair;
+    const bool exp_ok = grad_or_null && g.pair && p.num_n_blocks <= RESCALE_MAX_TILES;
     const bool try_onepass = grad_or_null && g.pair && d->coop.load() >= 0 && !g.no_flags &&
                              (path == 1 || (path == 0 && (!exp_ok || forced != 0)));
     // One pass, when a whole 256-row block of tiles (two per pair) fits on the
@@ -890,35 +875,10 @@ lf_status xent_impl(const void *x, bool x_mn, const void *w, bool w_mn, const in
         // exp pass: partials and e = fp16(exp(z - tile max)) into grad, then
         // the rescale kernel: lse, loss, and grad rewritten in place as bf16
         p.out = grad_or_null;
-        p.loss = loss;
-        p.rs_units = 0;
-        p.rs_ctl = nullptr;
-        if (g_xent_overlap.load() == 1 && g.pair && !p.streamk) {
-            // Overlap the rescale with the GEMM: the tiles walk bands of M
-            // blocks (two, unless a band height is set or chosen for L2), the
-            // epilogue warps rescale the rows of every finished band but the
-            // last while the rest computes, the rescale kernel the remainder.
-            const int MB = p.num_m_blocks;
-            if (p.band_m == 0 && g_band.load() < 0 && MB >= 2)
-                p.band_m = (MB + 1) / 2;
-            const int nbands = p.band_m > 0 ? (MB + p.band_m - 1) / p.band_m : 1;
-            const long long units = static_cast<long long>(nbands - 1) * p.band_m * 2 * lf::BM *
-                                    lf::rs_units_per_row(p.num_n_blocks);
-            if (nbands >= 2 && nbands <= lf::RS_MAX_BANDS && units < (1ll << 30)) {
-                p.rs_units = static_cast<int>(units);
-                p.rs_ctl = d->tile_ctl + RS_CTL_OFF;
-            }
-        }
-        const int rs_bands = p.rs_units > 0 ? (p.num_m_blocks + p.band_m - 1) / p.band_m - 1 : 0;
-        const long long per_band = rs_bands > 0 ? p.rs_units / rs_bands : 0;
-        g_rs_total.store(static_cast<long long>(p.M) * lf::rs_units_per_row(p.num_n_blocks));
-        g_rs_bands.store(rs_bands);
         if ((st = launched(run_gemm(lf::EPI_XENT_EXP, g, stream), 1)) != LF_OK)
             return st;
         return launched(lf::launch_xent_rescale(p.part_max, p.part_sum, p.label_logit, labels, p.M, p.N,
-                                                p.num_n_blocks, loss, grad_or_null,
-                                                rs_bands > 0 ? p.rs_ctl + lf::RS_CTL_DONE : nullptr, per_band,
-                                                rs_bands, stream),
+                                                p.num_n_blocks, loss, grad_or_null, stream),
                         1);
     }
     if ((st = launched(run_gemm(lf::EPI_XENT_PARTIAL, g, stream), 1)) != LF_OK)
@@ -1052,31 +1012,6 @@ uint64_t lf_launch_count(void) { return g_launches.load(); }
 
 int lf_last_device_wait_code(void) { return g_last_wait_code.load(); }
 
-lf_status lf_last_xent_overlap(cudaStream_t stream, long long *taken, long long *total)
-{
-    if (!taken || !total)
-        return LF_ERR_NULL;
-    *taken = 0;
-    *total = g_rs_total.load();
-    const int bands = g_rs_bands.load();
-    if (bands <= 0)
-        return LF_OK;
-    DeviceState *d = nullptr;
-    lf_status st = current_device(&d);
-    if (st != LF_OK)
-        return st;
-    unsigned v[lf::RS_MAX_BANDS] = {};
-    if (cudaStreamSynchronize(stream) != cudaSuccess ||
-        cudaMemcpy(v, d->tile_ctl + RS_CTL_OFF + lf::RS_CTL_DONE, bands * sizeof(unsigned),
-                   cudaMemcpyDeviceToHost) != cudaSuccess) {
-        cudaGetLastError();
-        return LF_ERR_LAUNCH;
-    }
-    for (int b = 0; b < bands; ++b)
-        *taken += v[b];
-    return LF_OK;
-}
-
 void lf_last_gemm_plan(int *grid, int *cta_pairs, int *stream_k, int *tile_n)
 {
     const uint64_t v = g_last_plan.load();
@@ -1112,8 +1047,6 @@ void lf_set_tuning(int l2_prefetch_kblocks, int gemm_variant)
 void lf_set_xent_grad_path(int path) { g_xent_path.store(path >= 1 && path <= 3 ? path : 0); }
 
 void lf_set_tile_band(int m_blocks) { g_band.store(m_blocks < 0 ? -1 : m_blocks); }
-
-void lf_set_xent_overlap(int mode) { g_xent_overlap.store(mode < 0 ? -1 : (mode != 0 ? 1 : 0)); }
 
 void lf_set_tile_schedule(int mode) { g_tile_sched.store(mode < 0 ? -1 : (mode ? 1 : 0)); }
 

@@ -42,7 +42,6 @@
 #include <cuda_fp16.h>
 
 #include "lf_gemm_common.cuh"
-#include "lf_xent_rescale.cuh"
 
 namespace lf {
 namespace {
@@ -664,96 +663,6 @@ __device__ __forceinline__ void pair_xent_exp(const GemmParams &p, const CUtenso
     }
 }
 
-// The gradient's rescale overlapped with the exp pass (p.rs_units > 0; whole
-// tiles walking bands of p.band_m M blocks, so a band's rows are final once
-// its tiles are: "Allow reductions in matmul epilogues", the follow-up's row
-// reduction across tiles, done for one band while the next one's MMAs run).
-// No step waits for another CTA: a unit is taken only if its band is
-// complete, and whatever the launch did not take is left to the follow-up
-// rescale kernel, so the protocol holds whether or not all CTAs are resident.
-//
-// After a tile's exp epilogue, each epilogue warp counts its part of the tile
-// for the tile's band (not for the last band, whose rows the follow-up kernel
-// rescales): its TMA stores written (not only read out of shared memory),
-// its partials written, then a fence and the count.
-__device__ __forceinline__ void rs_tile_done(const GemmParams &p, int mb)
-{
-    const int band = mb / p.band_m;
-    const int nbands = (p.num_m_blocks + p.band_m - 1) / p.band_m;
-    if (band >= nbands - 1)
-        return;
-    const int lane = threadIdx.x & 31;
-    if (lane == 0 && p.tma_store) {
-        bulk_wait_group_all();
-        fence_proxy_async_global();
-    }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0)
-        atomicAdd(p.rs_ctl + RS_CTL_TILES + band, 1u);
-}
-
-// One unit of the overlapped rescale, if one is free.  Lane 0 advances
-// `ready` over the bands whose tile count is complete (an acquire), then
-// claims from the first band not known to be used up: a fetch-and-add on the
-// band's claim word, whose results below the band's unit count are its units,
-// each handed out once (a compare-and-swap on one word would let one claim
-// through per L2 round trip -- about 0.2 us -- for all warps together); a
-// result past the count marks the band used up for this warp.  False if no
-// unit was free.
-__device__ __forceinline__ bool rs_take_unit(const GemmParams &p, const RescaleArgs &ra, int &ready, int &cur)
-{
-    const int lane = threadIdx.x & 31;
-    const int nbands = (p.num_m_blocks + p.band_m - 1) / p.band_m;
-    const int upr = rs_units_per_row(p.num_n_blocks);
-    const unsigned per_band = static_cast<unsigned>(p.band_m * PAIR_M * upr);
-    int u = -1;
-    if (lane == 0) {
-        const unsigned full = static_cast<unsigned>(p.band_m * (p.num_tiles / p.num_m_blocks) * 2 *
-                                                    pair_epi_warps<EPI_XENT_EXP>());
-        while (ready < nbands - 1 && ld_acquire_gpu(p.rs_ctl + RS_CTL_TILES + ready) >= full)
-            ++ready;
-        while (cur < ready) {
-            const unsigned k = atomicAdd(p.rs_ctl + RS_CTL_CLAIMS + cur, 1u);
-            if (k < per_band) {
-                u = cur * static_cast<int>(per_band) + static_cast<int>(k);
-                break;
-            }
-            ++cur;
-        }
-    }
-    u = __shfl_sync(0xffffffffu, u, 0);
-    if (u < 0)
-        return false;
-    xent_rescale_unit(ra, u / upr, u % upr);
-    return true;
-}
-
-// At the CTA's end (one thread, after the CTA's last unit): the CTA that
-// completes the count has seen every claim; it publishes, per band, how many
-// units the launch did (each claim below the count was done by its claimer)
-// for the follow-up kernel, and zeroes the other words for the next launch.
-__device__ __forceinline__ void rs_cta_done(const GemmParams &p)
-{
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                 : "=r"(old)
-                 : "l"(p.rs_ctl + RS_CTL_EXITED)
-                 : "memory");
-    if (old != gridDim.x - 1u)
-        return;
-    const int nbands = (p.num_m_blocks + p.band_m - 1) / p.band_m;
-    const unsigned per_band =
-        static_cast<unsigned>(p.band_m * PAIR_M * rs_units_per_row(p.num_n_blocks));
-    for (int b = 0; b < nbands - 1; ++b) {
-        const unsigned c = ld_relaxed_gpu(p.rs_ctl + RS_CTL_CLAIMS + b);
-        st_relaxed_gpu(p.rs_ctl + RS_CTL_DONE + b, c < per_band ? c : per_band);
-        st_relaxed_gpu(p.rs_ctl + RS_CTL_CLAIMS + b, 0u);
-        st_relaxed_gpu(p.rs_ctl + RS_CTL_TILES + b, 0u);
-    }
-    st_relaxed_gpu(p.rs_ctl + RS_CTL_EXITED, 0u);
-}
-
 template <int EPI, int LAYOUT, int KSUB = 1>
 __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     k_gemm_nt_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -998,12 +907,6 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
         uint32_t skw_phase = 0;
         WorkIter it(p, pair, num_pairs);
         it.attach(p, tq_slots, tq_bar, false, abort_flag, peer_abort);
-        const bool rs = EPI == EPI_XENT_EXP && p.rs_units > 0;
-        const RescaleArgs ra = {p.part_max, p.part_sum,  p.label_logit, p.labels,
-                                p.M,        p.N,         p.num_n_blocks, p.loss,
-                                static_cast<uint4 *>(p.out)};
-        int rs_ready = 0, rs_cur = 0;  // lane 0: leading bands known complete, known used up
-        bool ended = true; // the loop below ran out of tiles (no abort)
         for (Seg g; it.next(g);) {
             int mb, nbt;  // M block, batch-major N block
             tile_coords(p, g.tile, mb, nbt);
@@ -1043,23 +946,10 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                     pa.count = 0;
                 }
             }
-            if (rs) {
-                // while this tile's MMAs run: units of finished bands
-                for (;;) {
-                    int go = 0;
-                    if (lane == 0)
-                        go = !mbar_test_wait(TFULL_BAR(acc), acc_phase) && !*abort_flag;
-                    if (!__shfl_sync(0xffffffffu, go, 0) || !rs_take_unit(p, ra, rs_ready, rs_cur))
-                        break;
-                }
-            }
             const bool ok = wait_bar(TFULL_BAR(acc), acc_phase, abort_flag, p, ERR_EPI, peer_abort);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ended = false;
+            if (!__all_sync(0xffffffffu, ok))
                 break;
-            }
             tc_fence_after();
-            bool counted = false;  // the tile's exp epilogue ran (rs: count it for its band)
             if (g.kb0 != 0) {
                 // Not the tile's first K blocks: hand the partial sum to the
                 // pair that owns the tile's start.
@@ -1123,42 +1013,26 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
                             epi_xent_partial(p, taddr, row, nb, pa);
                         else if (EPI == EPI_XENT_ROW)
                             epi_xent_row(p, taddr, row, pa);
-                        else if (EPI == EPI_XENT_EXP) {
+                        else if (EPI == EPI_XENT_EXP)
                             pair_xent_exp(p, &tmO, taddr, row - lane, nb, pa,
                                           gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES,
                                           base + static_cast<uint32_t>(PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES));
-                            counted = true;
-                        }
                         else
                             pair_xent_grad(p, &tmO, taddr, row - lane, nb, pa,
                                            gbase + PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES,
                                            base + static_cast<uint32_t>(PAIR_STG_OFF + (warp - 2) * PAIR_STG_WARP_BYTES));
                     }
                 }
-                if (!done) {
-                    ended = false;
+                if (!done)
                     break;
-                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_cluster(mapa_shared(TEMPTY_BAR(acc), 0u));
-            if (rs && counted)
-                rs_tile_done(p, mb);  // after the accumulator is handed back
             if (++acc == PAIR_ACC_BUFS) {
                 acc = 0;
                 acc_phase ^= 1u;
-            }
-        }
-        if (rs && ended) {
-            // no tile left: the units of every band already finished
-            for (;;) {
-                int go = 0;
-                if (lane == 0)
-                    go = !*abort_flag;
-                if (!__shfl_sync(0xffffffffu, go, 0) || !rs_take_unit(p, ra, rs_ready, rs_cur))
-                    break;
             }
         }
     }
@@ -1176,8 +1050,6 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (EPI == EPI_XENT_EXP && p.rs_units > 0 && threadIdx.x == 0)
-        rs_cta_done(p);  // every warp of this CTA is past its last unit
     cluster_sync();  // the peer no longer touches this CTA's barriers, smem or TMEM
     if (warp == 1) {
         tc_fence_after();

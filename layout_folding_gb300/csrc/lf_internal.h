@@ -45,15 +45,13 @@ cudaError_t launch_xent_combine(const float *part_max, const float *part_sum, co
                                 const int32_t *labels, int M, int N, int num_n_blocks, float *loss,
                                 float *row_max, float *row_logsum, cudaStream_t s);
 
-// Second pass of the cross-entropy gradient after EPI_XENT_EXP, per unit (a
-// row's 32-tile segment): the combine (lse from the tile partials, loss), then
-// grad rewritten in place from the fp16 e = exp(z - tile max) it holds: grad =
-// bf16_rn(e * exp(tile max - lse)), the label column from the fp32 label logit.
-// Every unit but, with band_done (device words), the first band_done[b] units
-// of each band b < rs_bands of units_per_band units, which the GEMM did.
+// Second pass of the cross-entropy gradient after EPI_XENT_EXP: per row, the
+// combine (lse from the tile partials, loss), then grad rewritten in place
+// from the fp16 e = exp(z - tile max) it holds: grad = bf16_rn(e * exp(tile
+// max - lse)), the label column from the fp32 label logit.
 cudaError_t launch_xent_rescale(const float *part_max, const float *part_sum, const float *label_logit,
                                 const int32_t *labels, int M, int N, int num_n_blocks, float *loss, void *grad,
-                                const unsigned *band_done, long long units_per_band, int rs_bands, cudaStream_t s);
+                                cudaStream_t s);
 
 cudaError_t launch_matmul_k1_f32(const float *a, const float *b, float *out, int64_t M, int64_t N,
                                  int num_sms, cudaStream_t s);

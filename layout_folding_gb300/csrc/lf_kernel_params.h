@@ -79,34 +79,7 @@ struct GemmParams {
     // (M block fastest within a band, then the N blocks, then the next band);
     // 0 = one band of all M blocks
     int band_m;
-    // pair kernel, EPI_XENT_EXP, whole tiles in two or more bands: the
-    // epilogue warps rescale the gradient's rows (xent_rescale_unit) of every
-    // band whose tiles are all finished, except the last band, while later
-    // bands' MMAs run.  rs_units: the units of those bands (rows x units per
-    // row; 0 = off).  rs_ctl (words of the tile_ctl block, RS_CTL_* below):
-    // per band, the epilogue warps that finished one of its tiles, the units
-    // claimed (a fetch-and-add; past the band's units a claim is void), and
-    // the units done, published by the launch's last CTA (which zeroes the
-    // other words) for the follow-up rescale kernel; and the CTAs finished.
-    int rs_units;
-    unsigned *rs_ctl;
 };
-
-// A unit of the gradient's rescale: one row and RS_SEG_TILES consecutive
-// 256-column tiles of it (units numbered row-major).
-constexpr int RS_SEG_TILES = 32;
-__host__ __device__ constexpr int rs_units_per_row(int num_n_blocks)
-{
-    return (num_n_blocks + RS_SEG_TILES - 1) / RS_SEG_TILES;
-}
-
-// The rs_ctl words (above), band b < RS_MAX_BANDS.
-constexpr int RS_MAX_BANDS = 32;
-constexpr int RS_CTL_EXITED = 0;                       // CTAs past their last unit
-constexpr int RS_CTL_TILES = 8;                        // + b: warps done with a tile of band b
-constexpr int RS_CTL_CLAIMS = RS_CTL_TILES + RS_MAX_BANDS;   // + b: units of band b claimed
-constexpr int RS_CTL_DONE = RS_CTL_CLAIMS + RS_MAX_BANDS;    // + b: units of band b the launch did
-constexpr int RS_CTL_WORDS = RS_CTL_DONE + RS_MAX_BANDS;
 
 // One stream-K partial slot: a CTA's 128 rows x 256 columns of fp32,
 // stored as [column / 4][row][4] so each warp access is contiguous.

@@ -18,7 +18,6 @@
 #include <math_constants.h>
 
 #include "lf_internal.h"
-#include "lf_xent_rescale.cuh"
 
 namespace lf {
 namespace {
@@ -128,29 +127,133 @@ __global__ void __launch_bounds__(256) k_xent_combine(const float *__restrict__ 
 // Second pass of the cross-entropy gradient after the GEMM's exp epilogue
 // ("Allow reductions in matmul epilogues": the row's log-sum-exp is a
 // reduction across the row's output tiles, merged here, and the gradient
-// reuses it; the arithmetic is xent_rescale_unit's, lf_xent_rescale.cuh).
-// Every unit the GEMM did not take: with band_done, the first band_done[b]
-// units of each of the first rs_bands bands (per_band units each) were
-// rescaled inside the GEMM and are skipped.  Eight warps per CTA, each taking
-// every (warps in the grid)-th unit, so the loads of many units are in flight
-// on every SM.
+// reuses it).  One CTA per row:
+//   1. the combine: m = max_j m_j, s = sum_j s_j exp(m_j - m), lse = m + log s,
+//      loss = lse - z[label] (NaN for a label outside [0, N));
+//   2. per 256-column tile j: scale_j = exp(m_j - lse) into shared memory;
+//   3. the row of grad, which holds e = fp16(exp(z - m_j)), is rewritten in
+//      place, 8 columns (16 bytes) per load and store:
+//        grad = bf16_rn(e * scale_j),
+//      except the label column, computed from the fp32 label logit:
+//        grad[label] = bf16_rn(exp(z[label] - lse) - 1).
+// Error: fp16 keeps e to 2^-11 relative, so a non-label entry p < 1/2 is off by
+// at most p 2^-11 (+ 1e-6) before its bf16 rounding (<= 9.8e-4 below 1/2): under
+// 1.3e-3 in all; an entry p >= 1/2 is the row's (hence its tile's) maximum,
+// where e = 1 exactly, so only its bf16 rounding remains.  The label entry is
+// computed as in the single-pass epilogues.
 constexpr int RESCALE_THREADS = 256;
-constexpr int RESCALE_MAX_CTAS = 4096;
 
-__global__ void __launch_bounds__(RESCALE_THREADS) k_xent_rescale(const RescaleArgs a,
-                                                                  const unsigned *__restrict__ band_done,
-                                                                  long long per_band, int rs_bands, long long total)
+__device__ __forceinline__ float ex2_approx_pw(float x)
 {
-    const long long warps = static_cast<long long>(gridDim.x) * (RESCALE_THREADS / 32);
-    const int upr = rs_units_per_row(a.NB);
-    for (long long u = static_cast<long long>(blockIdx.x) * (RESCALE_THREADS / 32) + (threadIdx.x >> 5); u < total;
-         u += warps) {
-        if (band_done) {
-            const long long b = u / per_band;
-            if (b < rs_bands && u - b * per_band < static_cast<long long>(__ldcg(band_done + b)))
-                continue;  // done inside the GEMM
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t rescale_pair(uint32_t hpair, float scale)
+{
+    const __half2 h = *reinterpret_cast<const __half2 *>(&hpair);
+    const float2 f = __half22float2(h);
+    __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__global__ void __launch_bounds__(RESCALE_THREADS) k_xent_rescale(const float *__restrict__ part_max,
+                                                                  const float *__restrict__ part_sum,
+                                                                  const float *__restrict__ label_logit,
+                                                                  const int32_t *__restrict__ labels, int M, int N,
+                                                                  int NB, float *__restrict__ loss,
+                                                                  uint4 *__restrict__ grad)
+{
+    extern __shared__ float scale[];  // [NB]
+    __shared__ float red[RESCALE_THREADS / 32];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int row = blockIdx.x; row < M; row += gridDim.x) {
+        const float *pm = part_max + static_cast<size_t>(row) * NB;
+        const float *ps = part_sum + static_cast<size_t>(row) * NB;
+        // 1. the row's max and rescaled sum over its tiles
+        float m = -CUDART_INF_F;
+        for (int j = tid; j < NB; j += RESCALE_THREADS)
+            m = fmaxf(m, pm[j]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0)
+            red[warp] = m;
+        __syncthreads();
+        m = red[0];
+#pragma unroll
+        for (int w = 1; w < RESCALE_THREADS / 32; ++w)
+            m = fmaxf(m, red[w]);
+        __syncthreads();
+        float s = 0.f;
+        for (int j = tid; j < NB; j += RESCALE_THREADS)
+            s += ps[j] * exp2f((pm[j] - m) * LOG2E);
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0)
+            red[warp] = s;
+        __syncthreads();
+        s = 0.f;
+#pragma unroll
+        for (int w = 0; w < RESCALE_THREADS / 32; ++w)
+            s += red[w];
+        const float ls = logf(s);
+        const float lse = m + ls;
+        const int lab = labels[row];
+        const bool lab_ok = lab >= 0 && lab < N;
+        const float zl = lab_ok ? label_logit[row] : 0.f;
+        if (tid == 0)
+            loss[row] = lab_ok ? (m - zl) + ls : CUDART_NAN_F;
+        // 2. per-tile scales exp(m_j - lse)
+        const float lsel = lse * LOG2E;
+        for (int j = tid; j < NB; j += RESCALE_THREADS)
+            scale[j] = ex2_approx_pw(fmaf(pm[j], LOG2E, -lsel));
+        __syncthreads();
+        // 3. the row, 8 columns per step; the label column from the fp32 logit
+        const float g_lab = ex2_approx_pw(fmaf(zl, LOG2E, -lsel)) - 1.f;
+        uint4 *rowp = grad + static_cast<size_t>(row) * (N / 8);
+        const int nv = N / 8;
+        const int lab_v = lab_ok ? lab >> 3 : -1;
+        constexpr int U = 4;
+        for (int v0 = tid; v0 < nv; v0 += U * RESCALE_THREADS) {
+            uint4 q[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * RESCALE_THREADS;
+                if (v < nv)
+                    q[u] = __ldcs(rowp + v);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * RESCALE_THREADS;
+                if (v < nv) {
+                    const float sc = scale[v >> 5];  // 256 columns = 32 vectors per tile
+                    uint4 o;
+                    o.x = rescale_pair(q[u].x, sc);
+                    o.y = rescale_pair(q[u].y, sc);
+                    o.z = rescale_pair(q[u].z, sc);
+                    o.w = rescale_pair(q[u].w, sc);
+                    if (v == lab_v) {  // column lab & 7 of the 8: half (lab & 1) of word (lab & 7) >> 1
+                        const uint32_t gb = __bfloat16_as_ushort(__float2bfloat16_rn(g_lab));
+                        const int wsel = (lab & 7) >> 1;
+                        const bool hi = (lab & 1) != 0;
+                        const auto patch = [&](uint32_t &word, int w) {
+                            if (w == wsel)
+                                word = hi ? ((word & 0xFFFFu) | (gb << 16)) : ((word & 0xFFFF0000u) | gb);
+                        };
+                        patch(o.x, 0);
+                        patch(o.y, 1);
+                        patch(o.z, 2);
+                        patch(o.w, 3);
+                    }
+                    __stcs(rowp + v, o);
+                }
+            }
         }
-        xent_rescale_unit(a, static_cast<int>(u / upr), static_cast<int>(u % upr));
+        __syncthreads();  // scale[] and red[] are rewritten for the next row
     }
 }
 
@@ -225,15 +328,18 @@ cudaError_t launch_xent_combine(const float *part_max, const float *part_sum, co
 
 cudaError_t launch_xent_rescale(const float *part_max, const float *part_sum, const float *label_logit,
                                 const int32_t *labels, int M, int N, int num_n_blocks, float *loss, void *grad,
-                                const unsigned *band_done, long long units_per_band, int rs_bands, cudaStream_t s)
+                                cudaStream_t s)
 {
-    const RescaleArgs a = {part_max, part_sum, label_logit, labels, M, N, num_n_blocks, loss,
-                           static_cast<uint4 *>(grad)};
-    const long long total = static_cast<long long>(M) * rs_units_per_row(num_n_blocks);
-    const long long need = (total + RESCALE_THREADS / 32 - 1) / (RESCALE_THREADS / 32);
-    const int grid = static_cast<int>(need < RESCALE_MAX_CTAS ? need : RESCALE_MAX_CTAS);
-    k_xent_rescale<<<grid, RESCALE_THREADS, 0, s>>>(a, band_done, units_per_band > 0 ? units_per_band : 1,
-                                                     rs_bands, total);
+    const size_t smem = static_cast<size_t>(num_n_blocks) * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_xent_rescale, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess)
+            return e;
+    }
+    const int grid = M < (1 << 30) ? M : (1 << 30);
+    k_xent_rescale<<<grid, RESCALE_THREADS, smem, s>>>(part_max, part_sum, label_logit, labels, M, N, num_n_blocks,
+                                                       loss, static_cast<uint4 *>(grad));
     return cudaGetLastError();
 }
 

@@ -660,13 +660,12 @@ def test_xent_whole_row_in_one_tile(M, N, K, variant):
 
 
 
-@pytest.mark.parametrize("N,launches", [(20000 * 256, 2), (49153 * 256, 2)], ids=["20000_tiles", "49153_tiles"])
+@pytest.mark.parametrize("N,launches", [(20000 * 256, 2), (49153 * 256, 3)], ids=["80KiB_scales", "past_limit"])
 def test_xent_gradient_very_wide_rows(N, launches):
-    """Rows of 20,000 and 49,153 tiles of 256 columns (625 and 1,537 rescale
-    units per row, the last one partial): the exp pass and the rescale kernel,
-    whose warps keep one tile scale per lane and need no shared memory per
-    row, so no row is too wide for it.  M = 130 (CTA pairs), K = 8; sampled
-    rows, every column, against the oracle."""
+    """Rows so wide that the rescale kernel keeps 20,000 tile scales (80 KiB)
+    in shared memory -- past the 48 KiB default, so the launch opts in to more;
+    and one tile past its 49,152-tile limit, where the recompute form runs.
+    M = 130 (CTA pairs), K = 8; sampled rows, every column, against the oracle."""
     M, K = 130, 8
     x = synthetic.bf16_normal((M, K), 1.0, 91)
     w = synthetic.bf16_normal((N, K), 1.0 / math.sqrt(K), 92)
